@@ -1,0 +1,447 @@
+#!/usr/bin/env python3
+"""Benchmark of the block-scaled FP8 weight GEMM (libbsf8) on one GB300 per rank.
+
+Workload (the wo_a decode layer of the page "recipes/docker-images/mia-tp4/adapter/
+wo_a_w8.py"): G = 2 groups of W[1024, 4096] as e4m3 twins with 32x32 exponents, M = 6
+token rows, split_k = 8 summed in a fixed order, 43 distinct seeded weight copies (one
+per layer) cycled so the L2 is cold.  One step = the 43 layer calls of one decode step,
+captured once in a CUDA graph and replayed.  Inputs are seeded synthetic tensors (there
+is no model checkpoint here).
+
+Prints ONE JSON line on rank 0.  `value` is the weight-stream bandwidth (e4m3 codes +
+exponent bytes per call / time per call) summed over all ranks; `e2e` is the same metric
+measured through the public Python API with the activations copied from pinned host
+memory and the outputs copied back inside the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl bsf8|reference]
+
+`--impl reference` times the CPU oracle (oracle/, a plain C restatement of the pages)
+on a bounded sample of the same workload: the baseline this library is compared with.
+Multi-GPU runs (torchrun, one rank per GPU) are independent replicas: the op has no
+exchange step, so no collective runs on the data path; only the timing is combined
+(max over ranks) and the bytes summed.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "weight-stream HBM GB/s (frac of GB300 peak) and us/call at M=6, L2 cold"
+LAYERS = 43
+KERNEL_SOURCES = ("block_scaled_fp8_weight_gb300/csrc/bsf8_gemm.cu",
+                  "block_scaled_fp8_weight_gb300/csrc/bsf8_device.cuh")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_wo_a_m6_dram_traffic.txt")
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", choices=("bsf8", "reference"), default="bsf8")
+    p.add_argument("--e2e-steps", type=int, default=2000)
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="CPU time budget of the oracle baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, device_is_cuda):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group("nccl" if device_is_cuda else "gloo")
+    return dist
+
+
+def barrier(dist, device):
+    if dist is None:
+        return
+    import torch
+    if device.type == "cuda":
+        dist.barrier(device_ids=[device.index])
+    else:
+        dist.barrier()
+
+
+def aggregate(dist, elapsed_s: float, units: float, device):
+    """Replicas: the job's time is the slowest rank's, its work the sum of all ranks'."""
+    if dist is None:
+        return elapsed_s, units
+    import torch
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ------------------------------------------------------------------ environment
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel source (else None)."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    vals = {}
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256_16") != kernel_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons every 100 ms in the background."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []   # (t, sm_mhz, max_mhz, reasons)
+        self._stop = threading.Event()
+        self._thr = None
+
+    def _poll(self):
+        while not self._stop.is_set():
+            try:
+                out = subprocess.run(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                      "--format=csv,noheader,nounits"], capture_output=True,
+                                     text=True, timeout=5).stdout.strip()
+                f = [x.strip() for x in out.split(",")]
+                reasons = []
+                for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                      "sw_power_cap"), f[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.append(name)
+                self.samples.append((time.time(), float(f[1]), float(f[2]), reasons))
+            except Exception:
+                pass
+            self._stop.wait(0.1)
+
+    def start(self):
+        self._thr = threading.Thread(target=self._poll, daemon=True)
+        self._thr.start()
+
+    def stop(self):
+        self._stop.set()
+        if self._thr:
+            self._thr.join(timeout=10)
+
+    def summary(self, t0, t1):
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        window = "timed region"
+        if not inside:
+            inside = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
+            window = "nearest samples to a timed region shorter than the sampling period"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = sorted({r for s in inside for r in s[3]})
+        return {"sm_mhz": statistics.median(s[1] for s in inside),
+                "sm_max_mhz": max(s[2] for s in inside), "reasons": reasons,
+                "samples": len(inside), "window": window}
+
+
+# ------------------------------------------------------------------ workload
+
+def workload():
+    from block_scaled_fp8_weight_gb300 import workloads as wl
+    return wl.WO_A
+
+
+def config_dict(wk, pdl=True):
+    return {
+        "workload": f"wo_a decode step: G={wk.G} x W[{wk.N},{wk.K}] e4m3 + 32x32 ue8m0 exponents, "
+                    f"M={wk.M}, split_k={wk.split_k}, {LAYERS} distinct layer copies per step",
+        "G": wk.G, "N": wk.N, "K": wk.K, "M": wk.M, "split_k": wk.split_k, "layers": LAYERS,
+        "l2": f"inputs larger than L2: {LAYERS} weight copies x {wk.weight_bytes / 1e6:.2f} MB "
+              f"= {LAYERS * wk.weight_bytes / 1e6:.0f} MB streamed per step (L2 129 MB)",
+        "launch": "one CUDA graph per step" + (", programmatic dependent launch" if pdl else ""),
+    }
+
+
+def cpu_oracle_baseline(wk, seconds: float):
+    """The oracle, as it stands, on one host core: whole wo_a layer calls at M=6."""
+    import oracle
+    w8, ex = wk.weights(copy=0)
+    x = wk.x(copy=0)
+    oracle.gemm(x, w8, ex)                       # load + first touch
+    calls, t0 = 0, time.perf_counter()
+    while True:
+        oracle.gemm(x, w8, ex)
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": wk.weight_bytes * calls / el / 1e9, "unit": "GB/s", "cores": 1,
+            "kind": "oracle", "us_per_call": el / calls * 1e6,
+            "sample": f"{calls} whole wo_a layer calls (G=2, N=1024, K=4096, M=6), "
+                      f"{el:.1f} s on one host core"}
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle as the reference arm: each step is a bounded slice of one layer
+    call (a contiguous range of weight rows), timed on one host core."""
+    if rank != 0:
+        return None
+    import oracle
+    wk = workload()
+    w8, ex = wk.weights(copy=0)
+    x = wk.x(copy=0)
+    budget = 90.0
+    probe_rows = 32
+    t0 = time.perf_counter()
+    oracle.gemm(x, w8[:, :probe_rows], ex[:, :probe_rows // 32])
+    t_probe = max(time.perf_counter() - t0, 1e-6)
+    per_step = budget / max(1, args.steps + args.warmup)
+    rows = int(min(wk.N, max(probe_rows, (per_step / t_probe) * probe_rows)) // 32 * 32)
+    rows = max(32, rows)
+    ws, es = w8[:, :rows], ex[:, :rows // 32]
+    for _ in range(args.warmup):
+        oracle.gemm(x, ws, es)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.gemm(x, ws, es)
+    el = time.perf_counter() - t0
+    bytes_step = wk.G * rows * wk.K + wk.G * (rows // 32) * (wk.K // 32)
+    value = bytes_step * args.steps / el / 1e9
+    sample = (f"each step: rows [0, {rows}) of both groups of one wo_a layer (M=6), "
+              f"{rows / wk.N:.4f} of a layer call, one host core")
+    cfg = config_dict(wk, pdl=False)
+    cfg["launch"] = "CPU oracle (plain C, binary32 index-order sum), single thread"
+    return {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": cfg, "impl": "reference",
+        "us_per_call": el / args.steps * 1e6 * wk.N / rows,
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def build_layers(wk, device):
+    import torch
+    layers = []
+    for c in range(LAYERS):
+        w8, ex = wk.weights(copy=c)
+        x = wk.x(copy=c)
+        layers.append((torch.from_numpy(w8).to(device), torch.from_numpy(ex).to(device),
+                       torch.from_numpy(x.view("int16")).view(torch.bfloat16).to(device)))
+    return layers
+
+
+def time_graph(layers, wk, steps, warmup, pdl, stream, sampler=None):
+    """Captures the 43 calls of one step in a CUDA graph; replays `warmup` untimed then
+    `steps` timed steps; returns (seconds, wall t0, wall t1)."""
+    import torch
+    import block_scaled_fp8_weight_gb300 as bsf8
+    bsf8.set_option(bsf8.OPT_PDL, 1 if pdl else 0)
+    outs = [torch.empty((wk.M, wk.G, wk.N), dtype=torch.bfloat16, device=stream.device) for _ in layers]
+    try:
+        with torch.cuda.stream(stream):
+            for (w8, ex, x), y in zip(layers, outs):          # eager warm call (module load)
+                bsf8.gemm(x, w8, ex, split_k=wk.split_k, out=y)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for (w8, ex, x), y in zip(layers, outs):
+                    bsf8.gemm(x, w8, ex, split_k=wk.split_k, out=y)
+            for _ in range(warmup):
+                g.replay()
+            stream.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            w0 = time.time()
+            e0.record(stream)
+            for _ in range(steps):
+                g.replay()
+            e1.record(stream)
+            stream.synchronize()
+            w1 = time.time()
+    finally:
+        bsf8.set_option(bsf8.OPT_PDL, 1)
+    return e0.elapsed_time(e1) / 1e3, w0, w1
+
+
+def time_eager(layers, wk, steps, stream):
+    import torch
+    import block_scaled_fp8_weight_gb300 as bsf8
+    outs = [torch.empty((wk.M, wk.G, wk.N), dtype=torch.bfloat16, device=stream.device) for _ in layers]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            for (w8, ex, x), y in zip(layers, outs):
+                bsf8.gemm(x, w8, ex, split_k=wk.split_k, out=y)
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            for (w8, ex, x), y in zip(layers, outs):
+                bsf8.gemm(x, w8, ex, split_k=wk.split_k, out=y)
+        e1.record(stream)
+        stream.synchronize()
+    return e0.elapsed_time(e1) / 1e3
+
+
+def time_e2e(layers, wk, steps, stream):
+    """End to end through the public API: every step copies each layer's activations
+    from pinned host memory, runs bsf8.gemm, and copies the outputs back."""
+    import torch
+    import block_scaled_fp8_weight_gb300 as bsf8
+    dev = stream.device
+    xh = [x.cpu().pin_memory() for (_, _, x) in layers]
+    yh = [torch.empty((wk.M, wk.G, wk.N), dtype=torch.bfloat16).pin_memory() for _ in layers]
+    xd = [torch.empty_like(x, device=dev) for x in xh]
+    yd = [torch.empty((wk.M, wk.G, wk.N), dtype=torch.bfloat16, device=dev) for _ in layers]
+
+    def step():
+        for (w8, ex, _), a, b, xa, yb in zip(layers, xh, yh, xd, yd):
+            xa.copy_(a, non_blocking=True)
+            bsf8.gemm(xa, w8, ex, split_k=wk.split_k, out=yb)
+            b.copy_(yb, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        stream.synchronize()
+    h2d = sum(x.numel() * x.element_size() for x in xh)
+    d2h = sum(y.numel() * y.element_size() for y in yh)
+    return e0.elapsed_time(e1) / 1e3, h2d, d2h
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+
+    import torch
+    import block_scaled_fp8_weight_gb300 as bsf8
+    from block_scaled_fp8_weight_gb300 import build as bsf8_build
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (libbsf8 has no CPU path)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, True)
+    bsf8_build.build()
+    bsf8.load()
+    wk = workload()
+    layers = build_layers(wk, device)
+    stream = torch.cuda.Stream(device=device)
+
+    # Variants first (untimed for the headline): eager launches, graph without PDL.
+    t_eager = time_eager(layers, wk, max(1, args.steps // 20), stream)
+    t_nopdl, _, _ = time_graph(layers, wk, max(1, args.steps // 4), max(3, args.warmup), False, stream)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(dist, device)
+    torch.cuda.synchronize(device)
+    elapsed, w0, w1 = time_graph(layers, wk, args.steps, max(3, args.warmup), True, stream)
+    torch.cuda.synchronize(device)
+    barrier(dist, device)
+    time.sleep(0.25)
+    sampler.stop()
+    clocks = sampler.summary(w0, w1)
+
+    calls = LAYERS * args.steps
+    t_job, bytes_job = aggregate(dist, elapsed, float(wk.weight_bytes) * calls, device)
+    value = bytes_job / t_job / 1e9
+    us_call = elapsed / calls * 1e6
+
+    e2e_steps = max(1, min(args.e2e_steps, args.steps))
+    t_e2e, h2d, d2h = time_e2e(layers, wk, e2e_steps, stream)
+    t_e2e_job, bytes_e2e = aggregate(dist, t_e2e, float(wk.weight_bytes) * LAYERS * e2e_steps, device)
+
+    peak, peak_kind = measured_peaks()
+    achieved = wk.algorithmic_bytes / (elapsed / calls) / 1e9
+    traffic = recorded_traffic()
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_job / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_dict(wk), "us_per_call": us_call,
+        "frac_of_peak": {"measured_6781": value / world / peak, "nominal_8000": value / world / 8000.0},
+        "gpu_launches": calls,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
+                     "algorithmic_bytes_per_launch": wk.algorithmic_bytes},
+        "e2e": {"value": bytes_e2e / t_e2e_job / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "us_per_call": t_e2e / (LAYERS * e2e_steps) * 1e6,
+                "steps": e2e_steps, "path": "bsf8.gemm, eager, pinned host x -> device -> host y"},
+        "clocks": clocks,
+        "variants": {
+            "graph_no_pdl_us_per_call": t_nopdl / (LAYERS * max(1, args.steps // 4)) * 1e6,
+            "eager_us_per_call": t_eager / (LAYERS * max(1, args.steps // 20)) * 1e6,
+        },
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_baseline(wk, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

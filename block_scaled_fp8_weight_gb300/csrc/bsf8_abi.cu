@@ -1,0 +1,237 @@
+// bsf8_abi.cu -- the extern "C" entry points of libbsf8 (declared in include/bsf8.h).
+//
+// Every entry point validates its arguments on the host before touching CUDA, so a bad
+// call returns a status code without a GPU being involved; then it enqueues kernels on
+// the caller's stream and returns.  Nothing here allocates memory.
+#include "bsf8.h"
+#include "bsf8_device.cuh"
+#include "bsf8_internal.h"
+
+#include <atomic>
+#include <cstdint>
+
+namespace bsf8 {
+
+__device__ int g_status = 0;
+
+namespace {
+std::atomic<int> g_opt_pdl{1};
+std::atomic<long long> g_opt_timeout_ns{2000000000LL};
+std::atomic<int> g_opt_skip_loads{0};
+}  // namespace
+
+int *status_word() {
+    static int *addr[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    int *a = __atomic_load_n(&addr[dev], __ATOMIC_ACQUIRE);
+    if (!a) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+        a = static_cast<int *>(p);
+        __atomic_store_n(&addr[dev], a, __ATOMIC_RELEASE);
+    }
+    return a;
+}
+
+Options options() {
+    Options o;
+    o.pdl = g_opt_pdl.load(std::memory_order_relaxed);
+    o.timeout_ns = (unsigned long long)g_opt_timeout_ns.load(std::memory_order_relaxed);
+    o.skip_loads = g_opt_skip_loads.load(std::memory_order_relaxed);
+    return o;
+}
+
+}  // namespace bsf8
+
+using namespace bsf8;
+
+namespace {
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return BSF8_OK;
+    if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction ||
+        e == cudaErrorUnsupportedPtxVersion)
+        return BSF8_ERR_DEVICE;
+    return BSF8_ERR_CUDA;
+}
+
+// Common shape rules: sizes >= 1, N and K multiples of 32, element counts that fit.
+inline int check_gnk(int G, int N, int K) {
+    if (G < 1 || N < 32 || K < 32 || (N % 32) != 0 || (K % 32) != 0) return BSF8_ERR_SHAPE;
+    if ((long long)G * N * (long long)K > (1LL << 46)) return BSF8_ERR_SHAPE;
+    return BSF8_OK;
+}
+
+inline int check_gemm_args(const void *x, const uint8_t *w8, const uint8_t *exp, const void *out,
+                           int M, int N, int K, int G, int split_k, int64_t ldx) {
+    if (!x || !w8 || !exp || !out) return BSF8_ERR_NULL;
+    int st = check_gnk(G, N, K);
+    if (st) return st;
+    if (M < 1 || M > BSF8_MAX_M) return BSF8_ERR_SHAPE;
+    if (split_k < 0 || split_k > K / 32) return BSF8_ERR_SHAPE;
+    if (ldx < (int64_t)G * K) return BSF8_ERR_STRIDE;
+    if (!aligned16(x) || (ldx % 8) != 0 || !aligned16(w8)) return BSF8_ERR_ALIGN;
+    return BSF8_OK;
+}
+
+constexpr size_t kMaxSmem = 227 * 1024;
+
+}  // namespace
+
+extern "C" {
+
+const char *bsf8_strerror(int status) {
+    switch (status) {
+        case BSF8_OK: return "ok";
+        case BSF8_ERR_SHAPE: return "invalid shape (sizes < 1, N or K not a multiple of 32, M or split_k out of range)";
+        case BSF8_ERR_ALIGN: return "misaligned pointer or stride (16-byte rule)";
+        case BSF8_ERR_STRIDE: return "row stride ldx smaller than G*K";
+        case BSF8_ERR_WORKSPACE: return "workspace missing or too small";
+        case BSF8_ERR_NULL: return "required pointer is NULL";
+        case BSF8_ERR_CUDA: return "CUDA runtime error";
+        case BSF8_ERR_TIMEOUT: return "a kernel gave up a bounded wait (outputs undefined)";
+        case BSF8_ERR_DEVICE: return "device cannot run the sm_103a kernels";
+        case BSF8_ERR_VALUE: return "option or scalar argument out of range";
+        default: return "unknown status";
+    }
+}
+
+int bsf8_version(void) { return 100; }
+
+int bsf8_make_twin(const void *w, uint8_t *w8, uint8_t *exp, uint8_t *block_ok, int32_t *accepted,
+                   int G, int N, int K, bsf8_stream_t stream) {
+    if (!w || !w8 || !exp || !accepted) return BSF8_ERR_NULL;
+    int st = check_gnk(G, N, K);
+    if (st) return st;
+    if (!aligned16(w) || !aligned16(w8)) return BSF8_ERR_ALIGN;
+    return from_cuda(launch_make_twin(w, w8, exp, block_ok, accepted, G, N, K,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int bsf8_dequant(const uint8_t *w8, const uint8_t *exp, void *out, int G, int N, int K,
+                 bsf8_stream_t stream) {
+    if (!w8 || !exp || !out) return BSF8_ERR_NULL;
+    int st = check_gnk(G, N, K);
+    if (st) return st;
+    if (!aligned16(w8) || !aligned16(out)) return BSF8_ERR_ALIGN;
+    return from_cuda(launch_dequant(w8, exp, out, G, N, K, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int bsf8_gemm_auto_split(int M, int N, int K, int G) {
+    int st = check_gnk(G, N, K);
+    if (st) return -st;
+    if (M < 1 || M > BSF8_MAX_M) return -BSF8_ERR_SHAPE;
+    return auto_split(M, N, K, G);
+}
+
+size_t bsf8_gemm_workspace_bytes(int M, int N, int K, int G, int split_k) {
+    if (check_gnk(G, N, K) || M < 1 || M > BSF8_MAX_M || split_k < 0 || split_k > K / 32) return 0;
+    const int S = split_k == 0 ? auto_split(M, N, K, G) : split_k;
+    if (S <= kMaxClusterSplits) return 0;
+    return (size_t)S * M * G * N * sizeof(float);
+}
+
+int bsf8_gemm(const void *x, const uint8_t *w8, const uint8_t *exp, void *y, int M, int N, int K,
+              int G, int split_k, int64_t ldx, void *workspace, size_t workspace_bytes,
+              bsf8_stream_t stream) {
+    int st = check_gemm_args(x, w8, exp, y, M, N, K, G, split_k, ldx);
+    if (st) return st;
+    const int S = split_k == 0 ? auto_split(M, N, K, G) : split_k;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (S <= kMaxClusterSplits) {
+        const GemmPlan pl = plan_gemm(M, N, K, G, S, S == 1 ? kModeDirect : kModeCluster);
+        if (pl.smem_bytes > kMaxSmem) return BSF8_ERR_SHAPE;
+        return from_cuda(launch_gemm(pl, x, ldx, w8, exp, y, nullptr, M, N, K, G, s));
+    }
+    const size_t need = (size_t)S * M * G * N * sizeof(float);
+    if (!workspace || workspace_bytes < need) return BSF8_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return BSF8_ERR_ALIGN;
+    const GemmPlan pl = plan_gemm(M, N, K, G, S, kModePartials);
+    if (pl.smem_bytes > kMaxSmem) return BSF8_ERR_SHAPE;
+    float *P = static_cast<float *>(workspace);
+    st = from_cuda(launch_gemm(pl, x, ldx, w8, exp, nullptr, P, M, N, K, G, s));
+    if (st) return st;
+    return from_cuda(launch_splitk_reduce(P, y, S, (long long)M * G * N, s));
+}
+
+int bsf8_gemm_partials(const void *x, const uint8_t *w8, const uint8_t *exp, float *partials,
+                       int M, int N, int K, int G, int split_k, int64_t ldx,
+                       bsf8_stream_t stream) {
+    int st = check_gemm_args(x, w8, exp, partials, M, N, K, G, split_k, ldx);
+    if (st) return st;
+    if (split_k < 1) return BSF8_ERR_SHAPE;
+    if (!aligned16(partials)) return BSF8_ERR_ALIGN;
+    const GemmPlan pl = plan_gemm(M, N, K, G, split_k, kModePartials);
+    if (pl.smem_bytes > kMaxSmem) return BSF8_ERR_SHAPE;
+    return from_cuda(launch_gemm(pl, x, ldx, w8, exp, nullptr, partials, M, N, K, G,
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int bsf8_splitk_reduce(const float *partials, void *y, int S, int64_t count, bsf8_stream_t stream) {
+    if (S < 1 || count < 0) return BSF8_ERR_SHAPE;
+    if (count == 0) return BSF8_OK;
+    if (!partials || !y) return BSF8_ERR_NULL;
+    return from_cuda(launch_splitk_reduce(partials, y, S, (long long)count,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int bsf8_pad_k(const uint8_t *w8, const uint8_t *exp, uint8_t *w8_out, uint8_t *exp_out, int G,
+               int N, int K, int Kp, int pad_exp, bsf8_stream_t stream) {
+    if (!w8 || !exp || !w8_out || !exp_out) return BSF8_ERR_NULL;
+    int st = check_gnk(G, N, K);
+    if (st) return st;
+    if (Kp < K || (Kp % 32) != 0 || check_gnk(G, N, Kp)) return BSF8_ERR_SHAPE;
+    if (pad_exp < 0 || pad_exp > 255) return BSF8_ERR_VALUE;
+    if (!aligned16(w8) || !aligned16(w8_out)) return BSF8_ERR_ALIGN;
+    return from_cuda(launch_pad_k(w8, exp, w8_out, exp_out, G, N, K, Kp, pad_exp,
+                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int bsf8_pad_x(const void *x, int64_t ldx, void *x_out, int M, int G, int K, int Kp,
+               bsf8_stream_t stream) {
+    if (!x || !x_out) return BSF8_ERR_NULL;
+    if (M < 1 || G < 1 || K < 32 || (K % 32) != 0 || Kp < K || (Kp % 32) != 0) return BSF8_ERR_SHAPE;
+    if ((long long)M * G * (long long)Kp > (1LL << 46)) return BSF8_ERR_SHAPE;
+    if (ldx < (int64_t)G * K) return BSF8_ERR_STRIDE;
+    if (!aligned16(x) || (ldx % 8) != 0 || !aligned16(x_out)) return BSF8_ERR_ALIGN;
+    return from_cuda(launch_pad_x(x, (long long)ldx, x_out, M, G, K, Kp,
+                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int bsf8_device_status(int *status, bsf8_stream_t stream) {
+    if (!status) return BSF8_ERR_NULL;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return from_cuda(e);
+    int v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_status, sizeof v);
+    if (e != cudaSuccess) return from_cuda(e);
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_status, &zero, sizeof zero);
+    if (e != cudaSuccess) return from_cuda(e);
+    *status = v;
+    return BSF8_OK;
+}
+
+int bsf8_set_option(int option, int64_t value) {
+    if (value < 0) return BSF8_ERR_VALUE;
+    switch (option) {
+        case BSF8_OPT_PDL: g_opt_pdl.store(value ? 1 : 0); return BSF8_OK;
+        case BSF8_OPT_WAIT_TIMEOUT_NS: g_opt_timeout_ns.store((long long)value); return BSF8_OK;
+        case BSF8_OPT_DEBUG_SKIP_LOADS: g_opt_skip_loads.store(value ? 1 : 0); return BSF8_OK;
+        default: return BSF8_ERR_VALUE;
+    }
+}
+
+int64_t bsf8_get_option(int option) {
+    switch (option) {
+        case BSF8_OPT_PDL: return g_opt_pdl.load();
+        case BSF8_OPT_WAIT_TIMEOUT_NS: return g_opt_timeout_ns.load();
+        case BSF8_OPT_DEBUG_SKIP_LOADS: return g_opt_skip_loads.load();
+        default: return -BSF8_ERR_VALUE;
+    }
+}
+
+}  // extern "C"

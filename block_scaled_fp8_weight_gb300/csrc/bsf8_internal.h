@@ -1,0 +1,65 @@
+// bsf8_internal.h -- host-side interface between the C ABI (bsf8_abi.cu) and the
+// kernel translation units.  Not installed; not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace bsf8 {
+
+// Process-wide launch options (see BSF8_OPT_* in bsf8.h).
+struct Options {
+    int pdl;
+    unsigned long long timeout_ns;
+    int skip_loads;
+};
+Options options();
+
+// Device address of the library's status word on the current device (looked up once
+// per device); nullptr if the lookup fails.
+int *status_word();
+
+// GEMM geometry shared by the host planner and the kernels.
+constexpr int kBN = 64;           // weight rows per CTA
+constexpr int kStageK = 256;      // weight columns per pipeline stage (4 warps x 64)
+constexpr int kRowPitch = 320;    // shared-memory bytes per staged row (256 + 64 pad)
+constexpr int kStageBytes = kBN * kRowPitch;
+constexpr int kMaxStages = 4;
+constexpr int kConsumerWarps = 4;
+constexpr int kGemmThreads = (kConsumerWarps + 1) * 32;
+constexpr int kPrefetchCols = 1024;  // L2 prefetch per CTA row before the dependency wait
+constexpr int kMaxClusterSplits = 8;
+constexpr int kTargetCtas = 2 * 152; // GB300: 152 SMs
+
+enum GemmMode { kModeDirect = 0, kModeCluster = 1, kModePartials = 2 };
+
+struct GemmPlan {
+    int S;            // splits
+    int chunk_cols;   // columns per split (multiple of 32)
+    int nt8;          // n8 tiles of tokens per CTA (1..4)
+    int m_chunks;     // ceil(M / (8 * nt8))
+    int stages;       // ring depth
+    int mode;
+    size_t smem_bytes;
+};
+
+int auto_split(int M, int N, int K, int G);
+GemmPlan plan_gemm(int M, int N, int K, int G, int S, int mode);
+
+// Launchers return a cudaError_t.
+cudaError_t launch_gemm(const GemmPlan &plan, const void *x, long long ldx, const uint8_t *w8,
+                        const uint8_t *ex, void *y, float *partials, int M, int N, int K, int G,
+                        cudaStream_t stream);
+cudaError_t launch_splitk_reduce(const float *P, void *y, int S, long long count,
+                                 cudaStream_t stream);
+cudaError_t launch_dequant(const uint8_t *w8, const uint8_t *ex, void *out, int G, int N, int K,
+                           cudaStream_t stream);
+cudaError_t launch_make_twin(const void *w, uint8_t *w8, uint8_t *ex, uint8_t *ok,
+                             int32_t *accepted, int G, int N, int K, cudaStream_t stream);
+cudaError_t launch_pad_k(const uint8_t *w8, const uint8_t *ex, uint8_t *w8_out, uint8_t *ex_out,
+                         int G, int N, int K, int Kp, int pad_exp, cudaStream_t stream);
+cudaError_t launch_pad_x(const void *x, long long ldx, void *x_out, int M, int G, int K, int Kp,
+                         cudaStream_t stream);
+
+}  // namespace bsf8

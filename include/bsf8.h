@@ -1,0 +1,190 @@
+/*
+ * bsf8.h -- C ABI of libbsf8, a block-scaled FP8 weight library for GB300 (sm_103a).
+ *
+ * The method (pages "recipes/docker-images/mia-tp4/adapter/wo_a_w8.py" and
+ * "recipes/docker-images/mia-tp4/adapter/shared_pad_k.py"):
+ *   A bf16 weight W[G][N][K] is kept as an fp8 "twin": one e4m3 code per element plus
+ *   one exponent byte (ue8m0, byte = e + 127) per 32x32 block.  The small-batch linear
+ *   y[m][g][n] = sum_k x[m][g*K + k] * W[g][n][k] reads the twin, rebuilds each bf16
+ *   weight exactly as bf16(e4m3 * 2^(byte-127)) in registers and accumulates in fp32;
+ *   split-K partials are summed in a fixed order, so results are deterministic.
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers owned by the caller, except where a parameter says
+ *     "host".  The library never allocates and keeps no hidden scratch: every buffer a
+ *     call touches is named in its argument list.
+ *   - bf16 tensors are passed as void* holding IEEE bfloat16 bit patterns.
+ *   - Row-major layouts:  w8[G][N][K] (uint8 e4m3fn codes),  exp[G][N/32][K/32]
+ *     (uint8, byte = e + 127),  x[M][ldx] (bf16; group g uses columns [g*K, (g+1)*K)),
+ *     y[M][G][N] (bf16),  partials[S][M][G][N] (fp32).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream), do not synchronise the host, and allocate nothing.
+ *   - Every call validates its arguments on the host first and returns a status code
+ *     without launching anything when they are invalid; on success it returns BSF8_OK
+ *     once the work is enqueued.  Faults found by the kernels themselves (a bounded
+ *     wait that ran out) are recorded in a device status word read by
+ *     bsf8_device_status().
+ *   - Shapes: N and K are multiples of 32 (one exponent per 32x32 block); G >= 1.
+ *
+ * This library needs an sm_103a GPU (GB300); it has no CPU fallback.
+ */
+#ifndef BSF8_H
+#define BSF8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t without pulling in the CUDA headers. */
+typedef struct CUstream_st *bsf8_stream_t;
+
+/* Status codes. */
+enum {
+    BSF8_OK = 0,
+    BSF8_ERR_SHAPE = 1,     /* N or K not a multiple of 32, a size < 1, M out of range  */
+    BSF8_ERR_ALIGN = 2,     /* a pointer or stride breaks the 16-byte rule of the call  */
+    BSF8_ERR_STRIDE = 3,    /* ldx < G*K                                                */
+    BSF8_ERR_WORKSPACE = 4, /* workspace missing or smaller than the call needs         */
+    BSF8_ERR_NULL = 5,      /* a required pointer is NULL                               */
+    BSF8_ERR_CUDA = 6,      /* a CUDA runtime call failed (launch, attribute, copy)     */
+    BSF8_ERR_TIMEOUT = 7,   /* a kernel gave up a bounded wait (device status only)     */
+    BSF8_ERR_DEVICE = 8,    /* the current device is not sm_103 / cannot run the kernels */
+    BSF8_ERR_VALUE = 9      /* an option or scalar argument is out of range             */
+};
+
+/* Largest row count a single bsf8_gemm call accepts (decode, verify and draft batches;
+ * the pages serve 2..8 and 9..192 rows from the twin). */
+#define BSF8_MAX_M 192
+
+/* Returns a static, human-readable name for a status code. */
+const char *bsf8_strerror(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int bsf8_version(void);
+
+/* --------------------------------------------------------------------- make_twin
+ * "wo_a_w8.py", make_twin(): per 32x32 block of the bf16 weight w[G][N][K]
+ *   amax = max |w| (raised to at least 2^-126),  e = ceil(log2(amax/448)) in [-127,127],
+ *   w8   = e4m3 round-to-nearest-even of w / 2^e,  exp = e + 127,
+ *   block_ok = 1 iff bf16(e4m3 * 2^e) == w for all 1024 elements (value equality),
+ * and *accepted = 1 iff every block is ok (the pages keep the twin only then).
+ * Blocks holding NaN or Inf get block_ok = 0, exp = 0xFF and codes 0x7F (the pages
+ * leave them undefined; the tensor is rejected either way).
+ *   w        device, bf16 [G][N][K], 16-byte aligned
+ *   w8       device, out, uint8 [G][N][K], 16-byte aligned
+ *   exp      device, out, uint8 [G][N/32][K/32]
+ *   block_ok device, out, uint8 [G][N/32][K/32], or NULL
+ *   accepted device, out, one int32 (written 1 or 0 on the stream)
+ * Errors: BSF8_ERR_NULL, BSF8_ERR_SHAPE, BSF8_ERR_ALIGN, BSF8_ERR_CUDA. */
+int bsf8_make_twin(const void *w, uint8_t *w8, uint8_t *exp, uint8_t *block_ok,
+                   int32_t *accepted, int G, int N, int K, bsf8_stream_t stream);
+
+/* ----------------------------------------------------------------------- dequant
+ * "wo_a_w8.py", _dequant_kernel(): out[g][n][k] = bf16( e4m3(w8[g][n][k]) *
+ * 2^(exp[g][n/32][k/32] - 127) ), rounded to nearest even; exact for every code and
+ * exponent byte (byte 255 is a +inf scale: 0 -> NaN, others -> +-inf; e4m3 NaN codes
+ * give NaN).  The page's drop mode serves prefill from such a per-call copy.
+ *   w8  device, uint8 [G][N][K], 16-byte aligned
+ *   exp device, uint8 [G][N/32][K/32]
+ *   out device, out, bf16 [G][N][K], 16-byte aligned
+ * Errors: BSF8_ERR_NULL, BSF8_ERR_SHAPE, BSF8_ERR_ALIGN, BSF8_ERR_CUDA. */
+int bsf8_dequant(const uint8_t *w8, const uint8_t *exp, void *out, int G, int N, int K,
+                 bsf8_stream_t stream);
+
+/* -------------------------------------------------------------------------- GEMM
+ * "wo_a_w8.py", _wo_a_partial_w8() / _wo_a_mid_kernel() and their fixed-order
+ * reduction (module docstring: "Split-K partials are summed in a fixed order"):
+ *   y[m][g][n] = bf16( sum_{s=0..S-1} P[s][m][g][n] ),  summed s = 0, 1, ... in fp32,
+ *   P[s][m][g][n] = sum over split s's columns of x[m][g*K+k] * bf16(W8[g][n][k]*2^e),
+ * with the products accumulated in fp32 on the tensor cores.  Split s covers columns
+ * [s*c*32, min(K, (s+1)*c*32)) with c = ceil((K/32)/S) (it may be empty).
+ *   x         device, bf16 [M][ldx], 16-byte aligned, ldx a multiple of 8, ldx >= G*K
+ *   w8, exp   the twin (layouts above); w8 16-byte aligned
+ *   y         device, out, bf16 [M][G][N]
+ *   M         1 .. BSF8_MAX_M
+ *   split_k   0 = the library chooses (bsf8_gemm_auto_split), else 1 .. K/32
+ *   workspace device scratch of at least bsf8_gemm_workspace_bytes(...) bytes, or
+ *             NULL when that is 0.  It is used only when split_k > 8 (fp32 partials
+ *             between the two passes); no zeroing is needed, and it must not be shared
+ *             by calls that can run concurrently.
+ * For 2 <= S <= 8 the S splits of one output tile run as one thread-block cluster and
+ * are summed through distributed shared memory in the same fixed order; S > 8 runs
+ * bsf8_gemm_partials then bsf8_splitk_reduce.  Both give the same bits.
+ * The kernel may prefetch w8/exp into L2 before the preceding kernel on the stream has
+ * finished (programmatic dependent launch); it reads x and writes y only after it.
+ * Errors: BSF8_ERR_NULL, BSF8_ERR_SHAPE, BSF8_ERR_ALIGN, BSF8_ERR_STRIDE,
+ *         BSF8_ERR_WORKSPACE, BSF8_ERR_CUDA. */
+int bsf8_gemm(const void *x, const uint8_t *w8, const uint8_t *exp, void *y,
+              int M, int N, int K, int G, int split_k, int64_t ldx,
+              void *workspace, size_t workspace_bytes, bsf8_stream_t stream);
+
+/* Workspace bsf8_gemm needs for these sizes (0 when split_k resolves to <= 8). */
+size_t bsf8_gemm_workspace_bytes(int M, int N, int K, int G, int split_k);
+
+/* The split count bsf8_gemm uses for split_k = 0 (host only; no GPU needed).  Returns
+ * a value in 1 .. min(8, K/32), or a negative status for invalid sizes. */
+int bsf8_gemm_auto_split(int M, int N, int K, int G);
+
+/* First pass alone: writes the fp32 partials P[S][M][G][N] (S = split_k >= 1, every
+ * split written, empty splits as +0).  Same arguments as bsf8_gemm.
+ *   partials device, out, fp32 [S][M][G][N], 16-byte aligned
+ * Errors: as bsf8_gemm. */
+int bsf8_gemm_partials(const void *x, const uint8_t *w8, const uint8_t *exp,
+                       float *partials, int M, int N, int K, int G, int split_k,
+                       int64_t ldx, bsf8_stream_t stream);
+
+/* Second pass alone ("wo_a_w8.py", the reduce after _partial_w8): for i < count,
+ *   y[i] = bf16_rne( ((P[0][i] + P[1][i]) + P[2][i]) + ... + P[S-1][i] )
+ * in fp32, left to right.
+ *   partials device, fp32 [S][count]
+ *   y        device, out, bf16 [count]
+ * Errors: BSF8_ERR_NULL, BSF8_ERR_SHAPE, BSF8_ERR_CUDA. */
+int bsf8_splitk_reduce(const float *partials, void *y, int S, int64_t count,
+                       bsf8_stream_t stream);
+
+/* ------------------------------------------------------------------------- pad-K
+ * "shared_pad_k.py", _pad_weight(): the twin [G][N][K] becomes [G][N][Kp] with code 0
+ * (+0) in the new columns and its exponents [G][N/32][K/32] become [G][N/32][Kp/32]
+ * with pad_exp in the new block columns (127 = scale 1.0, the page's choice; any byte
+ * but 255 leaves every output unchanged, since 0 * 2^e = 0).
+ *   w8, exp           device, the input twin; w8 16-byte aligned
+ *   w8_out, exp_out   device, out; w8_out 16-byte aligned
+ *   Kp                a multiple of 32, >= K;  pad_exp  0 .. 255
+ * Errors: BSF8_ERR_NULL, BSF8_ERR_SHAPE, BSF8_ERR_ALIGN, BSF8_ERR_VALUE, BSF8_ERR_CUDA. */
+int bsf8_pad_k(const uint8_t *w8, const uint8_t *exp, uint8_t *w8_out, uint8_t *exp_out,
+               int G, int N, int K, int Kp, int pad_exp, bsf8_stream_t stream);
+
+/* "shared_pad_k.py", _pad_input(): x[M][ldx] (group g in columns [g*K, (g+1)*K))
+ * becomes x_out[M][G*Kp] with +0 in the new columns of every group.
+ *   x      device, bf16, 16-byte aligned, ldx a multiple of 8, ldx >= G*K
+ *   x_out  device, out, bf16 [M][G*Kp], 16-byte aligned
+ * Errors: BSF8_ERR_NULL, BSF8_ERR_SHAPE, BSF8_ERR_ALIGN, BSF8_ERR_STRIDE, BSF8_ERR_CUDA. */
+int bsf8_pad_x(const void *x, int64_t ldx, void *x_out, int M, int G, int K, int Kp,
+               bsf8_stream_t stream);
+
+/* --------------------------------------------------------------- status, options
+ * Synchronises `stream`, then reads into *status (host) and clears the device status
+ * word of the current device: BSF8_OK, or BSF8_ERR_TIMEOUT if a kernel gave up a
+ * bounded wait since the last read (its outputs are then undefined).
+ * Errors: BSF8_ERR_NULL, BSF8_ERR_CUDA. */
+int bsf8_device_status(int *status, bsf8_stream_t stream);
+
+/* Process-wide options (host state, read at each launch). */
+enum {
+    BSF8_OPT_PDL = 1,              /* 1 (default): programmatic dependent launch on    */
+    BSF8_OPT_WAIT_TIMEOUT_NS = 2,  /* bound of every in-kernel wait (default 2e9 ns)   */
+    BSF8_OPT_DEBUG_SKIP_LOADS = 3  /* test only: GEMM issues no weight loads, so its   */
+                                   /* waits run out and it reports BSF8_ERR_TIMEOUT    */
+};
+/* Errors: BSF8_ERR_VALUE for an unknown option or a negative value. */
+int bsf8_set_option(int option, int64_t value);
+int64_t bsf8_get_option(int option);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSF8_H */

@@ -1,0 +1,65 @@
+"""Shared helpers for the GPU parity tests: tensor <-> numpy bit transfers and the
+tolerance the GEMM is held to (stated for floating point outputs: max |y - y_ref| <=
+1e-2 * rms(y_ref), and at least 99.9% of outputs within one bf16 ulp of the oracle)."""
+import numpy as np
+import torch
+
+import oracle
+
+REL_MAX = 1e-2
+ULP_FRACTION = 0.999
+
+
+def to_dev_u8(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint8)).cuda()
+
+
+def to_dev_bf16(bits):
+    t = torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint16).view(np.int16))
+    return t.view(torch.bfloat16).cuda()
+
+
+def bf16_bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def is_nan_bits(b):
+    return (np.asarray(b, dtype=np.uint16) & 0x7FFF) > 0x7F80
+
+
+def same_bits(a, b, zero_sign=False):
+    """Bitwise equality, any NaN equal to any NaN, optionally +0 equal to -0."""
+    a = np.asarray(a, dtype=np.uint16)
+    b = np.asarray(b, dtype=np.uint16)
+    eq = a == b
+    na, nb = is_nan_bits(a), is_nan_bits(b)
+    eq = np.where(na | nb, na & nb, eq)
+    if zero_sign:
+        eq |= ((a & 0x7FFF) == 0) & ((b & 0x7FFF) == 0)
+    return eq
+
+
+def bf16_ord(b):
+    b = np.asarray(b, dtype=np.uint16).astype(np.int64)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def gemm_error(y_bits, ref_bits):
+    """(max |y - ref| / rms(ref), fraction within 1 bf16 ulp, nan mismatches)."""
+    y = oracle.bf16_bits_to_f32(y_bits).astype(np.float64)
+    r = oracle.bf16_bits_to_f32(ref_bits).astype(np.float64)
+    nan_mismatch = int(np.count_nonzero(np.isnan(y) != np.isnan(r)))
+    ok = ~(np.isnan(y) | np.isnan(r))
+    rms = np.sqrt(np.mean(r[ok] ** 2)) if ok.any() else 0.0
+    max_rel = float(np.max(np.abs(y[ok] - r[ok])) / rms) if ok.any() and rms > 0 else 0.0
+    within = float(np.mean(np.abs(bf16_ord(y_bits)[ok] - bf16_ord(ref_bits)[ok]) <= 1)) if ok.any() else 1.0
+    return max_rel, within, nan_mismatch
+
+
+def assert_gemm_close(y_bits, ref_bits, what=""):
+    max_rel, within, nan_mismatch = gemm_error(y_bits, ref_bits)
+    assert nan_mismatch == 0, f"{what}: NaN pattern differs"
+    assert max_rel <= REL_MAX, f"{what}: max|dy|/rms = {max_rel:.3g}"
+    assert within >= ULP_FRACTION, f"{what}: only {within:.5f} within 1 ulp"
+    return max_rel, within
