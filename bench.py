@@ -54,6 +54,9 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="CPU time budget of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--profile-calls", type=int, default=0,
+                   help="profiling mode: run this many eager layer calls and exit (no JSON)")
+    p.add_argument("--split-k", type=int, default=None, help="override the workload's split_k")
     return p.parse_args(argv)
 
 
@@ -384,8 +387,18 @@ def main(argv=None):
     bsf8_build.build()
     bsf8.load()
     wk = workload()
+    if args.split_k is not None:
+        import dataclasses
+        wk = dataclasses.replace(wk, split_k=args.split_k)
     layers = build_layers(wk, device)
     stream = torch.cuda.Stream(device=device)
+    if args.profile_calls:
+        with torch.cuda.stream(stream):
+            for i in range(args.profile_calls):
+                w8, ex, x = layers[i % LAYERS]
+                bsf8.gemm(x, w8, ex, split_k=wk.split_k)
+        torch.cuda.synchronize(device)
+        return 0
 
     # Variants first (untimed for the headline): eager launches, graph without PDL.
     t_eager = time_eager(layers, wk, max(1, args.steps // 20), stream)

@@ -18,6 +18,7 @@ namespace {
 std::atomic<int> g_opt_pdl{1};
 std::atomic<long long> g_opt_timeout_ns{2000000000LL};
 std::atomic<int> g_opt_skip_loads{0};
+std::atomic<int> g_opt_gemm_path{0};
 }  // namespace
 
 int *status_word() {
@@ -39,6 +40,7 @@ Options options() {
     o.pdl = g_opt_pdl.load(std::memory_order_relaxed);
     o.timeout_ns = (unsigned long long)g_opt_timeout_ns.load(std::memory_order_relaxed);
     o.skip_loads = g_opt_skip_loads.load(std::memory_order_relaxed);
+    o.gemm_path = g_opt_gemm_path.load(std::memory_order_relaxed);
     return o;
 }
 
@@ -130,7 +132,7 @@ int bsf8_gemm_auto_split(int M, int N, int K, int G) {
 size_t bsf8_gemm_workspace_bytes(int M, int N, int K, int G, int split_k) {
     if (check_gnk(G, N, K) || M < 1 || M > BSF8_MAX_M || split_k < 0 || split_k > K / 32) return 0;
     const int S = split_k == 0 ? auto_split(M, N, K, G) : split_k;
-    if (S <= kMaxClusterSplits) return 0;
+    if (plan_stream(M, N, K, G, S, false).mode != kStreamPartials) return 0;
     return (size_t)S * M * G * N * sizeof(float);
 }
 
@@ -141,20 +143,23 @@ int bsf8_gemm(const void *x, const uint8_t *w8, const uint8_t *exp, void *y, int
     if (st) return st;
     const int S = split_k == 0 ? auto_split(M, N, K, G) : split_k;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (S <= kMaxClusterSplits) {
+    if (options().gemm_path == 0 || S > kMaxClusterSplits) {
+        const StreamPlan pl = plan_stream(M, N, K, G, S, false);
+        if (pl.mode != kStreamPartials)
+            return from_cuda(launch_stream(pl, x, ldx, w8, exp, y, nullptr, M, N, K, G, s));
+        const size_t need = (size_t)S * M * G * N * sizeof(float);
+        if (!workspace || workspace_bytes < need) return BSF8_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return BSF8_ERR_ALIGN;
+        float *P = static_cast<float *>(workspace);
+        st = from_cuda(launch_stream(pl, x, ldx, w8, exp, nullptr, P, M, N, K, G, s));
+        if (st) return st;
+        return from_cuda(launch_splitk_reduce(P, y, S, (long long)M * G * N, s));
+    }
+    {  // the shared-memory TMA-ring kernel (BSF8_OPT_GEMM_PATH = 1), S <= 8
         const GemmPlan pl = plan_gemm(M, N, K, G, S, S == 1 ? kModeDirect : kModeCluster);
         if (pl.smem_bytes > kMaxSmem) return BSF8_ERR_SHAPE;
         return from_cuda(launch_gemm(pl, x, ldx, w8, exp, y, nullptr, M, N, K, G, s));
     }
-    const size_t need = (size_t)S * M * G * N * sizeof(float);
-    if (!workspace || workspace_bytes < need) return BSF8_ERR_WORKSPACE;
-    if (!aligned16(workspace)) return BSF8_ERR_ALIGN;
-    const GemmPlan pl = plan_gemm(M, N, K, G, S, kModePartials);
-    if (pl.smem_bytes > kMaxSmem) return BSF8_ERR_SHAPE;
-    float *P = static_cast<float *>(workspace);
-    st = from_cuda(launch_gemm(pl, x, ldx, w8, exp, nullptr, P, M, N, K, G, s));
-    if (st) return st;
-    return from_cuda(launch_splitk_reduce(P, y, S, (long long)M * G * N, s));
 }
 
 int bsf8_gemm_partials(const void *x, const uint8_t *w8, const uint8_t *exp, float *partials,
@@ -164,10 +169,14 @@ int bsf8_gemm_partials(const void *x, const uint8_t *w8, const uint8_t *exp, flo
     if (st) return st;
     if (split_k < 1) return BSF8_ERR_SHAPE;
     if (!aligned16(partials)) return BSF8_ERR_ALIGN;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (options().gemm_path == 0) {
+        const StreamPlan pl = plan_stream(M, N, K, G, split_k, true);
+        return from_cuda(launch_stream(pl, x, ldx, w8, exp, nullptr, partials, M, N, K, G, s));
+    }
     const GemmPlan pl = plan_gemm(M, N, K, G, split_k, kModePartials);
     if (pl.smem_bytes > kMaxSmem) return BSF8_ERR_SHAPE;
-    return from_cuda(launch_gemm(pl, x, ldx, w8, exp, nullptr, partials, M, N, K, G,
-                                 reinterpret_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_gemm(pl, x, ldx, w8, exp, nullptr, partials, M, N, K, G, s));
 }
 
 int bsf8_splitk_reduce(const float *partials, void *y, int S, int64_t count, bsf8_stream_t stream) {
@@ -221,6 +230,10 @@ int bsf8_set_option(int option, int64_t value) {
         case BSF8_OPT_PDL: g_opt_pdl.store(value ? 1 : 0); return BSF8_OK;
         case BSF8_OPT_WAIT_TIMEOUT_NS: g_opt_timeout_ns.store((long long)value); return BSF8_OK;
         case BSF8_OPT_DEBUG_SKIP_LOADS: g_opt_skip_loads.store(value ? 1 : 0); return BSF8_OK;
+        case BSF8_OPT_GEMM_PATH:
+            if (value > 1) return BSF8_ERR_VALUE;
+            g_opt_gemm_path.store((int)value);
+            return BSF8_OK;
         default: return BSF8_ERR_VALUE;
     }
 }
@@ -230,6 +243,7 @@ int64_t bsf8_get_option(int option) {
         case BSF8_OPT_PDL: return g_opt_pdl.load();
         case BSF8_OPT_WAIT_TIMEOUT_NS: return g_opt_timeout_ns.load();
         case BSF8_OPT_DEBUG_SKIP_LOADS: return g_opt_skip_loads.load();
+        case BSF8_OPT_GEMM_PATH: return g_opt_gemm_path.load();
         default: return -BSF8_ERR_VALUE;
     }
 }

@@ -13,6 +13,7 @@ struct Options {
     int pdl;
     unsigned long long timeout_ns;
     int skip_loads;
+    int gemm_path;  // 0: weight-streaming kernel; 1: shared-memory TMA-ring kernel
 };
 Options options();
 
@@ -43,6 +44,20 @@ struct GemmPlan {
     int mode;
     size_t smem_bytes;
 };
+
+// Weight-streaming kernel (bsf8_stream.cu): warp tasks of 16 rows x a column range.
+enum StreamMode { kStreamInCta = 0, kStreamCluster = 1, kStreamPartials = 2 };
+
+struct StreamPlan {
+    int S, chunk_cols, kt, tps;  // splits, columns per split, per task, tasks per split
+    int nt8, m_chunks;           // token tiles of 8 per pass, passes over the tokens
+    int mode, spc, cluster, spl, cps, grid_x;
+};
+
+StreamPlan plan_stream(int M, int N, int K, int G, int S, bool partials);
+cudaError_t launch_stream(const StreamPlan &plan, const void *x, long long ldx, const uint8_t *w8,
+                          const uint8_t *ex, void *y, float *partials, int M, int N, int K, int G,
+                          cudaStream_t stream);
 
 int auto_split(int M, int N, int K, int G);
 GemmPlan plan_gemm(int M, int N, int K, int G, int S, int mode);

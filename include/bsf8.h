@@ -107,12 +107,12 @@ int bsf8_dequant(const uint8_t *w8, const uint8_t *exp, void *out, int G, int N,
  *   M         1 .. BSF8_MAX_M
  *   split_k   0 = the library chooses (bsf8_gemm_auto_split), else 1 .. K/32
  *   workspace device scratch of at least bsf8_gemm_workspace_bytes(...) bytes, or
- *             NULL when that is 0.  It is used only when split_k > 8 (fp32 partials
- *             between the two passes); no zeroing is needed, and it must not be shared
- *             by calls that can run concurrently.
- * For 2 <= S <= 8 the S splits of one output tile run as one thread-block cluster and
- * are summed through distributed shared memory in the same fixed order; S > 8 runs
- * bsf8_gemm_partials then bsf8_splitk_reduce.  Both give the same bits.
+ *             NULL when that is 0 (it is 0 unless a slab of 16 rows needs more than 64
+ *             column tasks, e.g. split_k > 64): fp32 partials between the two passes.
+ *             No zeroing is needed; it must not be shared by calls that can overlap.
+ * The partials of a 16-row slab are summed inside one thread block, or across a cluster
+ * of up to 8 blocks through distributed shared memory, in the same fixed order as
+ * bsf8_gemm_partials followed by bsf8_splitk_reduce, which give the same bits.
  * The kernel may prefetch w8/exp into L2 before the preceding kernel on the stream has
  * finished (programmatic dependent launch); it reads x and writes y only after it.
  * Errors: BSF8_ERR_NULL, BSF8_ERR_SHAPE, BSF8_ERR_ALIGN, BSF8_ERR_STRIDE,
@@ -121,7 +121,7 @@ int bsf8_gemm(const void *x, const uint8_t *w8, const uint8_t *exp, void *y,
               int M, int N, int K, int G, int split_k, int64_t ldx,
               void *workspace, size_t workspace_bytes, bsf8_stream_t stream);
 
-/* Workspace bsf8_gemm needs for these sizes (0 when split_k resolves to <= 8). */
+/* Workspace bsf8_gemm needs for these sizes (0 for most shapes; see bsf8_gemm). */
 size_t bsf8_gemm_workspace_bytes(int M, int N, int K, int G, int split_k);
 
 /* The split count bsf8_gemm uses for split_k = 0 (host only; no GPU needed).  Returns
@@ -176,8 +176,10 @@ int bsf8_device_status(int *status, bsf8_stream_t stream);
 enum {
     BSF8_OPT_PDL = 1,              /* 1 (default): programmatic dependent launch on    */
     BSF8_OPT_WAIT_TIMEOUT_NS = 2,  /* bound of every in-kernel wait (default 2e9 ns)   */
-    BSF8_OPT_DEBUG_SKIP_LOADS = 3  /* test only: GEMM issues no weight loads, so its   */
-                                   /* waits run out and it reports BSF8_ERR_TIMEOUT    */
+    BSF8_OPT_DEBUG_SKIP_LOADS = 3, /* test only: the TMA-ring GEMM issues no weight    */
+                                   /* loads, so its waits run out (BSF8_ERR_TIMEOUT)   */
+    BSF8_OPT_GEMM_PATH = 4         /* 0 (default): weight-streaming kernel; 1: the     */
+                                   /* shared-memory TMA-ring kernel (split_k <= 8)     */
 };
 /* Errors: BSF8_ERR_VALUE for an unknown option or a negative value. */
 int bsf8_set_option(int option, int64_t value);

@@ -77,12 +77,13 @@ def test_gemm_validation(lib):
     assert _gemm(lib, x=A + 2) == ALIGN
     assert _gemm(lib, w8=B + 8) == ALIGN
     assert _gemm(lib, ldx=2 * 4096 + 4) == ALIGN
-    # split_k > 8 runs through the workspace: missing or short workspace is rejected
-    assert _gemm(lib, S=16) == WORKSPACE
-    need = lib.bsf8_gemm_workspace_bytes(6, 1024, 4096, 2, 16)
-    assert need == 16 * 6 * 2 * 1024 * 4
-    assert _gemm(lib, S=16, ws=A, wsb=need - 1) == WORKSPACE
-    assert _gemm(lib, S=16, ws=A + 4, wsb=need) == ALIGN
+    # more than 64 column tasks per 16-row slab run through the workspace: a missing or
+    # short workspace is rejected
+    assert _gemm(lib, S=128) == WORKSPACE
+    need = lib.bsf8_gemm_workspace_bytes(6, 1024, 4096, 2, 128)
+    assert need == 128 * 6 * 2 * 1024 * 4
+    assert _gemm(lib, S=128, ws=A, wsb=need - 1) == WORKSPACE
+    assert _gemm(lib, S=128, ws=A + 4, wsb=need) == ALIGN
 
 
 def test_partials_reduce_pad_validation(lib):
@@ -122,10 +123,12 @@ def test_twin_and_dequant_validation(lib):
 
 
 def test_workspace_and_auto_split(lib):
-    # up to 8 splits run as one cluster: no workspace
-    assert lib.bsf8_gemm_workspace_bytes(6, 1024, 4096, 2, 8) == 0
-    assert lib.bsf8_gemm_workspace_bytes(6, 1024, 4096, 2, 0) == 0
-    assert lib.bsf8_gemm_workspace_bytes(6, 1024, 4096, 2, 9) == 9 * 6 * 2 * 1024 * 4
+    # up to 64 column tasks per slab are summed on chip: no workspace
+    for S in (0, 1, 8, 9, 16, 64):
+        assert lib.bsf8_gemm_workspace_bytes(6, 1024, 4096, 2, S) == 0, S
+    assert lib.bsf8_gemm_workspace_bytes(6, 1024, 4096, 2, 65) == 65 * 6 * 2 * 1024 * 4
+    # very long splits need more than 8 tasks each: K = 65536 in 16 splits
+    assert lib.bsf8_gemm_workspace_bytes(6, 64, 65536, 1, 16) == 16 * 6 * 64 * 4
     # wo_a (16 tiles x 2 groups): 8 splits, as on the page (grid (16, G, 8))
     assert lib.bsf8_gemm_auto_split(6, 1024, 4096, 2) == 8
     # the head-like shape has enough tiles for one split

@@ -124,8 +124,10 @@ def test_head_sweep_sampled(bsf8_lib, M):
     (3, 96, 160, 7, 2, 8),         # three groups, row stride > G*K
     (2, 160, 544, 13, 8, 0),       # 17 blocks in 8 splits: chunk 3, two empty splits
     (1, 64, 576, 33, 5, 24),       # two token chunks of 32
-    (1, 64, 1024, 9, 32, 0),       # one block per split (workspace path)
-    (2, 128, 2048, 5, 12, 0),      # workspace path, uneven splits
+    (1, 64, 1024, 9, 32, 0),       # one block per split: a cluster of 4 blocks
+    (2, 128, 2048, 5, 12, 0),      # uneven splits
+    (1, 64, 2560, 9, 80, 0),       # 80 tasks per slab: partials + reduce (workspace)
+    (1, 96, 65536 // 8, 2, 1, 0),  # a long single split: 8 tasks of 1024 columns
     (1, 4096, 64, 192, 2, 0),      # the largest M
 ])
 def test_ragged_and_edge_shapes(bsf8_lib, G, N, K, M, S, pad):
@@ -236,3 +238,22 @@ def test_sequence_of_calls_matches_oracle(bsf8_lib):
     for x, y in zip(xs, ys):
         assert np.array_equal(bf16_bits(y), bf16_bits(bsf8.gemm(to_dev_bf16(x), w8_d, ex_d, split_k=4)))
         assert_gemm_close(bf16_bits(y), oracle.gemm(x, w8, ex))
+
+
+@pytest.mark.parametrize("wk,M,S", [(wl.WO_A, 6, 8), (wl.TINY, 4, 1), (wl.DOWN_PROJ, 6, 4),
+                                    (wl.MID, 40, 2)])
+def test_tma_ring_path_matches_oracle_and_its_two_pass(bsf8_lib, wk, M, S):
+    """The optional shared-memory TMA-ring kernel (BSF8_OPT_GEMM_PATH = 1)."""
+    w8, ex = wk.weights()
+    x = wk.x(M=M)
+    w8_d, ex_d, x_d = dev(w8, ex, x)
+    bsf8.set_option(bsf8.OPT_GEMM_PATH, 1)
+    try:
+        y = run(x_d, w8_d, ex_d, S)
+        two = bf16_bits(bsf8.splitk_reduce(bsf8.gemm_partials(x_d, w8_d, ex_d, S)))
+        assert bsf8.device_status() == 0
+    finally:
+        bsf8.set_option(bsf8.OPT_GEMM_PATH, 0)
+    assert np.array_equal(y, two)
+    rows = [0, M - 1]
+    assert_gemm_close(y[rows], oracle.gemm(x[rows], w8, ex))
