@@ -57,6 +57,9 @@ def parse_args(argv=None):
     p.add_argument("--profile-calls", type=int, default=0,
                    help="profiling mode: run this many eager layer calls and exit (no JSON)")
     p.add_argument("--split-k", type=int, default=None, help="override the workload's split_k")
+    p.add_argument("--workload", choices=("wo_a", "down_proj", "mid", "gate_up", "head"),
+                   default="wo_a", help="profiling mode only: which workload to run")
+    p.add_argument("--m", type=int, default=None, help="profiling mode only: token rows")
     return p.parse_args(argv)
 
 
@@ -269,10 +272,10 @@ def run_reference(args, world, rank):
     }
 
 
-def build_layers(wk, device):
+def build_layers(wk, device, copies=LAYERS):
     import torch
     layers = []
-    for c in range(LAYERS):
+    for c in range(copies):
         w8, ex = wk.weights(copy=c)
         x = wk.x(copy=c)
         layers.append((torch.from_numpy(w8).to(device), torch.from_numpy(ex).to(device),
@@ -387,15 +390,21 @@ def main(argv=None):
     bsf8_build.build()
     bsf8.load()
     wk = workload()
+    if args.profile_calls:
+        from block_scaled_fp8_weight_gb300 import workloads as wl
+        wk = {"wo_a": wl.WO_A, "down_proj": wl.DOWN_PROJ, "mid": wl.MID, "gate_up": wl.GATE_UP,
+              "head": wl.HEAD}[args.workload]
+    import dataclasses
     if args.split_k is not None:
-        import dataclasses
         wk = dataclasses.replace(wk, split_k=args.split_k)
-    layers = build_layers(wk, device)
+    if args.m is not None:
+        wk = dataclasses.replace(wk, M=args.m)
+    layers = build_layers(wk, device, copies=LAYERS if wk.copies > 1 else 3)
     stream = torch.cuda.Stream(device=device)
     if args.profile_calls:
         with torch.cuda.stream(stream):
             for i in range(args.profile_calls):
-                w8, ex, x = layers[i % LAYERS]
+                w8, ex, x = layers[i % len(layers)]
                 bsf8.gemm(x, w8, ex, split_k=wk.split_k)
         torch.cuda.synchronize(device)
         return 0
