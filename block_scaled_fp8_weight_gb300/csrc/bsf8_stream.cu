@@ -52,14 +52,6 @@ struct StreamParams {
 constexpr int kStreamWarps = 8;
 constexpr int kStreamThreads = kStreamWarps * 32;
 
-__device__ __forceinline__ uint4 ldg_stream(const void *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
 __device__ __forceinline__ uint4 ldg_v4(const void *p) {
     uint4 v;
     asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -74,115 +66,118 @@ __device__ __forceinline__ uint32_t ldg_u8(const uint8_t *p) {
     return v;
 }
 
-// Rebuilds 4 codes and flags e4m3 NaN codes: after the shift-and-mask a NaN code has
-// magnitude bits 0x07F0, the only pattern for which adding 0x0010 carries into bit 11.
-__device__ __forceinline__ void rebuild4_flag(uint32_t w, const Scale &s, uint32_t &lo,
-                                              uint32_t &hi, uint32_t &flag) {
-    uint32_t t0, t1;
+// 16-byte asynchronous copy global -> shared (L2 only); src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint32_t bf16x2_max_abs(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Shifted-and-masked codes (bf16 bits of e4m3 * 2^-120) for the four codes of w.
+__device__ __forceinline__ void spread4(uint32_t w, uint32_t &t0, uint32_t &t1) {
     asm("prmt.b32 %0, %1, 0, 0x9180;" : "=r"(t0) : "r"(w));
     asm("prmt.b32 %0, %1, 0, 0xB3A2;" : "=r"(t1) : "r"(w));
     t0 = (t0 << 4) & 0x87F087F0u;
     t1 = (t1 << 4) & 0x87F087F0u;
-    flag |= (t0 + 0x00100010u) | (t1 + 0x00100010u);
-    lo = bf16x2_mul(t0, s.s1);
-    hi = bf16x2_mul(t1, s.s1);
-    if (s.two) {
-        lo = bf16x2_mul(lo, s.s2);
-        hi = bf16x2_mul(hi, s.s2);
-    }
 }
 
-// Step width: 128 columns (thread covers 32) for up to two token tiles, else 64 (16).
+// Step geometry: one weight row piece per thread per step.
+//   NT8 == 1: 128-column steps, a thread owns 32 columns (8 MMAs per step);
+//   NT8 >= 2: 64-column steps, a thread owns 16 columns (4 MMAs per step).
 template <int NT8>
 struct StepCfg {
-    static constexpr int KS = NT8 <= 2 ? 128 : 64;
-    static constexpr int TC = KS / 4;      // columns per thread per step
-    static constexpr int WV = TC / 16;     // 16-byte weight vectors per row per step
-    static constexpr int XV = TC / 8;      // 16-byte x vectors per token row per step
-    static constexpr int MMAS = TC / 4;    // MMAs per step (each takes 4 columns/thread)
+    static constexpr int KS = NT8 == 1 ? 128 : 64;
+    static constexpr int TC = KS / 4;                 // columns per thread per step
+    static constexpr int WV = TC / 16;                // 16-byte vectors per row per thread
+    static constexpr int XV = TC / 8;                 // 16-byte x vectors per token row
+    static constexpr int MMAS = TC / 4;               // MMAs per step per token tile
+    static constexpr int PITCH = KS == 128 ? 144 : 64;  // smem row pitch (conflict-free)
+    static constexpr int STAGE = 16 * PITCH;          // one warp's stage: 16 rows
+    static constexpr int DEPTH = KS == 128 ? 4 : 6;   // stages per warp ring
+    static constexpr int CPL = 16 * KS / 16 / 32;    // 16-byte copies per lane per step
+    static constexpr int ACC = NT8 == 1 ? 2 : 1;      // accumulator sets (MMA chain split)
 };
 
 template <int NT8>
-struct StepBuf {
-    uint4 wa[StepCfg<NT8>::WV];           // row r
-    uint4 wb[StepCfg<NT8>::WV];           // row r + 8
-    uint4 xv[NT8][StepCfg<NT8>::XV];      // token rows of each n8 tile
-    uint32_t e;                           // exponent byte of this thread's block
-    bool valid;
+struct XBuf {
+    uint4 v[NT8][StepCfg<NT8>::XV];
+    uint32_t e;
 };
 
-template <int NT8>
-__device__ __forceinline__ void load_step(StepBuf<NT8> &b, const StreamParams &p, int g, int n_r,
-                                          int mbase, int lane, int kcol, int k1) {
+template <int NT8, bool TWO>
+__device__ __forceinline__ void compute_step(const uint8_t *stage, int r, int q, const XBuf<NT8> &xb,
+                                             float (&acc)[StepCfg<NT8>::ACC][NT8][4]) {
     using C = StepCfg<NT8>;
-    b.valid = kcol < k1;
-    if (b.valid) {
-        const uint8_t *ra = p.w8 + ((size_t)g * p.N + n_r) * p.K + kcol;
-        const uint8_t *rb = ra + (size_t)8 * p.K;
+    uint32_t wa[4 * C::WV], wb[4 * C::WV];
 #pragma unroll
-        for (int v = 0; v < C::WV; ++v) {
-            b.wa[v] = ldg_stream(ra + 16 * v);
-            b.wb[v] = ldg_stream(rb + 16 * v);
-        }
-        b.e = ldg_u8(p.ex + ((size_t)g * (p.N / 32) + n_r / 32) * (p.K / 32) + kcol / 32);
-#pragma unroll
-        for (int j = 0; j < NT8; ++j) {
-            const int m = mbase + j * 8 + (lane >> 2);
-            if (m < p.M) {
-                const uint16_t *src = p.x + (size_t)m * p.ldx + (size_t)g * p.K + kcol;
-#pragma unroll
-                for (int v = 0; v < C::XV; ++v) b.xv[j][v] = ldg_v4(src + 8 * v);
-            } else {
-#pragma unroll
-                for (int v = 0; v < C::XV; ++v) b.xv[j][v] = make_uint4(0, 0, 0, 0);
-            }
-        }
-    } else {
-#pragma unroll
-        for (int v = 0; v < C::WV; ++v) b.wa[v] = b.wb[v] = make_uint4(0, 0, 0, 0);
-        b.e = 127;
-#pragma unroll
-        for (int j = 0; j < NT8; ++j)
-#pragma unroll
-            for (int v = 0; v < C::XV; ++v) b.xv[j][v] = make_uint4(0, 0, 0, 0);
+    for (int v = 0; v < C::WV; ++v) {
+        const uint4 a = *reinterpret_cast<const uint4 *>(stage + r * C::PITCH + q * C::TC + 16 * v);
+        const uint4 b = *reinterpret_cast<const uint4 *>(stage + (r + 8) * C::PITCH + q * C::TC + 16 * v);
+        wa[4 * v] = a.x; wa[4 * v + 1] = a.y; wa[4 * v + 2] = a.z; wa[4 * v + 3] = a.w;
+        wb[4 * v] = b.x; wb[4 * v + 1] = b.y; wb[4 * v + 2] = b.z; wb[4 * v + 3] = b.w;
     }
-}
-
-__device__ __forceinline__ uint32_t u4_word(const uint4 &v, int i) {
-    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
-}
-
-template <int NT8>
-__device__ __forceinline__ void compute_step(const StepBuf<NT8> &b, float (&acc)[2][NT8][4]) {
-    using C = StepCfg<NT8>;
-    const Scale sc = make_scale(b.e);
-    uint32_t flag = 0;
+    const Scale sc = make_scale(xb.e);
+    uint32_t s1 = sc.s1, s2 = sc.s2;
+    if (TWO) {  // exact for every exponent byte: restore e4m3 * 1, then scale by 2^(e-127)
+        s1 = 0x7B807B80u;
+        const uint32_t b = xb.e == 0 ? 0x0040u : (xb.e << 7);
+        s2 = b | (b << 16);
+    }
     uint32_t alo[C::MMAS], ahi[C::MMAS], blo[C::MMAS], bhi[C::MMAS];
+    uint32_t mx = 0;
 #pragma unroll
     for (int j = 0; j < C::MMAS; ++j) {
-        rebuild4_flag(u4_word(b.wa[j / 4], j % 4), sc, alo[j], ahi[j], flag);
-        rebuild4_flag(u4_word(b.wb[j / 4], j % 4), sc, blo[j], bhi[j], flag);
+        uint32_t t0, t1, u0, u1;
+        spread4(wa[j], t0, t1);
+        spread4(wb[j], u0, u1);
+        mx = bf16x2_max_abs(mx, bf16x2_max_abs(t0, t1));
+        mx = bf16x2_max_abs(mx, bf16x2_max_abs(u0, u1));
+        alo[j] = bf16x2_mul(t0, s1);
+        ahi[j] = bf16x2_mul(t1, s1);
+        blo[j] = bf16x2_mul(u0, s1);
+        bhi[j] = bf16x2_mul(u1, s1);
+        if (TWO) {
+            alo[j] = bf16x2_mul(alo[j], s2);
+            ahi[j] = bf16x2_mul(ahi[j], s2);
+            blo[j] = bf16x2_mul(blo[j], s2);
+            bhi[j] = bf16x2_mul(bhi[j], s2);
+        }
     }
-    if (flag & 0x08000800u) {  // an e4m3 NaN code is present (cold path)
+    // An e4m3 NaN code rebuilds to the bf16 pattern 0x07F0, above every finite code's
+    // 0x07E0 (448 * 2^-120): patch it to NaN on this cold path.
+    if ((mx & 0x7FFFu) >= 0x07F0u || ((mx >> 16) & 0x7FFFu) >= 0x07F0u) {
 #pragma unroll
         for (int j = 0; j < C::MMAS; ++j) {
-            patch_nan_codes(u4_word(b.wa[j / 4], j % 4), alo[j], ahi[j]);
-            patch_nan_codes(u4_word(b.wb[j / 4], j % 4), blo[j], bhi[j]);
+            patch_nan_codes(wa[j], alo[j], ahi[j]);
+            patch_nan_codes(wb[j], blo[j], bhi[j]);
         }
     }
 #pragma unroll
     for (int j = 0; j < C::MMAS; ++j)
 #pragma unroll
         for (int t = 0; t < NT8; ++t) {
-            // thread's x words: word i holds columns (2i, 2i+1) of its TC columns
-            const uint32_t b0 = u4_word(b.xv[t][(2 * j) / 4], (2 * j) % 4);
-            const uint32_t b1 = u4_word(b.xv[t][(2 * j + 1) / 4], (2 * j + 1) % 4);
-            mma_bf16_16816(acc[j & 1][t], alo[j], blo[j], ahi[j], bhi[j], b0, b1);
+            // x word i holds the thread's columns (2i, 2i+1); MMA j takes 4j .. 4j+3
+            const uint4 &xv0 = xb.v[t][(2 * j) / 4];
+            const uint32_t b0 = ((2 * j) % 4) == 0 ? xv0.x : xv0.z;
+            const uint32_t b1 = ((2 * j) % 4) == 0 ? xv0.y : xv0.w;
+            mma_bf16_16816(acc[j % C::ACC][t], alo[j], blo[j], ahi[j], bhi[j], b0, b1);
         }
 }
 
 template <int NT8>
-__global__ void __launch_bounds__(kStreamThreads) stream_kernel(const __grid_constant__ StreamParams p) {
+__global__ void __launch_bounds__(kStreamThreads, NT8 <= 2 ? 2 : 1)
+    stream_kernel(const __grid_constant__ StreamParams p) {
     using C = StepCfg<NT8>;
     constexpr int MT = 8 * NT8;
     __shared__ __align__(16) float red[kStreamWarps][16][MT];  // per-warp task partials
@@ -234,37 +229,98 @@ __global__ void __launch_bounds__(kStreamThreads) stream_kernel(const __grid_con
     }
     pdl_wait();
 
-    float acc[2][NT8][4];
+    float acc[C::ACC][NT8][4];
 #pragma unroll
-    for (int a = 0; a < 2; ++a)
+    for (int a = 0; a < C::ACC; ++a)
 #pragma unroll
         for (int t = 0; t < NT8; ++t)
 #pragma unroll
             for (int c = 0; c < 4; ++c) acc[a][t][c] = 0.0f;
 
     if (active && k1 > k0) {
+        extern __shared__ __align__(128) uint8_t ring_smem[];
+        uint8_t *ring = ring_smem + warp * C::DEPTH * C::STAGE;
         const int nsteps = (k1 - k0 + C::KS - 1) / C::KS;
-        StepBuf<NT8> b0, b1;
-        load_step<NT8>(b0, p, g, n_r, mbase, lane, k0 + q * C::TC, k1);
-        int t = 0;
-        for (; t + 2 <= nsteps; t += 2) {
-            load_step<NT8>(b1, p, g, n_r, mbase, lane, k0 + (t + 1) * C::KS + q * C::TC, k1);
-            compute_step<NT8>(b0, acc);
-            if (t + 2 < nsteps)
-                load_step<NT8>(b0, p, g, n_r, mbase, lane, k0 + (t + 2) * C::KS + q * C::TC, k1);
-            compute_step<NT8>(b1, acc);
+        const int r = lane >> 2;
+        // weight copies: lane copies 16-byte chunk (lane % cpr) of rows crow + i * rows_per
+        constexpr int cpr = C::KS / 16;
+        constexpr int rows_per = 32 / cpr;
+        const int crow = lane / cpr, ccol = (lane % cpr) * 16;
+        const uint8_t *wsrc = p.w8 + ((size_t)g * p.N + slab * 16 + crow) * p.K + k0 + ccol;
+        const size_t rstride = (size_t)rows_per * p.K;
+        // token rows >= M read row M-1 instead: their outputs are never stored
+        const uint16_t *xsrc[NT8];
+#pragma unroll
+        for (int t = 0; t < NT8; ++t) {
+            const int m = min(mbase + t * 8 + r, p.M - 1);
+            xsrc[t] = p.x + (size_t)m * p.ldx + (size_t)g * p.K + k0 + q * C::TC;
         }
-        if (t < nsteps) compute_step<NT8>(b0, acc);
+        const uint8_t *esrc =
+            p.ex + ((size_t)g * (p.N / 32) + slab / 2) * (p.K / 32) + (k0 + q * C::TC) / 32;
+
+        auto issue = [&](int t) {
+            uint8_t *st = ring + (t % C::DEPTH) * C::STAGE;
+            const bool in = k0 + t * C::KS + ccol < k1;
+            const uint8_t *src = in ? wsrc + (size_t)t * C::KS : wsrc;  // zero-fill reads nothing
+#pragma unroll
+            for (int i = 0; i < C::CPL; ++i)
+                cp_async16(st + (crow + i * rows_per) * C::PITCH + ccol, src + i * rstride,
+                           in ? 16u : 0u);
+        };
+        auto load_x = [&](XBuf<NT8> &xb, int t) {
+            if (k0 + t * C::KS + q * C::TC < k1) {
+#pragma unroll
+                for (int tt = 0; tt < NT8; ++tt)
+#pragma unroll
+                    for (int v = 0; v < C::XV; ++v) xb.v[tt][v] = ldg_v4(xsrc[tt] + t * C::KS + 8 * v);
+                xb.e = ldg_u8(esrc + t * (C::KS / 32));
+            } else {
+#pragma unroll
+                for (int tt = 0; tt < NT8; ++tt)
+#pragma unroll
+                    for (int v = 0; v < C::XV; ++v) xb.v[tt][v] = make_uint4(0, 0, 0, 0);
+                xb.e = 127;
+            }
+        };
+        auto step = [&](int t, const XBuf<NT8> &cur, XBuf<NT8> &nxt) {
+            __syncwarp();  // every lane is done with the stage that step t+DEPTH-1 refills
+            if (t + C::DEPTH - 1 < nsteps) issue(t + C::DEPTH - 1);
+            cp_async_commit();
+            if (t + 1 < nsteps) load_x(nxt, t + 1);
+            cp_async_wait<C::DEPTH - 1>();
+            __syncwarp();  // step t's stage has landed for every lane
+            const uint8_t *st = ring + (t % C::DEPTH) * C::STAGE;
+            if (__any_sync(0xFFFFFFFFu, cur.e > 134u))
+                compute_step<NT8, true>(st, r, q, cur, acc);
+            else
+                compute_step<NT8, false>(st, r, q, cur, acc);
+        };
+
+#pragma unroll
+        for (int i = 0; i < C::DEPTH - 1; ++i) {
+            if (i < nsteps) issue(i);
+            cp_async_commit();
+        }
+        XBuf<NT8> xa, xb;
+        load_x(xa, 0);
+        int t = 0;
+        for (; t + 1 < nsteps; t += 2) {
+            step(t, xa, xb);
+            step(t + 1, xb, xa);
+        }
+        if (t < nsteps) step(t, xa, xb);
+        cp_async_wait<0>();
     }
 
     // ---- task partial -> shared memory (rows = weight rows, columns = tokens)
 #pragma unroll
     for (int t = 0; t < NT8; ++t) {
+        float v[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) v[c] = C::ACC == 2 ? acc[0][t][c] + acc[C::ACC - 1][t][c] : acc[0][t][c];
         const int row = lane >> 2, col = t * 8 + 2 * q;
-        *reinterpret_cast<float2 *>(&red[warp][row][col]) =
-            make_float2(acc[0][t][0] + acc[1][t][0], acc[0][t][1] + acc[1][t][1]);
-        *reinterpret_cast<float2 *>(&red[warp][row + 8][col]) =
-            make_float2(acc[0][t][2] + acc[1][t][2], acc[0][t][3] + acc[1][t][3]);
+        *reinterpret_cast<float2 *>(&red[warp][row][col]) = make_float2(v[0], v[1]);
+        *reinterpret_cast<float2 *>(&red[warp][row + 8][col]) = make_float2(v[2], v[3]);
     }
     const int mrows = min(MT, p.M - mbase);
 
@@ -370,7 +426,19 @@ cudaError_t launch_stream_nt8(const StreamPlan &pl, const StreamParams &prm, cud
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)pl.grid_x, (unsigned)(prm.G * pl.m_chunks), 1);
     cfg.blockDim = dim3(kStreamThreads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    const size_t smem = (size_t)kStreamWarps * StepCfg<NT8>::DEPTH * StepCfg<NT8>::STAGE;
+    static int configured[64] = {0};  // per device: dynamic shared memory limit raised
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!__atomic_load_n(&configured[dev], __ATOMIC_ACQUIRE)) {
+        e = cudaFuncSetAttribute(stream_kernel<NT8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        __atomic_store_n(&configured[dev], 1, __ATOMIC_RELEASE);
+    }
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attrs[2];
     int na = 0;
