@@ -104,7 +104,7 @@ struct StepCfg {
     static constexpr int MMAS = TC / 4;               // MMAs per step per token tile
     static constexpr int PITCH = KS == 128 ? 144 : 64;  // smem row pitch (conflict-free)
     static constexpr int STAGE = 16 * PITCH;          // one warp's stage: 16 rows
-    static constexpr int DEPTH = KS == 128 ? 4 : 6;   // stages per warp ring
+    static constexpr int DEPTH = KS == 128 ? 5 : 9;   // stages per warp ring
     static constexpr int CPL = 16 * KS / 16 / 32;    // 16-byte copies per lane per step
     static constexpr int ACC = NT8 == 1 ? 2 : 1;      // accumulator sets (MMA chain split)
 };
@@ -217,17 +217,8 @@ __global__ void __launch_bounds__(kStreamThreads, NT8 <= 2 ? 2 : 1)
         k0 = min(s_hi, s_lo + u * p.kt);
         k1 = min(s_hi, k0 + p.kt);
     }
-    const int n_r = slab * 16 + (lane >> 2);  // this thread's rows: n_r and n_r + 8
 
     pdl_trigger();
-    if (active && k1 > k0 && (lane >> 2) < 2) {
-        // Lanes 0..7 prefetch the warp's 16 weight rows into L2 before the dependency wait.
-        const int r = slab * 16 + lane * 2;
-        const uint8_t *base = p.w8 + ((size_t)g * p.N + r) * p.K + k0;
-        prefetch_l2(base, (uint32_t)(k1 - k0));
-        prefetch_l2(base + p.K, (uint32_t)(k1 - k0));
-    }
-    pdl_wait();
 
     float acc[C::ACC][NT8][4];
 #pragma unroll
@@ -237,17 +228,49 @@ __global__ void __launch_bounds__(kStreamThreads, NT8 <= 2 ? 2 : 1)
 #pragma unroll
             for (int c = 0; c < 4; ++c) acc[a][t][c] = 0.0f;
 
-    if (active && k1 > k0) {
-        extern __shared__ __align__(128) uint8_t ring_smem[];
-        uint8_t *ring = ring_smem + warp * C::DEPTH * C::STAGE;
-        const int nsteps = (k1 - k0 + C::KS - 1) / C::KS;
-        const int r = lane >> 2;
-        // weight copies: lane copies 16-byte chunk (lane % cpr) of rows crow + i * rows_per
-        constexpr int cpr = C::KS / 16;
-        constexpr int rows_per = 32 / cpr;
-        const int crow = lane / cpr, ccol = (lane % cpr) * 16;
-        const uint8_t *wsrc = p.w8 + ((size_t)g * p.N + slab * 16 + crow) * p.K + k0 + ccol;
-        const size_t rstride = (size_t)rows_per * p.K;
+    const bool work = active && k1 > k0;
+    extern __shared__ __align__(128) uint8_t ring_smem[];
+    uint8_t *ring = ring_smem + warp * C::DEPTH * C::STAGE;
+    const int nsteps = work ? (k1 - k0 + C::KS - 1) / C::KS : 0;
+    const int r = lane >> 2;
+    // weight copies: lane copies 16-byte chunk (lane % cpr) of rows crow + i * rows_per
+    constexpr int cpr = C::KS / 16;
+    constexpr int rows_per = 32 / cpr;
+    const int crow = lane / cpr, ccol = (lane % cpr) * 16;
+    const uint8_t *wsrc = p.w8 + ((size_t)g * p.N + slab * 16 + crow) * p.K + k0 + ccol;
+    const size_t rstride = (size_t)rows_per * p.K;
+    const uint8_t *esrc =
+        p.ex + ((size_t)g * (p.N / 32) + slab / 2) * (p.K / 32) + (k0 + q * C::TC) / 32;
+
+    auto issue = [&](int t) {
+        uint8_t *st = ring + (t % C::DEPTH) * C::STAGE;
+        const bool in = k0 + t * C::KS + ccol < k1;
+        const uint8_t *src = in ? wsrc + (size_t)t * C::KS : wsrc;  // zero-fill reads nothing
+#pragma unroll
+        for (int i = 0; i < C::CPL; ++i)
+            cp_async16(st + (crow + i * rows_per) * C::PITCH + ccol, src + i * rstride,
+                       in ? 16u : 0u);
+    };
+
+    // The twin is a static parameter: the first DEPTH-1 steps of this warp's weight rows
+    // are copied into its ring, and the rest of the task and its exponents prefetched into
+    // L2, before waiting for the preceding kernel (whose outputs include x).
+#pragma unroll
+    for (int i = 0; i < C::DEPTH - 1; ++i) {
+        if (i < nsteps) issue(i);
+        cp_async_commit();
+    }
+    if (work) {
+        if (nsteps > C::DEPTH - 1 && lane < 16) {
+            const int rest = (C::DEPTH - 1) * C::KS;
+            prefetch_l2(p.w8 + ((size_t)g * p.N + slab * 16 + lane) * p.K + k0 + rest,
+                        (uint32_t)(k1 - k0 - rest));
+        }
+        if (lane == 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(esrc) : "memory");
+    }
+    pdl_wait();
+
+    if (work) {
         // token rows >= M read row M-1 instead: their outputs are never stored
         const uint16_t *xsrc[NT8];
 #pragma unroll
@@ -255,18 +278,6 @@ __global__ void __launch_bounds__(kStreamThreads, NT8 <= 2 ? 2 : 1)
             const int m = min(mbase + t * 8 + r, p.M - 1);
             xsrc[t] = p.x + (size_t)m * p.ldx + (size_t)g * p.K + k0 + q * C::TC;
         }
-        const uint8_t *esrc =
-            p.ex + ((size_t)g * (p.N / 32) + slab / 2) * (p.K / 32) + (k0 + q * C::TC) / 32;
-
-        auto issue = [&](int t) {
-            uint8_t *st = ring + (t % C::DEPTH) * C::STAGE;
-            const bool in = k0 + t * C::KS + ccol < k1;
-            const uint8_t *src = in ? wsrc + (size_t)t * C::KS : wsrc;  // zero-fill reads nothing
-#pragma unroll
-            for (int i = 0; i < C::CPL; ++i)
-                cp_async16(st + (crow + i * rows_per) * C::PITCH + ccol, src + i * rstride,
-                           in ? 16u : 0u);
-        };
         auto load_x = [&](XBuf<NT8> &xb, int t) {
             if (k0 + t * C::KS + q * C::TC < k1) {
 #pragma unroll
@@ -296,11 +307,6 @@ __global__ void __launch_bounds__(kStreamThreads, NT8 <= 2 ? 2 : 1)
                 compute_step<NT8, false>(st, r, q, cur, acc);
         };
 
-#pragma unroll
-        for (int i = 0; i < C::DEPTH - 1; ++i) {
-            if (i < nsteps) issue(i);
-            cp_async_commit();
-        }
         XBuf<NT8> xa, xb;
         load_x(xa, 0);
         int t = 0;
@@ -309,8 +315,8 @@ __global__ void __launch_bounds__(kStreamThreads, NT8 <= 2 ? 2 : 1)
             step(t + 1, xb, xa);
         }
         if (t < nsteps) step(t, xa, xb);
-        cp_async_wait<0>();
     }
+    cp_async_wait<0>();
 
     // ---- task partial -> shared memory (rows = weight rows, columns = tokens)
 #pragma unroll
@@ -387,12 +393,13 @@ StreamPlan plan_stream(int M, int N, int K, int G, int S, bool partials) {
     StreamPlan pl{};
     pl.nt8 = std::min(4, (M + 7) / 8);
     pl.m_chunks = (M + 8 * pl.nt8 - 1) / (8 * pl.nt8);
-    const int ks = pl.nt8 <= 2 ? 128 : 64;
+    const int ks = pl.nt8 == 1 ? 128 : 64;
     const int nkb = K / 32;
     pl.S = S;
     pl.chunk_cols = ((nkb + S - 1) / S) * 32;
-    // Task width: at least two steps, and at most 8 tasks per split.
-    int kt = std::max(2 * ks, (pl.chunk_cols + 7) / 8);
+    // Task width: at least 512 columns (every step of such a task is in the warp's ring
+    // before the dependency wait), and at most 8 tasks per split.
+    int kt = std::max(512, (pl.chunk_cols + 7) / 8);
     kt = (kt + ks - 1) / ks * ks;
     pl.kt = kt;
     pl.tps = (pl.chunk_cols + kt - 1) / kt;

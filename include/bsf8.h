@@ -113,8 +113,11 @@ int bsf8_dequant(const uint8_t *w8, const uint8_t *exp, void *out, int G, int N,
  * The partials of a 16-row slab are summed inside one thread block, or across a cluster
  * of up to 8 blocks through distributed shared memory, in the same fixed order as
  * bsf8_gemm_partials followed by bsf8_splitk_reduce, which give the same bits.
- * The kernel may prefetch w8/exp into L2 before the preceding kernel on the stream has
- * finished (programmatic dependent launch); it reads x and writes y only after it.
+ * The twin is treated as a static parameter: with programmatic dependent launch
+ * (BSF8_OPT_PDL) the kernel starts reading w8 and exp while the kernel before it on the
+ * stream may still run, if that kernel allows it (the library's kernels that write a
+ * twin -- make_twin, pad_k -- never do; a caller's kernel that writes w8 or exp must not
+ * trigger its dependents early).  x is read and y written only after that kernel ends.
  * Errors: BSF8_ERR_NULL, BSF8_ERR_SHAPE, BSF8_ERR_ALIGN, BSF8_ERR_STRIDE,
  *         BSF8_ERR_WORKSPACE, BSF8_ERR_CUDA. */
 int bsf8_gemm(const void *x, const uint8_t *w8, const uint8_t *exp, void *y,
