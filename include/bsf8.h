@@ -148,6 +148,31 @@ int bsf8_gemm_partials(const void *x, const uint8_t *w8, const uint8_t *exp,
 int bsf8_splitk_reduce(const float *partials, void *y, int S, int64_t count,
                        bsf8_stream_t stream);
 
+/* --------------------------------------------------- GEMM without a workspace
+ * The pages have no counterpart for this entry point; it serves callers that cannot
+ * allocate device memory for a workspace -- e.g. a serving engine that has reserved all of
+ * the GPU's memory for its own arena, or a plugin running inside one that may not call
+ * the allocator.  It computes exactly what bsf8_gemm computes (same arguments, same
+ * fixed-order split-K sum) as two passes -- the fp32 partials, then the fixed-order
+ * reduce -- with the partials held in a buffer compiled into the library:
+ *   - the buffer is BSF8_STATIC_SCRATCH_BYTES (8 MiB) of device memory that every GPU
+ *     which loads the library holds until the process exits;
+ *   - a call whose partials S*M*G*N*4 bytes (S = the split count used) exceed it returns
+ *     BSF8_ERR_WORKSPACE without launching anything;
+ *   - nothing is allocated and nothing needs clearing: every split writes all of its
+ *     partials before the reduce reads them;
+ *   - every call on a device shares that one buffer, so calls that can overlap on the GPU
+ *     (on different streams, or on several host threads) race and must be serialised by
+ *     the caller;
+ *   - the first call on a device looks up the buffer's device address (a host call,
+ *     cudaGetSymbolAddress), so make that first call before any stream capture.
+ * Errors: as bsf8_gemm (BSF8_ERR_WORKSPACE as described). */
+#define BSF8_STATIC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+int bsf8_gemm_static_scratch(const void *x, const uint8_t *w8, const uint8_t *exp, void *y,
+                             int M, int N, int K, int G, int split_k, int64_t ldx,
+                             bsf8_stream_t stream);
+
 /* ------------------------------------------------------------------------- pad-K
  * "shared_pad_k.py", _pad_weight(): the twin [G][N][K] becomes [G][N][Kp] with code 0
  * (+0) in the new columns and its exponents [G][N/32][K/32] become [G][N/32][Kp/32]
