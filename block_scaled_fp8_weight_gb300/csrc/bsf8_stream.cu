@@ -115,18 +115,15 @@ struct XBuf {
     uint32_t e;
 };
 
+// One step of a warp task: rebuild the thread's codes of rows r and r+8 and feed each
+// word straight into its MMAs.  mxa / mxb collect the largest rebuilt magnitude of rows r /
+// r+8: an e4m3 NaN code rebuilds to the pattern 0x07F0, above every finite code's 0x07E0
+// (448 * 2^-120), so the task's rows holding one are set to NaN once, at the end.
 template <int NT8, bool TWO>
 __device__ __forceinline__ void compute_step(const uint8_t *stage, int r, int q, const XBuf<NT8> &xb,
-                                             float (&acc)[StepCfg<NT8>::ACC][NT8][4]) {
+                                             float (&acc)[StepCfg<NT8>::ACC][NT8][4],
+                                             uint32_t &mxa, uint32_t &mxb) {
     using C = StepCfg<NT8>;
-    uint32_t wa[4 * C::WV], wb[4 * C::WV];
-#pragma unroll
-    for (int v = 0; v < C::WV; ++v) {
-        const uint4 a = *reinterpret_cast<const uint4 *>(stage + r * C::PITCH + q * C::TC + 16 * v);
-        const uint4 b = *reinterpret_cast<const uint4 *>(stage + (r + 8) * C::PITCH + q * C::TC + 16 * v);
-        wa[4 * v] = a.x; wa[4 * v + 1] = a.y; wa[4 * v + 2] = a.z; wa[4 * v + 3] = a.w;
-        wb[4 * v] = b.x; wb[4 * v + 1] = b.y; wb[4 * v + 2] = b.z; wb[4 * v + 3] = b.w;
-    }
     const Scale sc = make_scale(xb.e);
     uint32_t s1 = sc.s1, s2 = sc.s2;
     if (TWO) {  // exact for every exponent byte: restore e4m3 * 1, then scale by 2^(e-127)
@@ -134,45 +131,40 @@ __device__ __forceinline__ void compute_step(const uint8_t *stage, int r, int q,
         const uint32_t b = xb.e == 0 ? 0x0040u : (xb.e << 7);
         s2 = b | (b << 16);
     }
-    uint32_t alo[C::MMAS], ahi[C::MMAS], blo[C::MMAS], bhi[C::MMAS];
-    uint32_t mx = 0;
 #pragma unroll
-    for (int j = 0; j < C::MMAS; ++j) {
-        uint32_t t0, t1, u0, u1;
-        spread4(wa[j], t0, t1);
-        spread4(wb[j], u0, u1);
-        mx = bf16x2_max_abs(mx, bf16x2_max_abs(t0, t1));
-        mx = bf16x2_max_abs(mx, bf16x2_max_abs(u0, u1));
-        alo[j] = bf16x2_mul(t0, s1);
-        ahi[j] = bf16x2_mul(t1, s1);
-        blo[j] = bf16x2_mul(u0, s1);
-        bhi[j] = bf16x2_mul(u1, s1);
-        if (TWO) {
-            alo[j] = bf16x2_mul(alo[j], s2);
-            ahi[j] = bf16x2_mul(ahi[j], s2);
-            blo[j] = bf16x2_mul(blo[j], s2);
-            bhi[j] = bf16x2_mul(bhi[j], s2);
+    for (int v = 0; v < C::WV; ++v) {
+        const uint4 a = *reinterpret_cast<const uint4 *>(stage + r * C::PITCH + q * C::TC + 16 * v);
+        const uint4 b = *reinterpret_cast<const uint4 *>(stage + (r + 8) * C::PITCH + q * C::TC + 16 * v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int j = 4 * v + i;
+            uint32_t t0, t1, u0, u1;
+            spread4(i == 0 ? a.x : i == 1 ? a.y : i == 2 ? a.z : a.w, t0, t1);
+            spread4(i == 0 ? b.x : i == 1 ? b.y : i == 2 ? b.z : b.w, u0, u1);
+            mxa = bf16x2_max_abs(mxa, bf16x2_max_abs(t0, t1));
+            mxb = bf16x2_max_abs(mxb, bf16x2_max_abs(u0, u1));
+            uint32_t alo = bf16x2_mul(t0, s1), ahi = bf16x2_mul(t1, s1);
+            uint32_t blo = bf16x2_mul(u0, s1), bhi = bf16x2_mul(u1, s1);
+            if (TWO) {
+                alo = bf16x2_mul(alo, s2);
+                ahi = bf16x2_mul(ahi, s2);
+                blo = bf16x2_mul(blo, s2);
+                bhi = bf16x2_mul(bhi, s2);
+            }
+#pragma unroll
+            for (int t = 0; t < NT8; ++t) {
+                // x word i holds the thread's columns (2i, 2i+1); MMA j takes 4j .. 4j+3
+                const uint4 &xv0 = xb.v[t][(2 * j) / 4];
+                const uint32_t b0 = ((2 * j) % 4) == 0 ? xv0.x : xv0.z;
+                const uint32_t b1 = ((2 * j) % 4) == 0 ? xv0.y : xv0.w;
+                mma_bf16_16816(acc[j % C::ACC][t], alo, blo, ahi, bhi, b0, b1);
+            }
         }
     }
-    // An e4m3 NaN code rebuilds to the bf16 pattern 0x07F0, above every finite code's
-    // 0x07E0 (448 * 2^-120): patch it to NaN on this cold path.
-    if ((mx & 0x7FFFu) >= 0x07F0u || ((mx >> 16) & 0x7FFFu) >= 0x07F0u) {
-#pragma unroll
-        for (int j = 0; j < C::MMAS; ++j) {
-            patch_nan_codes(wa[j], alo[j], ahi[j]);
-            patch_nan_codes(wb[j], blo[j], bhi[j]);
-        }
-    }
-#pragma unroll
-    for (int j = 0; j < C::MMAS; ++j)
-#pragma unroll
-        for (int t = 0; t < NT8; ++t) {
-            // x word i holds the thread's columns (2i, 2i+1); MMA j takes 4j .. 4j+3
-            const uint4 &xv0 = xb.v[t][(2 * j) / 4];
-            const uint32_t b0 = ((2 * j) % 4) == 0 ? xv0.x : xv0.z;
-            const uint32_t b1 = ((2 * j) % 4) == 0 ? xv0.y : xv0.w;
-            mma_bf16_16816(acc[j % C::ACC][t], alo[j], blo[j], ahi[j], bhi[j], b0, b1);
-        }
+}
+
+__device__ __forceinline__ bool has_nan_code(uint32_t mx) {
+    return (mx & 0x7FFFu) >= 0x07F0u || ((mx >> 16) & 0x7FFFu) >= 0x07F0u;
 }
 
 template <int NT8>
@@ -229,6 +221,7 @@ __global__ void __launch_bounds__(kStreamThreads, NT8 <= 2 ? 2 : 1)
             for (int c = 0; c < 4; ++c) acc[a][t][c] = 0.0f;
 
     const bool work = active && k1 > k0;
+    uint32_t mxa = 0, mxb = 0;  // largest rebuilt magnitudes of rows r and r+8
     extern __shared__ __align__(128) uint8_t ring_smem[];
     uint8_t *ring = ring_smem + warp * C::DEPTH * C::STAGE;
     const int nsteps = work ? (k1 - k0 + C::KS - 1) / C::KS : 0;
@@ -293,30 +286,52 @@ __global__ void __launch_bounds__(kStreamThreads, NT8 <= 2 ? 2 : 1)
                 xb.e = 127;
             }
         };
-        auto step = [&](int t, const XBuf<NT8> &cur, XBuf<NT8> &nxt) {
+        auto step = [&](int t, const XBuf<NT8> &cur, XBuf<NT8> &ahead) {
             __syncwarp();  // every lane is done with the stage that step t+DEPTH-1 refills
             if (t + C::DEPTH - 1 < nsteps) issue(t + C::DEPTH - 1);
             cp_async_commit();
-            if (t + 1 < nsteps) load_x(nxt, t + 1);
+            if (t + 2 < nsteps) load_x(ahead, t + 2);  // x two steps ahead
             cp_async_wait<C::DEPTH - 1>();
             __syncwarp();  // step t's stage has landed for every lane
             const uint8_t *st = ring + (t % C::DEPTH) * C::STAGE;
             if (__any_sync(0xFFFFFFFFu, cur.e > 134u))
-                compute_step<NT8, true>(st, r, q, cur, acc);
+                compute_step<NT8, true>(st, r, q, cur, acc, mxa, mxb);
             else
-                compute_step<NT8, false>(st, r, q, cur, acc);
+                compute_step<NT8, false>(st, r, q, cur, acc, mxa, mxb);
         };
 
-        XBuf<NT8> xa, xb;
-        load_x(xa, 0);
+        XBuf<NT8> x0, x1, x2;
+        load_x(x0, 0);
+        if (1 < nsteps) load_x(x1, 1);
         int t = 0;
-        for (; t + 1 < nsteps; t += 2) {
-            step(t, xa, xb);
-            step(t + 1, xb, xa);
+        for (; t + 3 <= nsteps; t += 3) {
+            step(t, x0, x2);
+            step(t + 1, x1, x0);
+            step(t + 2, x2, x1);
         }
-        if (t < nsteps) step(t, xa, xb);
+        if (t < nsteps) step(t, x0, x2);
+        if (t + 1 < nsteps) step(t + 1, x1, x0);
     }
     cp_async_wait<0>();
+
+    // A NaN code anywhere in row r (r+8) of the task makes that row's outputs NaN.
+    {
+        uint32_t fa = has_nan_code(mxa) ? 1u : 0u, fb = has_nan_code(mxb) ? 1u : 0u;
+        fa |= __shfl_xor_sync(0xFFFFFFFFu, fa, 1);
+        fa |= __shfl_xor_sync(0xFFFFFFFFu, fa, 2);
+        fb |= __shfl_xor_sync(0xFFFFFFFFu, fb, 1);
+        fb |= __shfl_xor_sync(0xFFFFFFFFu, fb, 2);
+        if (fa | fb) {
+            const float qnan = __uint_as_float(0x7FC00000u);
+#pragma unroll
+            for (int a = 0; a < C::ACC; ++a)
+#pragma unroll
+                for (int t = 0; t < NT8; ++t) {
+                    if (fa) acc[a][t][0] = acc[a][t][1] = qnan;
+                    if (fb) acc[a][t][2] = acc[a][t][3] = qnan;
+                }
+        }
+    }
 
     // ---- task partial -> shared memory (rows = weight rows, columns = tokens)
 #pragma unroll
