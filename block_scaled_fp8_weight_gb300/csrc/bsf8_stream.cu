@@ -167,192 +167,21 @@ __device__ __forceinline__ bool has_nan_code(uint32_t mx) {
     return (mx & 0x7FFFu) >= 0x07F0u || ((mx >> 16) & 0x7FFFu) >= 0x07F0u;
 }
 
+// End of a group: every warp has written its task partial to red[warp].  Sums them in the
+// fixed order (tasks of a split in task order, splits in split order) and stores y, or
+// stores the per-split partials P[s].  gslab is the first slab of the group.
 template <int NT8>
-__global__ void __launch_bounds__(kStreamThreads, NT8 <= 2 ? 2 : 1)
-    stream_kernel(const __grid_constant__ StreamParams p) {
-    using C = StepCfg<NT8>;
+__device__ __forceinline__ void group_epilogue(const StreamParams &p, float (*red)[16][8 * NT8], int g,
+                                               int mbase, int nslabs, int tslab, int gslab) {
     constexpr int MT = 8 * NT8;
-    __shared__ __align__(16) float red[kStreamWarps][16][MT];  // per-warp task partials
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int q = lane & 3;
-    const int g = blockIdx.y % p.G;
-    const int mbase = (blockIdx.y / p.G) * MT;
-    const int nslabs = p.N / 16;
-    const int tslab = p.S * p.tps;
-
-    // ---- this warp's task: slab, split s, task u within the split
-    int slab, s, u;
-    bool active;
-    if (p.mode == kStreamCluster) {
-        slab = blockIdx.x / p.cluster;
-        const int tau = (blockIdx.x % p.cluster) * kStreamWarps + warp;
-        s = tau / p.tps;
-        u = tau % p.tps;
-        active = tau < tslab;
-    } else if (p.mode == kStreamPartials) {
-        slab = blockIdx.x / p.cps;
-        s = (blockIdx.x % p.cps) * p.spl + warp / p.tps;
-        u = warp % p.tps;
-        active = warp < p.spl * p.tps && s < p.S;
-    } else {
-        slab = blockIdx.x * p.spc + warp / tslab;
-        s = (warp % tslab) / p.tps;
-        u = (warp % tslab) % p.tps;
-        active = warp < p.spc * tslab && slab < nslabs;
-    }
-    int k0 = 0, k1 = 0;
-    if (active) {
-        const int s_lo = min(p.K, s * p.chunk_cols);
-        const int s_hi = min(p.K, s_lo + p.chunk_cols);
-        k0 = min(s_hi, s_lo + u * p.kt);
-        k1 = min(s_hi, k0 + p.kt);
-    }
-
-    pdl_trigger();
-
-    float acc[C::ACC][NT8][4];
-#pragma unroll
-    for (int a = 0; a < C::ACC; ++a)
-#pragma unroll
-        for (int t = 0; t < NT8; ++t)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) acc[a][t][c] = 0.0f;
-
-    const bool work = active && k1 > k0;
-    uint32_t mxa = 0, mxb = 0;  // largest rebuilt magnitudes of rows r and r+8
-    extern __shared__ __align__(128) uint8_t ring_smem[];
-    uint8_t *ring = ring_smem + warp * C::DEPTH * C::STAGE;
-    const int nsteps = work ? (k1 - k0 + C::KS - 1) / C::KS : 0;
-    const int r = lane >> 2;
-    // weight copies: lane copies 16-byte chunk (lane % cpr) of rows crow + i * rows_per
-    constexpr int cpr = C::KS / 16;
-    constexpr int rows_per = 32 / cpr;
-    const int crow = lane / cpr, ccol = (lane % cpr) * 16;
-    const uint8_t *wsrc = p.w8 + ((size_t)g * p.N + slab * 16 + crow) * p.K + k0 + ccol;
-    const size_t rstride = (size_t)rows_per * p.K;
-    const uint8_t *esrc =
-        p.ex + ((size_t)g * (p.N / 32) + slab / 2) * (p.K / 32) + (k0 + q * C::TC) / 32;
-
-    auto issue = [&](int t) {
-        uint8_t *st = ring + (t % C::DEPTH) * C::STAGE;
-        const bool in = k0 + t * C::KS + ccol < k1;
-        const uint8_t *src = in ? wsrc + (size_t)t * C::KS : wsrc;  // zero-fill reads nothing
-#pragma unroll
-        for (int i = 0; i < C::CPL; ++i)
-            cp_async16(st + (crow + i * rows_per) * C::PITCH + ccol, src + i * rstride,
-                       in ? 16u : 0u);
-    };
-
-    // The twin is a static parameter: the first DEPTH-1 steps of this warp's weight rows
-    // are copied into its ring, and the rest of the task and its exponents prefetched into
-    // L2, before waiting for the preceding kernel (whose outputs include x).
-#pragma unroll
-    for (int i = 0; i < C::DEPTH - 1; ++i) {
-        if (i < nsteps) issue(i);
-        cp_async_commit();
-    }
-    if (work) {
-        if (nsteps > C::DEPTH - 1 && lane < 16) {
-            const int rest = (C::DEPTH - 1) * C::KS;
-            prefetch_l2(p.w8 + ((size_t)g * p.N + slab * 16 + lane) * p.K + k0 + rest,
-                        (uint32_t)(k1 - k0 - rest));
-        }
-        if (lane == 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(esrc) : "memory");
-    }
-    pdl_wait();
-
-    if (work) {
-        // token rows >= M read row M-1 instead: their outputs are never stored
-        const uint16_t *xsrc[NT8];
-#pragma unroll
-        for (int t = 0; t < NT8; ++t) {
-            const int m = min(mbase + t * 8 + r, p.M - 1);
-            xsrc[t] = p.x + (size_t)m * p.ldx + (size_t)g * p.K + k0 + q * C::TC;
-        }
-        auto load_x = [&](XBuf<NT8> &xb, int t) {
-            if (k0 + t * C::KS + q * C::TC < k1) {
-#pragma unroll
-                for (int tt = 0; tt < NT8; ++tt)
-#pragma unroll
-                    for (int v = 0; v < C::XV; ++v) xb.v[tt][v] = ldg_v4(xsrc[tt] + t * C::KS + 8 * v);
-                xb.e = ldg_u8(esrc + t * (C::KS / 32));
-            } else {
-#pragma unroll
-                for (int tt = 0; tt < NT8; ++tt)
-#pragma unroll
-                    for (int v = 0; v < C::XV; ++v) xb.v[tt][v] = make_uint4(0, 0, 0, 0);
-                xb.e = 127;
-            }
-        };
-        auto step = [&](int t, const XBuf<NT8> &cur, XBuf<NT8> &ahead) {
-            __syncwarp();  // every lane is done with the stage that step t+DEPTH-1 refills
-            if (t + C::DEPTH - 1 < nsteps) issue(t + C::DEPTH - 1);
-            cp_async_commit();
-            if (t + 2 < nsteps) load_x(ahead, t + 2);  // x two steps ahead
-            cp_async_wait<C::DEPTH - 1>();
-            __syncwarp();  // step t's stage has landed for every lane
-            const uint8_t *st = ring + (t % C::DEPTH) * C::STAGE;
-            if (__any_sync(0xFFFFFFFFu, cur.e > 134u))
-                compute_step<NT8, true>(st, r, q, cur, acc, mxa, mxb);
-            else
-                compute_step<NT8, false>(st, r, q, cur, acc, mxa, mxb);
-        };
-
-        XBuf<NT8> x0, x1, x2;
-        load_x(x0, 0);
-        if (1 < nsteps) load_x(x1, 1);
-        int t = 0;
-        for (; t + 3 <= nsteps; t += 3) {
-            step(t, x0, x2);
-            step(t + 1, x1, x0);
-            step(t + 2, x2, x1);
-        }
-        if (t < nsteps) step(t, x0, x2);
-        if (t + 1 < nsteps) step(t + 1, x1, x0);
-    }
-    cp_async_wait<0>();
-
-    // A NaN code anywhere in row r (r+8) of the task makes that row's outputs NaN.
-    {
-        uint32_t fa = has_nan_code(mxa) ? 1u : 0u, fb = has_nan_code(mxb) ? 1u : 0u;
-        fa |= __shfl_xor_sync(0xFFFFFFFFu, fa, 1);
-        fa |= __shfl_xor_sync(0xFFFFFFFFu, fa, 2);
-        fb |= __shfl_xor_sync(0xFFFFFFFFu, fb, 1);
-        fb |= __shfl_xor_sync(0xFFFFFFFFu, fb, 2);
-        if (fa | fb) {
-            const float qnan = __uint_as_float(0x7FC00000u);
-#pragma unroll
-            for (int a = 0; a < C::ACC; ++a)
-#pragma unroll
-                for (int t = 0; t < NT8; ++t) {
-                    if (fa) acc[a][t][0] = acc[a][t][1] = qnan;
-                    if (fb) acc[a][t][2] = acc[a][t][3] = qnan;
-                }
-        }
-    }
-
-    // ---- task partial -> shared memory (rows = weight rows, columns = tokens)
-#pragma unroll
-    for (int t = 0; t < NT8; ++t) {
-        float v[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) v[c] = C::ACC == 2 ? acc[0][t][c] + acc[C::ACC - 1][t][c] : acc[0][t][c];
-        const int row = lane >> 2, col = t * 8 + 2 * q;
-        *reinterpret_cast<float2 *>(&red[warp][row][col]) = make_float2(v[0], v[1]);
-        *reinterpret_cast<float2 *>(&red[warp][row + 8][col]) = make_float2(v[2], v[3]);
-    }
     const int mrows = min(MT, p.M - mbase);
-
     if (p.mode == kStreamInCta) {
         __syncthreads();
-        // per output: P_s = sum_u task(s,u) in task order; y = sum_s P_s in split order
         const int per_slab = 16 * mrows;
         for (int i = threadIdx.x; i < p.spc * per_slab; i += kStreamThreads) {
             const int sl = i / per_slab, rem = i - sl * per_slab;
             const int m = rem / 16, row = rem - m * 16;
-            const int sb = blockIdx.x * p.spc + sl;
+            const int sb = gslab + sl;
             if (sb >= nslabs) continue;
             const int w0 = sl * tslab;
             float y = 0.0f;
@@ -363,6 +192,7 @@ __global__ void __launch_bounds__(kStreamThreads, NT8 <= 2 ? 2 : 1)
             }
             p.y[((size_t)(mbase + m) * p.G + g) * p.N + sb * 16 + row] = f32_to_bf16_rn(y);
         }
+        __syncthreads();  // red is rewritten by the next group
     } else if (p.mode == kStreamPartials) {
         __syncthreads();
         const int per_split = 16 * mrows;
@@ -373,11 +203,12 @@ __global__ void __launch_bounds__(kStreamThreads, NT8 <= 2 ? 2 : 1)
             if (ss >= p.S) continue;
             float ps = red[ls * p.tps][row][m];
             for (int uu = 1; uu < p.tps; ++uu) ps = ps + red[ls * p.tps + uu][row][m];
-            p.partials[(((size_t)ss * p.M + mbase + m) * p.G + g) * p.N + slab * 16 + row] = ps;
+            p.partials[(((size_t)ss * p.M + mbase + m) * p.G + g) * p.N + gslab * 16 + row] = ps;
         }
+        __syncthreads();
     } else {
-        // Cluster of the slab's CTAs (rank c holds tasks 8c .. 8c+7): each CTA sums a share
-        // of the slab's outputs, reading every task partial in task order through DSMEM.
+        // Cluster of the slab's blocks (rank c holds tasks 8c .. 8c+7): each block sums a
+        // share of the slab's outputs, reading every task partial in task order via DSMEM.
         cluster_sync();
         const int total = 16 * mrows;
         const int c = blockIdx.x % p.cluster;
@@ -396,10 +227,211 @@ __global__ void __launch_bounds__(kStreamThreads, NT8 <= 2 ? 2 : 1)
                 }
                 y = ss == 0 ? ps : y + ps;
             }
-            p.y[((size_t)(mbase + m) * p.G + g) * p.N + slab * 16 + row] = f32_to_bf16_rn(y);
+            p.y[((size_t)(mbase + m) * p.G + g) * p.N + gslab * 16 + row] = f32_to_bf16_rn(y);
         }
-        cluster_sync();
+        cluster_sync();  // keep this block's shared memory alive until the others are done
     }
+}
+
+template <int NT8>
+__global__ void __launch_bounds__(kStreamThreads, NT8 <= 2 ? 2 : 1)
+    stream_kernel(const __grid_constant__ StreamParams p) {
+    using C = StepCfg<NT8>;
+    constexpr int MT = 8 * NT8;
+    __shared__ __align__(16) float red[kStreamWarps][16][MT];  // per-warp task partials
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int q = lane & 3;
+    const int r = lane >> 2;
+    const int g = blockIdx.y % p.G;
+    const int mbase = (blockIdx.y / p.G) * MT;
+    const int nslabs = p.N / 16;
+    const int tslab = p.S * p.tps;
+
+    // ---- groups and this warp's task.  In-block mode: a group is spc slabs with all their
+    // tasks, and a block walks groups blockIdx.x, blockIdx.x + gridDim.x, ... (persistent).
+    // Partials / cluster mode: one group per block.  A warp's task (split s, task u, columns
+    // [k0, k1)) is the same in every group; only the slab (its 16 rows) changes.
+    int ngroups = 1, s, u, slab0, slab_step = 0;
+    bool active;
+    if (p.mode == kStreamCluster) {
+        slab0 = blockIdx.x / p.cluster;
+        const int tau = (blockIdx.x % p.cluster) * kStreamWarps + warp;
+        s = tau / p.tps;
+        u = tau % p.tps;
+        active = tau < tslab;
+    } else if (p.mode == kStreamPartials) {
+        slab0 = blockIdx.x / p.cps;
+        s = (blockIdx.x % p.cps) * p.spl + warp / p.tps;
+        u = warp % p.tps;
+        active = warp < p.spl * p.tps && s < p.S;
+    } else {
+        const int groups_total = (nslabs + p.spc - 1) / p.spc;
+        ngroups = (int)blockIdx.x < groups_total
+                      ? (groups_total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+        slab0 = blockIdx.x * p.spc + warp / tslab;
+        slab_step = gridDim.x * p.spc;
+        s = (warp % tslab) / p.tps;
+        u = (warp % tslab) % p.tps;
+        active = warp < p.spc * tslab;
+    }
+    int k0 = 0, k1 = 0;
+    if (active) {
+        const int s_lo = min(p.K, s * p.chunk_cols);
+        const int s_hi = min(p.K, s_lo + p.chunk_cols);
+        k0 = min(s_hi, s_lo + u * p.kt);
+        k1 = min(s_hi, k0 + p.kt);
+    }
+    // Steps per group; a warp without columns runs one all-zero step so that every warp
+    // reaches each group's epilogue in the same loop.
+    const int nst = active && k1 > k0 ? (k1 - k0 + C::KS - 1) / C::KS : 1;
+    const long long total = (long long)ngroups * nst;
+
+    pdl_trigger();
+
+    float acc[C::ACC][NT8][4];
+#pragma unroll
+    for (int a = 0; a < C::ACC; ++a)
+#pragma unroll
+        for (int t = 0; t < NT8; ++t)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[a][t][c] = 0.0f;
+    uint32_t mxa = 0, mxb = 0;  // largest rebuilt magnitudes of rows r and r+8
+
+    extern __shared__ __align__(128) uint8_t ring_smem[];
+    uint8_t *ring = ring_smem + warp * C::DEPTH * C::STAGE;
+    // weight copies: lane copies 16-byte chunk (lane % cpr) of rows crow + i * rows_per
+    constexpr int cpr = C::KS / 16;
+    constexpr int rows_per = 32 / cpr;
+    const int crow = lane / cpr, ccol = (lane % cpr) * 16;
+    const size_t rstride = (size_t)rows_per * p.K;
+    const size_t gbase = (size_t)g * p.N;
+
+    // Issue cursor over the flattened (group, step) sequence of this warp.
+    int is_gi = 0, is_t = 0, is_slot = 0;
+    auto issue_next = [&]() {
+        if (is_gi < ngroups) {
+            const int slab = slab0 + is_gi * slab_step;
+            const bool in = active && slab < nslabs && k0 + is_t * C::KS + ccol < k1;
+            // a zero-fill copy reads nothing; it still gets a valid address
+            const uint8_t *src = in ? p.w8 + (gbase + slab * 16 + crow) * p.K + k0 + ccol + (size_t)is_t * C::KS
+                                    : p.w8;
+            uint8_t *st = ring + is_slot * C::STAGE;
+#pragma unroll
+            for (int i = 0; i < C::CPL; ++i)
+                cp_async16(st + (crow + i * rows_per) * C::PITCH + ccol, in ? src + i * rstride : src,
+                           in ? 16u : 0u);
+            if (++is_t == nst) {
+                is_t = 0;
+                ++is_gi;
+            }
+        }
+        is_slot = is_slot + 1 == C::DEPTH ? 0 : is_slot + 1;
+        cp_async_commit();
+    };
+
+    // The twin is a static parameter: the first DEPTH-1 steps of this warp's stream are
+    // copied into its ring, and the rest of its first task prefetched into L2, before
+    // waiting for the preceding kernel (whose outputs include x).
+#pragma unroll
+    for (int i = 0; i < C::DEPTH - 1; ++i) issue_next();
+    if (active && ngroups > 0 && slab0 < nslabs && nst > C::DEPTH - 1 && lane < 16) {
+        const int rest = (C::DEPTH - 1) * C::KS;
+        if (k1 - k0 > rest)
+            prefetch_l2(p.w8 + (gbase + slab0 * 16 + lane) * p.K + k0 + rest, (uint32_t)(k1 - k0 - rest));
+    }
+    pdl_wait();
+
+    // token rows >= M read row M-1 instead: their outputs are never stored
+    const uint16_t *xsrc[NT8];
+#pragma unroll
+    for (int t = 0; t < NT8; ++t) {
+        const int m = min(mbase + t * 8 + r, p.M - 1);
+        xsrc[t] = p.x + (size_t)m * p.ldx + (size_t)g * p.K + k0 + q * C::TC;
+    }
+    const size_t ebase = (size_t)g * (p.N / 32) * (p.K / 32) + (size_t)((k0 + q * C::TC) / 32);
+    auto load_x = [&](XBuf<NT8> &xb, int gi, int t) {
+        const int slab = slab0 + gi * slab_step;
+        if (active && gi < ngroups && slab < nslabs && k0 + t * C::KS + q * C::TC < k1) {
+#pragma unroll
+            for (int tt = 0; tt < NT8; ++tt)
+#pragma unroll
+                for (int v = 0; v < C::XV; ++v) xb.v[tt][v] = ldg_v4(xsrc[tt] + t * C::KS + 8 * v);
+            xb.e = ldg_u8(p.ex + ebase + (size_t)(slab / 2) * (p.K / 32) + t * (C::KS / 32));
+        } else {
+#pragma unroll
+            for (int tt = 0; tt < NT8; ++tt)
+#pragma unroll
+                for (int v = 0; v < C::XV; ++v) xb.v[tt][v] = make_uint4(0, 0, 0, 0);
+            xb.e = 127;
+        }
+    };
+    auto compute = [&](const uint8_t *st, const XBuf<NT8> &cur) {
+        if (__any_sync(0xFFFFFFFFu, cur.e > 134u))
+            compute_step<NT8, true>(st, r, q, cur, acc, mxa, mxb);
+        else
+            compute_step<NT8, false>(st, r, q, cur, acc, mxa, mxb);
+    };
+
+    XBuf<NT8> xa, xb;
+    int gi = 0, t = 0, slot = 0;
+    load_x(xa, 0, 0);
+    for (long long T = 0; T < total; ++T) {
+        __syncwarp();  // every lane is done with the slot the next issue refills
+        issue_next();
+        const int ngi = t + 1 == nst ? gi + 1 : gi, nt = t + 1 == nst ? 0 : t + 1;
+        const uint8_t *st = ring + slot * C::STAGE;
+        if (T & 1) {
+            load_x(xa, ngi, nt);
+            cp_async_wait<C::DEPTH - 1>();
+            __syncwarp();  // this step's slot has landed for every lane
+            compute(st, xb);
+        } else {
+            load_x(xb, ngi, nt);
+            cp_async_wait<C::DEPTH - 1>();
+            __syncwarp();
+            compute(st, xa);
+        }
+        slot = slot + 1 == C::DEPTH ? 0 : slot + 1;
+        if (nt == 0) {
+            // ---- end of group gi: the epilogue below runs once per group for every warp
+            const int slab = slab0 + gi * slab_step;
+            // A NaN code anywhere in row r (r+8) of the task makes that row's outputs NaN.
+            uint32_t fa = has_nan_code(mxa) ? 1u : 0u, fb = has_nan_code(mxb) ? 1u : 0u;
+            fa |= __shfl_xor_sync(0xFFFFFFFFu, fa, 1);
+            fa |= __shfl_xor_sync(0xFFFFFFFFu, fa, 2);
+            fb |= __shfl_xor_sync(0xFFFFFFFFu, fb, 1);
+            fb |= __shfl_xor_sync(0xFFFFFFFFu, fb, 2);
+            const float qnan = __uint_as_float(0x7FC00000u);
+#pragma unroll
+            for (int tt = 0; tt < NT8; ++tt) {
+                float v[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    v[c] = C::ACC == 2 ? acc[0][tt][c] + acc[C::ACC - 1][tt][c] : acc[0][tt][c];
+                    if ((c < 2 && fa) || (c >= 2 && fb)) v[c] = qnan;
+                }
+                const int col = tt * 8 + 2 * q;
+                *reinterpret_cast<float2 *>(&red[warp][r][col]) = make_float2(v[0], v[1]);
+                *reinterpret_cast<float2 *>(&red[warp][r + 8][col]) = make_float2(v[2], v[3]);
+            }
+#pragma unroll
+            for (int a = 0; a < C::ACC; ++a)
+#pragma unroll
+                for (int tt = 0; tt < NT8; ++tt)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) acc[a][tt][c] = 0.0f;
+            mxa = mxb = 0;
+            (void)slab;
+            const int gslab = p.mode == kStreamInCta ? ((int)blockIdx.x + gi * (int)gridDim.x) * p.spc
+                                                     : slab0;
+            group_epilogue<NT8>(p, red, g, mbase, nslabs, tslab, gslab);
+        }
+        gi = ngi;
+        t = nt;
+    }
+    cp_async_wait<0>();
 }
 
 // ------------------------------------------------------------------- host side
@@ -432,7 +464,7 @@ StreamPlan plan_stream(int M, int N, int K, int G, int S, bool partials) {
     } else if (tslab <= kStreamWarps) {
         pl.mode = kStreamInCta;
         pl.spc = kStreamWarps / tslab;
-        pl.grid_x = (nslabs + pl.spc - 1) / pl.spc;
+        pl.grid_x = (nslabs + pl.spc - 1) / pl.spc;  // capped at the resident blocks at launch
     } else {
         pl.mode = kStreamCluster;
         pl.cluster = (tslab + kStreamWarps - 1) / kStreamWarps;
@@ -461,6 +493,21 @@ cudaError_t launch_stream_nt8(const StreamPlan &pl, const StreamParams &prm, cud
         __atomic_store_n(&configured[dev], 1, __ATOMIC_RELEASE);
     }
     cfg.dynamicSmemBytes = smem;
+    if (pl.mode == kStreamInCta) {
+        // Persistent: at most the blocks that are resident at once (groups are strided).
+        static int cap[64] = {0};
+        int c = __atomic_load_n(&cap[dev], __ATOMIC_ACQUIRE);
+        if (c == 0) {
+            int sms = 0, per_sm = 0;
+            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            if (e != cudaSuccess) return e;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stream_kernel<NT8>, kStreamThreads, smem);
+            if (e != cudaSuccess) return e;
+            c = std::max(1, sms * std::max(1, per_sm));
+            __atomic_store_n(&cap[dev], c, __ATOMIC_RELEASE);
+        }
+        cfg.gridDim.x = (unsigned)std::min(pl.grid_x, c);
+    }
     cfg.stream = stream;
     cudaLaunchAttribute attrs[2];
     int na = 0;
