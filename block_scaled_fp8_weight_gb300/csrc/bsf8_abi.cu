@@ -81,6 +81,20 @@ inline int check_gemm_args(const void *x, const uint8_t *w8, const uint8_t *exp,
 
 constexpr size_t kMaxSmem = 227 * 1024;
 
+// Up to 16 token rows per pass run on the TMA-fed kernel, more on the streaming kernel.
+inline bool use_tma(int M, int N, int G) { return M <= 16 && (long long)G * N < (1LL << 31); }
+
+inline StreamPlan main_plan(int M, int N, int K, int G, int S, bool partials) {
+    return use_tma(M, N, G) ? plan_tma(M, N, K, G, S, partials) : plan_stream(M, N, K, G, S, partials);
+}
+
+inline cudaError_t main_launch(const StreamPlan &pl, const void *x, long long ldx, const uint8_t *w8,
+                               const uint8_t *ex, void *y, float *P, int M, int N, int K, int G,
+                               cudaStream_t s) {
+    return use_tma(M, N, G) ? launch_tma(pl, x, ldx, w8, ex, y, P, M, N, K, G, s)
+                            : launch_stream(pl, x, ldx, w8, ex, y, P, M, N, K, G, s);
+}
+
 }  // namespace
 
 extern "C" {
@@ -132,7 +146,7 @@ int bsf8_gemm_auto_split(int M, int N, int K, int G) {
 size_t bsf8_gemm_workspace_bytes(int M, int N, int K, int G, int split_k) {
     if (check_gnk(G, N, K) || M < 1 || M > BSF8_MAX_M || split_k < 0 || split_k > K / 32) return 0;
     const int S = split_k == 0 ? auto_split(M, N, K, G) : split_k;
-    if (plan_stream(M, N, K, G, S, false).mode != kStreamPartials) return 0;
+    if (main_plan(M, N, K, G, S, false).mode != kStreamPartials) return 0;
     return (size_t)S * M * G * N * sizeof(float);
 }
 
@@ -144,14 +158,14 @@ int bsf8_gemm(const void *x, const uint8_t *w8, const uint8_t *exp, void *y, int
     const int S = split_k == 0 ? auto_split(M, N, K, G) : split_k;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (options().gemm_path == 0 || S > kMaxClusterSplits) {
-        const StreamPlan pl = plan_stream(M, N, K, G, S, false);
+        const StreamPlan pl = main_plan(M, N, K, G, S, false);
         if (pl.mode != kStreamPartials)
-            return from_cuda(launch_stream(pl, x, ldx, w8, exp, y, nullptr, M, N, K, G, s));
+            return from_cuda(main_launch(pl, x, ldx, w8, exp, y, nullptr, M, N, K, G, s));
         const size_t need = (size_t)S * M * G * N * sizeof(float);
         if (!workspace || workspace_bytes < need) return BSF8_ERR_WORKSPACE;
         if (!aligned16(workspace)) return BSF8_ERR_ALIGN;
         float *P = static_cast<float *>(workspace);
-        st = from_cuda(launch_stream(pl, x, ldx, w8, exp, nullptr, P, M, N, K, G, s));
+        st = from_cuda(main_launch(pl, x, ldx, w8, exp, nullptr, P, M, N, K, G, s));
         if (st) return st;
         return from_cuda(launch_splitk_reduce(P, y, S, (long long)M * G * N, s));
     }
@@ -171,8 +185,8 @@ int bsf8_gemm_partials(const void *x, const uint8_t *w8, const uint8_t *exp, flo
     if (!aligned16(partials)) return BSF8_ERR_ALIGN;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (options().gemm_path == 0) {
-        const StreamPlan pl = plan_stream(M, N, K, G, split_k, true);
-        return from_cuda(launch_stream(pl, x, ldx, w8, exp, nullptr, partials, M, N, K, G, s));
+        const StreamPlan pl = main_plan(M, N, K, G, split_k, true);
+        return from_cuda(main_launch(pl, x, ldx, w8, exp, nullptr, partials, M, N, K, G, s));
     }
     const GemmPlan pl = plan_gemm(M, N, K, G, split_k, kModePartials);
     if (pl.smem_bytes > kMaxSmem) return BSF8_ERR_SHAPE;

@@ -55,6 +55,14 @@ struct StreamPlan {
 };
 
 StreamPlan plan_stream(int M, int N, int K, int G, int S, bool partials);
+// The same decomposition with an explicit step width and at most max_nt8 token tiles.
+StreamPlan plan_stream_ks(int M, int N, int K, int G, int S, bool partials, int ks, int max_nt8);
+
+// TMA-fed kernel (bsf8_tma.cu) for up to 16 token rows per pass; 128-column steps.
+StreamPlan plan_tma(int M, int N, int K, int G, int S, bool partials);
+cudaError_t launch_tma(const StreamPlan &plan, const void *x, long long ldx, const uint8_t *w8,
+                       const uint8_t *ex, void *y, float *partials, int M, int N, int K, int G,
+                       cudaStream_t stream);
 cudaError_t launch_stream(const StreamPlan &plan, const void *x, long long ldx, const uint8_t *w8,
                           const uint8_t *ex, void *y, float *partials, int M, int N, int K, int G,
                           cudaStream_t stream);

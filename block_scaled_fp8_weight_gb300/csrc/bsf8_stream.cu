@@ -437,10 +437,14 @@ __global__ void __launch_bounds__(kStreamThreads, NT8 <= 2 ? 2 : 1)
 // ------------------------------------------------------------------- host side
 
 StreamPlan plan_stream(int M, int N, int K, int G, int S, bool partials) {
+    const int nt8 = std::min(4, (M + 7) / 8);
+    return plan_stream_ks(M, N, K, G, S, partials, nt8 == 1 ? 128 : 64, 4);
+}
+
+StreamPlan plan_stream_ks(int M, int N, int K, int G, int S, bool partials, int ks, int max_nt8) {
     StreamPlan pl{};
-    pl.nt8 = std::min(4, (M + 7) / 8);
+    pl.nt8 = std::min(max_nt8, (M + 7) / 8);
     pl.m_chunks = (M + 8 * pl.nt8 - 1) / (8 * pl.nt8);
-    const int ks = pl.nt8 == 1 ? 128 : 64;
     const int nkb = K / 32;
     pl.S = S;
     pl.chunk_cols = ((nkb + S - 1) / S) * 32;
