@@ -82,17 +82,52 @@ inline int check_gemm_args(const void *x, const uint8_t *w8, const uint8_t *exp,
 constexpr size_t kMaxSmem = 227 * 1024;
 
 // Up to 16 token rows per pass run on the TMA-fed kernel, more on the streaming kernel.
-inline bool use_tma(int M, int N, int G) { return M <= 16 && (long long)G * N < (1LL << 31); }
+// Kernel for a call.  The decode-ahead kernel pays off when each of its blocks holds one
+// group of tasks, so that the group's weights are rebuilt before the dependency wait: up to
+// 8 token rows and at most two blocks an SM.  Larger calls stream (the cp.async kernel
+// sustains more bandwidth once the rebuild can no longer run ahead).  TMA coordinates are
+// 32-bit, so the TMA kernels need G*N < 2^31.
+enum MainKernel { kKernelStream = 0, kKernelTma = 1, kKernelLowM = 2 };
+
+inline int sm_count() {
+    static int count[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int c = __atomic_load_n(&count[dev], __ATOMIC_ACQUIRE);
+    if (c == 0 && cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+        __atomic_store_n(&count[dev], c, __ATOMIC_RELEASE);
+    return c;
+}
+
+inline MainKernel main_kernel(int M, int N, int K, int G, int S, bool partials) {
+    if ((long long)G * N >= (1LL << 31)) return kKernelStream;
+    switch (options().gemm_path) {  // a forced kernel, where it applies
+        case 2: return kKernelStream;
+        case 3: if (M <= 16) return kKernelTma; break;
+        case 4: if (M <= 8) return kKernelLowM; break;
+        default: break;
+    }
+    if (M > 8) return kKernelStream;
+    const StreamPlan pl = plan_lowm(M, N, K, G, S, partials);
+    return (long long)pl.grid_x * G <= 2LL * sm_count() ? kKernelLowM : kKernelStream;
+}
 
 inline StreamPlan main_plan(int M, int N, int K, int G, int S, bool partials) {
-    return use_tma(M, N, G) ? plan_tma(M, N, K, G, S, partials) : plan_stream(M, N, K, G, S, partials);
+    switch (main_kernel(M, N, K, G, S, partials)) {
+        case kKernelLowM: return plan_lowm(M, N, K, G, S, partials);
+        case kKernelTma: return plan_tma(M, N, K, G, S, partials);
+        default: return plan_stream(M, N, K, G, S, partials);
+    }
 }
 
 inline cudaError_t main_launch(const StreamPlan &pl, const void *x, long long ldx, const uint8_t *w8,
                                const uint8_t *ex, void *y, float *P, int M, int N, int K, int G,
-                               cudaStream_t s) {
-    return use_tma(M, N, G) ? launch_tma(pl, x, ldx, w8, ex, y, P, M, N, K, G, s)
-                            : launch_stream(pl, x, ldx, w8, ex, y, P, M, N, K, G, s);
+                               cudaStream_t s, int S, bool partials) {
+    switch (main_kernel(M, N, K, G, S, partials)) {
+        case kKernelLowM: return launch_lowm(pl, x, ldx, w8, ex, y, P, M, N, K, G, s);
+        case kKernelTma: return launch_tma(pl, x, ldx, w8, ex, y, P, M, N, K, G, s);
+        default: return launch_stream(pl, x, ldx, w8, ex, y, P, M, N, K, G, s);
+    }
 }
 
 }  // namespace
@@ -157,15 +192,15 @@ int bsf8_gemm(const void *x, const uint8_t *w8, const uint8_t *exp, void *y, int
     if (st) return st;
     const int S = split_k == 0 ? auto_split(M, N, K, G) : split_k;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (options().gemm_path == 0 || S > kMaxClusterSplits) {
+    if (options().gemm_path != 1 || S > kMaxClusterSplits) {
         const StreamPlan pl = main_plan(M, N, K, G, S, false);
         if (pl.mode != kStreamPartials)
-            return from_cuda(main_launch(pl, x, ldx, w8, exp, y, nullptr, M, N, K, G, s));
+            return from_cuda(main_launch(pl, x, ldx, w8, exp, y, nullptr, M, N, K, G, s, S, false));
         const size_t need = (size_t)S * M * G * N * sizeof(float);
         if (!workspace || workspace_bytes < need) return BSF8_ERR_WORKSPACE;
         if (!aligned16(workspace)) return BSF8_ERR_ALIGN;
         float *P = static_cast<float *>(workspace);
-        st = from_cuda(main_launch(pl, x, ldx, w8, exp, nullptr, P, M, N, K, G, s));
+        st = from_cuda(main_launch(pl, x, ldx, w8, exp, nullptr, P, M, N, K, G, s, S, false));
         if (st) return st;
         return from_cuda(launch_splitk_reduce(P, y, S, (long long)M * G * N, s));
     }
@@ -184,9 +219,9 @@ int bsf8_gemm_partials(const void *x, const uint8_t *w8, const uint8_t *exp, flo
     if (split_k < 1) return BSF8_ERR_SHAPE;
     if (!aligned16(partials)) return BSF8_ERR_ALIGN;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (options().gemm_path == 0) {
+    if (options().gemm_path != 1) {
         const StreamPlan pl = main_plan(M, N, K, G, split_k, true);
-        return from_cuda(main_launch(pl, x, ldx, w8, exp, nullptr, partials, M, N, K, G, s));
+        return from_cuda(main_launch(pl, x, ldx, w8, exp, nullptr, partials, M, N, K, G, s, split_k, true));
     }
     const GemmPlan pl = plan_gemm(M, N, K, G, split_k, kModePartials);
     if (pl.smem_bytes > kMaxSmem) return BSF8_ERR_SHAPE;
@@ -245,7 +280,7 @@ int bsf8_set_option(int option, int64_t value) {
         case BSF8_OPT_WAIT_TIMEOUT_NS: g_opt_timeout_ns.store((long long)value); return BSF8_OK;
         case BSF8_OPT_DEBUG_SKIP_LOADS: g_opt_skip_loads.store(value ? 1 : 0); return BSF8_OK;
         case BSF8_OPT_GEMM_PATH:
-            if (value > 1) return BSF8_ERR_VALUE;
+            if (value > 4) return BSF8_ERR_VALUE;
             g_opt_gemm_path.store((int)value);
             return BSF8_OK;
         default: return BSF8_ERR_VALUE;

@@ -51,6 +51,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return done != 0;
 }
 
+// As mbar_try_wait, but the thread may be suspended (issuing nothing) until the phase
+// completes or about hint_ns have passed, instead of returning at once.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t *bar, uint32_t parity,
+                                                      uint32_t hint_ns) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0;
+}
+
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -58,13 +73,15 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 
 // Waits for the phase of `bar` with the given parity to complete, for at most
-// timeout_ns of wall time.  Returns false when the bound ran out.
+// timeout_ns of wall time.  Returns false when the bound ran out.  While it waits the
+// thread sleeps in the barrier (suspend hint) rather than spinning, so a waiting warp
+// leaves the SM's issue slots to the warps that have work.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
                                                   uint64_t timeout_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_suspend(bar, parity, 1000000u)) return true;
         if (global_ns() - t0 > timeout_ns) return false;
     }
 }

@@ -13,7 +13,7 @@ struct Options {
     int pdl;
     unsigned long long timeout_ns;
     int skip_loads;
-    int gemm_path;  // 0: weight-streaming kernel; 1: shared-memory TMA-ring kernel
+    int gemm_path;  // 0: by shape; 1: TMA-ring; 2: streaming; 3: TMA-fed; 4: decode-ahead
 };
 Options options();
 
@@ -55,8 +55,17 @@ struct StreamPlan {
 };
 
 StreamPlan plan_stream(int M, int N, int K, int G, int S, bool partials);
-// The same decomposition with an explicit step width and at most max_nt8 token tiles.
-StreamPlan plan_stream_ks(int M, int N, int K, int G, int S, bool partials, int ks, int max_nt8);
+// The same decomposition with an explicit step width, at most max_nt8 token tiles and
+// tasks of at most max_kt columns.
+StreamPlan plan_stream_ks(int M, int N, int K, int G, int S, bool partials, int ks, int max_nt8,
+                          int max_kt = 1 << 30);
+
+// Decode-ahead kernel (bsf8_lowm.cu) for up to 8 token rows; 128-column steps, tasks of
+// at most 1024 columns.
+StreamPlan plan_lowm(int M, int N, int K, int G, int S, bool partials);
+cudaError_t launch_lowm(const StreamPlan &plan, const void *x, long long ldx, const uint8_t *w8,
+                        const uint8_t *ex, void *y, float *partials, int M, int N, int K, int G,
+                        cudaStream_t stream);
 
 // TMA-fed kernel (bsf8_tma.cu) for up to 16 token rows per pass; 128-column steps.
 StreamPlan plan_tma(int M, int N, int K, int G, int S, bool partials);

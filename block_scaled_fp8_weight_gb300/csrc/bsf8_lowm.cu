@@ -1,0 +1,799 @@
+// bsf8_lowm.cu -- the decode-ahead GEMM kernel for up to 8 token rows.
+//
+//   y[m][g][n] = bf16( sum_{s=0..S-1} P[s][m][g][n] ),  summed s = 0, 1, ... in fp32,
+//   W[g][n][k] = bf16( e4m3(w8[g][n][k]) * 2^(exp[g][n/32][k/32] - 127) ).
+//
+// Page: "recipes/docker-images/mia-tp4/adapter/wo_a_w8.py" -- _wo_a_partial_w8() and
+// _wo_a_mid_kernel() with their fixed-order split-K sums.
+//
+// A decode-step linear layer runs as one of a chain of dependent launches: its input x is
+// written by the kernel just before it, so nothing that reads x can start before that
+// kernel has finished (programmatic dependent launch, griddepcontrol.wait).  The weights
+// and their exponents are static, so everything that touches only them runs before the
+// wait, while the previous kernel is still working:
+//
+//   1. each warp streams its first (up to 4) 16 x 128 weight boxes into shared memory by
+//      TMA, rebuilds them exactly to bf16 MMA fragments in registers and parks the
+//      fragments in tensor memory (tcgen05.st: 32 columns of the warp's 32 TMEM lanes per
+//      box, 128 columns per warp, 256 per block);
+//   2. griddepcontrol.wait;
+//   3. x arrives by TMA (8 token rows x 128 columns per step, rows >= M zero-filled); the
+//      warp reads its fragments back (tcgen05.ld) and runs the MMAs.  Steps beyond the
+//      decoded-ahead prefix stream weights and x through the same ring and rebuild in
+//      registers as they go.
+//
+// After the wait a call then costs little more than its x round trip, its MMAs and its
+// fixed-order reduction; the rebuild work, the bulk of the instructions, overlaps the
+// previous kernel.  Two blocks fit on an SM (96 KB of ring, 256 TMEM columns, <= 128
+// registers a thread), so the next call's blocks become resident and start streaming
+// while this call finishes.
+//
+// Work decomposition (bsf8_stream.cu): a warp task is 16 weight rows (one slab) x a
+// column range inside one split; a block's 8 warps hold a group of tasks and walk groups
+// persistently (in-block mode), or a block is one group of a cluster (cluster mode, the
+// splits of a slab summed over DSMEM) or writes fp32 partials (partials mode).
+//
+// Each warp owns a private ring of 6 slots of 2 KB (a weight box or an x tile each) with
+// one mbarrier per slot; its lane 0 issues the copies, so no warp ever waits for another
+// until the group's reduction.  Every wait is bounded: on timeout the block records
+// BSF8_ERR_TIMEOUT, stores nothing, lets its copies land and returns.
+#include "bsf8_device.cuh"
+#include "bsf8_internal.h"
+
+#include <cuda.h>
+
+#include <algorithm>
+#include <mutex>
+
+namespace bsf8 {
+
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kKS = 128;           // columns per step
+constexpr int kSlotBytes = 2048;   // a 16 x 128 weight box, or an 8 x 128 bf16 x tile
+constexpr int kRing = 6;           // slots per warp
+constexpr int kPre = 4;            // steps per warp rebuilt ahead into tensor memory
+constexpr int kTmemCols = 256;     // per block: 128 columns for each of two warps a quarter
+constexpr int kRingBytes = kWarps * kRing * kSlotBytes;
+constexpr int kMaxKt = 1024;       // task columns: at most 32 exponent blocks (one per lane)
+static_assert(2 * (kRingBytes + 1024 + 6 * 1024) <= 228 * 1024, "two blocks fit an SM");
+
+struct LowParams {
+    CUtensorMap wmap;  // w8 as a [G*N rows][K columns] byte matrix, box 128 x 16
+    CUtensorMap xmap;  // x as a [M rows][G*K columns] bf16 matrix (row pitch ldx), box 64 x 8
+    const uint8_t *ex;
+    uint16_t *y;
+    float *partials;
+    int M, N, K, G, S;
+    int chunk_cols, kt, tps, spc, cluster, spl, cps, mode;
+    unsigned long long timeout_ns;
+    int skip_loads;
+    int *status;
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, int c0, int c1,
+                                       uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_2d_hint(void *dst, const CUtensorMap *map, int c0, int c1,
+                                            uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared-memory accesses before its later
+// async-proxy ones (a TMA copy into a slot the warp has just read).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 registers of this thread -> columns [taddr, taddr + 32) of its TMEM lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t max_xorsign_abs(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// e4m3 bytes -> bf16 patterns e4m3 * 2^-120 (sign-extending byte permute, shift, mask).
+__device__ __forceinline__ void spread_codes(uint32_t w, uint32_t &t0, uint32_t &t1) {
+    asm("prmt.b32 %0, %1, 0, 0x9180;" : "=r"(t0) : "r"(w));
+    asm("prmt.b32 %0, %1, 0, 0xB3A2;" : "=r"(t1) : "r"(w));
+    t0 = (t0 << 4) & 0x87F087F0u;
+    t1 = (t1 << 4) & 0x87F087F0u;
+}
+
+__device__ __forceinline__ bool nan_code_seen(uint32_t mx) {
+    return (mx & 0x7FFFu) >= 0x07F0u || ((mx >> 16) & 0x7FFFu) >= 0x07F0u;
+}
+
+}  // namespace
+
+namespace {
+
+// A warp's task: split s, task u of the split, columns [k0, k1), its slab in the block's
+// first group (slab0), the slab stride between groups and the block's group count.
+struct Task {
+    int s, u, k0, k1, slab0, slab_step, ngroups;
+    bool active;
+};
+
+__device__ __forceinline__ Task task_of(const LowParams &p, int w) {
+    Task t;
+    const int nslabs = p.N / 16;
+    const int tslab = p.S * p.tps;
+    t.ngroups = 1;
+    t.slab_step = 0;
+    if (p.mode == kStreamCluster) {
+        t.slab0 = blockIdx.x / p.cluster;
+        const int tau = (blockIdx.x % p.cluster) * kWarps + w;
+        t.s = tau / p.tps;
+        t.u = tau % p.tps;
+        t.active = tau < tslab;
+    } else if (p.mode == kStreamPartials) {
+        t.slab0 = blockIdx.x / p.cps;
+        t.s = (blockIdx.x % p.cps) * p.spl + w / p.tps;
+        t.u = w % p.tps;
+        t.active = w < p.spl * p.tps && t.s < p.S;
+    } else {
+        const int groups_total = (nslabs + p.spc - 1) / p.spc;
+        t.ngroups = (int)blockIdx.x < groups_total
+                        ? (groups_total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+        t.slab0 = blockIdx.x * p.spc + w / tslab;
+        t.slab_step = gridDim.x * p.spc;
+        t.s = (w % tslab) / p.tps;
+        t.u = (w % tslab) % p.tps;
+        t.active = w < p.spc * tslab;
+    }
+    t.k0 = t.k1 = 0;
+    if (t.active) {
+        const int s_lo = min(p.K, t.s * p.chunk_cols);
+        const int s_hi = min(p.K, s_lo + p.chunk_cols);
+        t.k0 = min(s_hi, s_lo + t.u * p.kt);
+        t.k1 = min(s_hi, t.k0 + p.kt);
+    }
+    return t;
+}
+
+// Byte offsets of this thread's 16-byte units in a 16 x 128 weight box written with the
+// 128-byte swizzle (unit u of row r sits at unit u ^ (r % 8)): row r units 2q, 2q+1 and
+// row r+8 units 2q, 2q+1.
+struct BoxOffs {
+    int a0, a1, b0, b1;
+};
+
+__device__ __forceinline__ BoxOffs box_offsets(int r, int q) {
+    BoxOffs o;
+    o.a0 = r * 128 + (((2 * q) ^ (r & 7)) << 4);
+    o.a1 = r * 128 + (((2 * q + 1) ^ (r & 7)) << 4);
+    o.b0 = o.a0 + 8 * 128;
+    o.b1 = o.a1 + 8 * 128;
+    return o;
+}
+
+// Rebuilds this thread's share of one weight box into the A fragments of the step's 8
+// MMAs: a[4j..4j+3] = (row r, cols 4j..4j+1), (row r+8, same), (row r, cols 4j+2..4j+3),
+// (row r+8, same), where col c means column 32q + c of the step.  mxa / mxb keep the
+// largest rebuilt magnitude of rows r / r+8 before scaling (an e4m3 NaN code spreads to
+// 0x07F0, above every finite code's 0x07E0).
+template <bool TWO>
+__device__ __forceinline__ void decode_box(const uint8_t *box, const BoxOffs &o, bool mine,
+                                           uint32_t e, uint32_t (&a)[32], uint32_t &mxa,
+                                           uint32_t &mxb) {
+    uint4 ra[2], rb[2];
+    if (mine) {
+        ra[0] = *reinterpret_cast<const uint4 *>(box + o.a0);
+        ra[1] = *reinterpret_cast<const uint4 *>(box + o.a1);
+        rb[0] = *reinterpret_cast<const uint4 *>(box + o.b0);
+        rb[1] = *reinterpret_cast<const uint4 *>(box + o.b1);
+    } else {
+        ra[0] = ra[1] = rb[0] = rb[1] = make_uint4(0, 0, 0, 0);
+    }
+    uint32_t s1, s2 = 0;
+    if (TWO) {  // exact for every exponent byte: restore e4m3 * 1, then scale by 2^(e-127)
+        s1 = 0x7B807B80u;
+        const uint32_t bb = e == 0 ? 0x0040u : (e << 7);
+        s2 = bb | (bb << 16);
+    } else {    // e <= 134: one multiply by 2^(e-7)
+        const uint32_t b = (e + 120u) << 7;
+        s1 = b | (b << 16);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint4 &av = ra[j / 4], &bv = rb[j / 4];
+        const int i = j % 4;
+        uint32_t t0, t1, u0, u1;
+        spread_codes(i == 0 ? av.x : i == 1 ? av.y : i == 2 ? av.z : av.w, t0, t1);
+        spread_codes(i == 0 ? bv.x : i == 1 ? bv.y : i == 2 ? bv.z : bv.w, u0, u1);
+        mxa = max_xorsign_abs(mxa, max_xorsign_abs(t0, t1));
+        mxb = max_xorsign_abs(mxb, max_xorsign_abs(u0, u1));
+        uint32_t alo = bf16x2_mul(t0, s1), ahi = bf16x2_mul(t1, s1);
+        uint32_t blo = bf16x2_mul(u0, s1), bhi = bf16x2_mul(u1, s1);
+        if (TWO) {
+            alo = bf16x2_mul(alo, s2);
+            ahi = bf16x2_mul(ahi, s2);
+            blo = bf16x2_mul(blo, s2);
+            bhi = bf16x2_mul(bhi, s2);
+        }
+        a[4 * j + 0] = alo;
+        a[4 * j + 1] = blo;
+        a[4 * j + 2] = ahi;
+        a[4 * j + 3] = bhi;
+    }
+}
+
+// This thread's x fragment of a step: token r, columns 32q .. 32q+31 (16 words, word i =
+// columns 2i, 2i+1), from an 8 x 128 tile stored as two 8 x 64 boxes with the 128-byte
+// swizzle.  Zero where the thread's columns are past its task.
+__device__ __forceinline__ void load_xfrag(const uint8_t *slot, int r, int q, bool mine,
+                                           uint4 (&xv)[4]) {
+    const uint8_t *row = slot + (q >> 1) * 1024 + r * 128;
+#pragma unroll
+    for (int v = 0; v < 4; ++v)
+        xv[v] = mine ? *reinterpret_cast<const uint4 *>(row + ((((q & 1) * 4 + v) ^ r) << 4))
+                     : make_uint4(0, 0, 0, 0);
+}
+
+// The step's 8 MMAs (m16n8k16, rows r / r+8 of the slab, tokens 0..7): MMA j multiplies
+// columns 4j..4j+3 of every thread's 32.  Two accumulators break the dependency chain.
+__device__ __forceinline__ void mma_step(const uint32_t (&a)[32], const uint4 (&xv)[4],
+                                         float (&acc)[2][4]) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint4 &x = xv[j / 2];
+        mma_bf16_16816(acc[j & 1], a[4 * j], a[4 * j + 1], a[4 * j + 2], a[4 * j + 3],
+                       (j & 1) ? x.z : x.x, (j & 1) ? x.w : x.y);
+    }
+}
+
+// End of a group.  red[w] holds warp w's task partial [16 rows][8 tokens]; sums them in
+// the fixed order (tasks of a split in task order, splits in split order) and stores y,
+// or stores the per-split partials.  Stores are skipped when the block met an error.
+__device__ __forceinline__ void group_epilogue(const LowParams &p, float (*red)[16][8],
+                                               const volatile int *err, int g, int gslab) {
+    const int nslabs = p.N / 16, tslab = p.S * p.tps;
+    const int mrows = min(8, p.M);
+    const int tid = threadIdx.x;
+    if (p.mode == kStreamCluster) {
+        cluster_sync();
+        if (!*err) {
+            const int total = 16 * mrows;
+            const int c = blockIdx.x % p.cluster;
+            const int per = (total + p.cluster - 1) / p.cluster;
+            const int lo = c * per, hi = min(total, lo + per);
+            for (int i = lo + tid; i < hi; i += kThreads) {
+                const int m = i / 16, row = i - m * 16;
+                float y = 0.0f;
+                for (int ss = 0; ss < p.S; ++ss) {
+                    float ps = 0.0f;
+                    for (int uu = 0; uu < p.tps; ++uu) {
+                        const int tau = ss * p.tps + uu;
+                        const float v = ld_cluster_f32(
+                            map_to_rank(&red[tau % kWarps][row][m], (uint32_t)(tau / kWarps)));
+                        ps = uu == 0 ? v : ps + v;
+                    }
+                    y = ss == 0 ? ps : y + ps;
+                }
+                p.y[((size_t)m * p.G + g) * p.N + gslab * 16 + row] = f32_to_bf16_rn(y);
+            }
+        }
+        cluster_sync();  // keep this block's shared memory alive until the others are done
+        return;
+    }
+    __syncthreads();
+    if (!*err) {
+        if (p.mode == kStreamInCta) {
+            const int per_slab = 16 * mrows;
+            for (int i = tid; i < p.spc * per_slab; i += kThreads) {
+                const int sl = i / per_slab, rem = i - sl * per_slab;
+                const int m = rem / 16, row = rem - m * 16;
+                const int sb = gslab + sl;
+                if (sb >= nslabs) continue;
+                const int w0 = sl * tslab;
+                float y = 0.0f;
+                for (int ss = 0; ss < p.S; ++ss) {
+                    float ps = red[w0 + ss * p.tps][row][m];
+                    for (int uu = 1; uu < p.tps; ++uu) ps = ps + red[w0 + ss * p.tps + uu][row][m];
+                    y = ss == 0 ? ps : y + ps;
+                }
+                p.y[((size_t)m * p.G + g) * p.N + sb * 16 + row] = f32_to_bf16_rn(y);
+            }
+        } else {
+            const int per_split = 16 * mrows;
+            for (int i = tid; i < p.spl * per_split; i += kThreads) {
+                const int ls = i / per_split, rem = i - ls * per_split;
+                const int m = rem / 16, row = rem - m * 16;
+                const int ss = (blockIdx.x % p.cps) * p.spl + ls;
+                if (ss >= p.S) continue;
+                float ps = red[ls * p.tps][row][m];
+                for (int uu = 1; uu < p.tps; ++uu) ps = ps + red[ls * p.tps + uu][row][m];
+                p.partials[(((size_t)ss * p.M + m) * p.G + g) * p.N + gslab * 16 + row] = ps;
+            }
+        }
+    }
+    __syncthreads();  // red is rewritten by the next group
+}
+
+}  // namespace
+
+// One block: 8 warps, each with a private ring of kRing slots and kRing mbarriers.  Load
+// sequence of a warp with U steps (U = groups x steps per group) and P = min(steps per
+// group, kPre) steps rebuilt ahead:
+//     W(0) .. W(P-1) | X(0) .. X(P-1) | W(P) X(P) W(P+1) X(P+1) .. W(U-1) X(U-1)
+// (W = weight box, X = x tile of a step).  Load n goes to slot n % kRing and completes
+// phase n / kRing of that slot's barrier; the warp consumes loads in the same order and
+// issues load n + kRing once load n is consumed.  X loads are issued only after the
+// dependency wait.
+__global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant__ LowParams p) {
+    extern __shared__ uint8_t dyn_smem[];
+    // the swizzled boxes need 1024-byte alignment
+    uint8_t *ring = dyn_smem + ((1024u - (smem_u32(dyn_smem) & 1023u)) & 1023u);
+    __shared__ __align__(16) float red[kWarps][16][8];
+    __shared__ __align__(8) uint64_t bars[kWarps][kRing];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_err;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int q = lane & 3, r = lane >> 2;
+    const int g = blockIdx.y;
+    const int nslabs = p.N / 16;
+    const int nst = p.kt / kKS;  // steps per group
+    const Task me = task_of(p, warp);
+    const int U = me.ngroups * nst;
+    const int P = U > 0 ? min(nst, kPre) : 0;
+    const int L = 2 * U;
+    uint8_t *const wring = ring + warp * (kRing * kSlotBytes);
+    uint64_t *const wbar = bars[warp];
+
+    if (lane == 0) {
+        for (int s = 0; s < kRing; ++s) mbar_init(&wbar[s], 1);
+        fence_mbar_init();
+    }
+    if (threadIdx.x == 0) s_err = 0;
+    if (threadIdx.x == 32) {  // the descriptors' first use should not wait for their fetch
+        prefetch_tensormap(&p.wmap);
+        prefetch_tensormap(&p.xmap);
+    }
+    if (warp == 0) tmem_alloc(&s_tmem, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    pdl_trigger();
+    // this warp's 128 TMEM columns in its lane quarter
+    const uint32_t tbase = s_tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (warp >= 4 ? 128u : 0u);
+
+    // ---------------------------------------------------------------- copy issue (lane 0)
+    int issued = 0;
+    int i_kind = 0, i_gi = 0, i_t = 0, i_slot = 0;  // next load: kind (0 W, 1 X), group, step
+    bool waited = false;                            // dependency wait done (X loads allowed)
+    const uint64_t pol = evict_first_policy();
+    auto issue_upto = [&](int limit) {  // lane 0: issue loads while fewer than `limit`
+        limit = min(limit, L);
+        if (issued < limit) fence_proxy_async_smem();  // the warp's reads of the slots first
+        while (issued < limit) {
+            if (i_kind == 1 && !waited) break;
+            const int slab = me.slab0 + i_gi * me.slab_step;
+            const int col = me.k0 + i_t * kKS;
+            const bool valid = me.active && i_gi < me.ngroups && slab < nslabs && col < me.k1;
+            uint64_t *bar = &wbar[i_slot];
+            uint8_t *dst = wring + i_slot * kSlotBytes;
+            mbar_arrive_expect_tx(bar, valid ? (uint32_t)kSlotBytes : 0u);
+            if (valid && !p.skip_loads) {
+                if (i_kind == 1) {
+                    tma_2d(dst, &p.xmap, g * p.K + col, 0, bar);
+                    tma_2d(dst + 1024, &p.xmap, g * p.K + col + 64, 0, bar);
+                } else {
+                    tma_2d_hint(dst, &p.wmap, col, g * p.N + slab * 16, bar, pol);
+                }
+            }
+            const int n = issued++;
+            i_slot = i_slot + 1 == kRing ? 0 : i_slot + 1;
+            if (n == P - 1) {               // rebuilt-ahead weights done: their x tiles next
+                i_kind = 1;
+                i_gi = 0;
+                i_t = 0;
+            } else if (n == 2 * P - 1) {    // then the streamed steps, from step P
+                i_kind = 0;
+                i_gi = P == nst ? 1 : 0;
+                i_t = P == nst ? 0 : P;
+            } else if (n >= 2 * P && i_kind == 0) {
+                i_kind = 1;                 // the x tile of the same step
+            } else {
+                i_kind = n >= 2 * P ? 0 : i_kind;
+                if (++i_t == nst) {
+                    i_t = 0;
+                    ++i_gi;
+                }
+            }
+        }
+    };
+
+    // ---------------------------------------------------------------- consumption
+    int err = 0, first_bad = 0;
+    int c_slot = 0, consumed = 0;
+    uint32_t c_par = 0;
+    auto wait_next = [&]() -> const uint8_t * {
+        const uint8_t *slot = wring + c_slot * kSlotBytes;
+        if (!err) {
+            const bool ok = mbar_wait_bounded(&wbar[c_slot], c_par, p.timeout_ns);
+            if (!__all_sync(0xFFFFFFFFu, ok)) {
+                err = 1;
+                first_bad = consumed;
+                *(volatile int *)&s_err = 1;
+                if (lane == 0) report_timeout(p.status);
+            }
+        }
+        return slot;
+    };
+    auto release = [&]() {
+        ++consumed;
+        if (++c_slot == kRing) {
+            c_slot = 0;
+            c_par ^= 1u;
+        }
+        __syncwarp();
+        if (lane == 0 && !err) issue_upto(consumed + kRing);
+    };
+    // exponent bytes of a group's task: lane l holds block (k0 / 32 + l) of the slab's row
+    // block (127 past the task); static, so read before the wait
+    const int nkb = (me.k1 - me.k0) / 32;
+    auto load_exps = [&](int gi_) -> uint32_t {
+        const int slab = me.slab0 + gi_ * me.slab_step;
+        if (me.active && gi_ < me.ngroups && slab < nslabs && lane < nkb)
+            return (uint32_t)__ldg(p.ex + (size_t)g * (p.N / 32) * (p.K / 32) +
+                                   (size_t)(slab / 2) * (p.K / 32) + me.k0 / 32 + lane);
+        return 127u;
+    };
+
+    uint32_t ereg = load_exps(0), enext = load_exps(1);
+    if (lane == 0) issue_upto(kRing);
+    bool two = __any_sync(0xFFFFFFFFu, ereg > 134u);
+    uint32_t mxa = 0, mxb = 0;
+    float acc[2][4];
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[a][c] = 0.0f;
+    const BoxOffs bo = box_offsets(r, q);
+
+    auto end_group = [&](int gi_done) {
+        uint32_t fa = nan_code_seen(mxa) ? 1u : 0u, fb = nan_code_seen(mxb) ? 1u : 0u;
+        fa |= __shfl_xor_sync(0xFFFFFFFFu, fa, 1);
+        fa |= __shfl_xor_sync(0xFFFFFFFFu, fa, 2);
+        fb |= __shfl_xor_sync(0xFFFFFFFFu, fb, 1);
+        fb |= __shfl_xor_sync(0xFFFFFFFFu, fb, 2);
+        const float qnan = __uint_as_float(0x7FC00000u);
+        float v[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            v[c] = acc[0][c] + acc[1][c];
+            if ((c < 2 && fa) || (c >= 2 && fb)) v[c] = qnan;
+            acc[0][c] = acc[1][c] = 0.0f;
+        }
+        *reinterpret_cast<float2 *>(&red[warp][r][2 * q]) = make_float2(v[0], v[1]);
+        *reinterpret_cast<float2 *>(&red[warp][r + 8][2 * q]) = make_float2(v[2], v[3]);
+        mxa = mxb = 0;
+        const int gslab = p.mode == kStreamInCta ? ((int)blockIdx.x + gi_done * (int)gridDim.x) * p.spc
+                                                 : me.slab0;
+        group_epilogue(p, red, &s_err, g, gslab);
+        ereg = enext;
+        enext = load_exps(gi_done + 2);
+        two = __any_sync(0xFFFFFFFFu, ereg > 134u);
+    };
+
+    // ---- phase A (before the wait): rebuild the first P steps of group 0 into TMEM
+    for (int u = 0; u < P; ++u) {
+        const uint8_t *slot = wait_next();
+        const int col = me.k0 + u * kKS;
+        const bool mine = me.active && me.slab0 < nslabs && col + q * 32 < me.k1;
+        const uint32_t e = __shfl_sync(0xFFFFFFFFu, ereg, (4 * u + q) & 31);
+        uint32_t a[32];
+        if (two)
+            decode_box<true>(slot, bo, mine, e, a, mxa, mxb);
+        else
+            decode_box<false>(slot, bo, mine, e, a, mxa, mxb);
+        tmem_st32(tbase + 32u * u, a);
+        release();
+    }
+    tmem_wait_st();
+
+    // ---- the dependency wait: x (and y) belong to the kernels before this one
+    pdl_wait();
+    waited = true;
+    __syncwarp();
+    if (lane == 0 && !err) issue_upto(consumed + kRing);
+
+    // ---- phase B: x tiles for the rebuilt-ahead steps, fragments back from TMEM
+    for (int u = 0; u < P; ++u) {
+        uint32_t a[32];
+        tmem_ld32(tbase + 32u * u, a);
+        const uint8_t *slot = wait_next();
+        const int col = me.k0 + u * kKS;
+        const bool boxed = me.active && me.slab0 < nslabs && col < me.k1;
+        const bool mine = boxed && col + q * 32 < me.k1;
+        uint4 xv[4];
+        load_xfrag(slot, r, q, mine, xv);
+        tmem_wait_ld();
+        if (!err && boxed) mma_step(a, xv, acc);
+        release();
+        if (u + 1 == nst) end_group(0);
+    }
+
+    // ---- phase C: the remaining steps stream weights and x and rebuild in registers
+    {
+        int gi = P == nst ? 1 : 0, t = P == nst ? 0 : P;
+        for (int u = P; u < U; ++u) {
+            const int slab = me.slab0 + gi * me.slab_step;
+            const int col = me.k0 + t * kKS;
+            const bool boxed = me.active && slab < nslabs && col < me.k1;
+            const bool mine = boxed && col + q * 32 < me.k1;
+            const uint32_t e = __shfl_sync(0xFFFFFFFFu, ereg, (4 * t + q) & 31);
+            uint32_t a[32];
+            const uint8_t *wslot = wait_next();
+            if (two)
+                decode_box<true>(wslot, bo, mine, e, a, mxa, mxb);
+            else
+                decode_box<false>(wslot, bo, mine, e, a, mxa, mxb);
+            release();
+            const uint8_t *xslot = wait_next();
+            uint4 xv[4];
+            load_xfrag(xslot, r, q, mine, xv);
+            if (!err && boxed) mma_step(a, xv, acc);
+            release();
+            if (++t == nst) {
+                end_group(gi);
+                t = 0;
+                ++gi;
+            }
+        }
+    }
+
+    // After an error, let every copy this warp issued land before the block exits.
+    if (err && lane == 0) {
+        for (int n = first_bad; n < issued; ++n)
+            (void)mbar_wait_bounded(&wbar[n % kRing], (uint32_t)((n / kRing) & 1), p.timeout_ns);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(s_tmem, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------- host side
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// A small cache of encoded maps, keyed by everything the encoding depends on.
+struct MapKey {
+    const void *ptr;
+    long long d0, d1, pitch;
+    int kind;
+    bool operator==(const MapKey &o) const {
+        return ptr == o.ptr && d0 == o.d0 && d1 == o.d1 && pitch == o.pitch && kind == o.kind;
+    }
+};
+
+cudaError_t cached_map(const MapKey &key, CUtensorMap *out) {
+    static std::mutex mu;
+    static MapKey keys[64];
+    static CUtensorMap maps[64];
+    static int used = 0, next = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (keys[i] == key) {
+            *out = maps[i];
+            return cudaSuccess;
+        }
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return cudaErrorNotSupported;
+    CUtensorMap m;
+    CUresult res;
+    const cuuint32_t estr[2] = {1u, 1u};
+    if (key.kind == 0) {  // weights: [rows][K] bytes, box 128 x 16
+        const cuuint64_t dims[2] = {(cuuint64_t)key.d0, (cuuint64_t)key.d1};
+        const cuuint64_t strides[1] = {(cuuint64_t)key.pitch};
+        const cuuint32_t box[2] = {(cuuint32_t)kKS, 16u};
+        res = fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(key.ptr), dims, strides, box,
+                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {              // x: [M][G*K] bf16 with row pitch ldx, box 64 x 8 (rows >= M read 0)
+        const cuuint64_t dims[2] = {(cuuint64_t)key.d0, (cuuint64_t)key.d1};
+        const cuuint64_t strides[1] = {(cuuint64_t)key.pitch * 2u};
+        const cuuint32_t box[2] = {64u, 8u};
+        res = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(key.ptr), dims, strides,
+                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (res != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    keys[next] = key;
+    maps[next] = m;
+    next = (next + 1) % 64;
+    if (used < 64) ++used;
+    *out = m;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+StreamPlan plan_lowm(int M, int N, int K, int G, int S, bool partials) {
+    return plan_stream_ks(M, N, K, G, S, partials, kKS, 1, kMaxKt);
+}
+
+cudaError_t launch_lowm(const StreamPlan &pl, const void *x, long long ldx, const uint8_t *w8,
+                        const uint8_t *ex, void *y, float *partials, int M, int N, int K, int G,
+                        cudaStream_t stream) {
+    if (M < 1 || M > 8 || pl.nt8 != 1 || pl.m_chunks != 1 || pl.kt > kMaxKt) return cudaErrorInvalidValue;
+    const Options opt = options();
+    LowParams prm;
+    cudaError_t e = cached_map(MapKey{w8, K, (long long)G * N, K, 0}, &prm.wmap);
+    if (e != cudaSuccess) return e;
+    e = cached_map(MapKey{x, (long long)G * K, M, ldx, 1}, &prm.xmap);
+    if (e != cudaSuccess) return e;
+    prm.ex = ex;
+    prm.y = static_cast<uint16_t *>(y);
+    prm.partials = partials;
+    prm.M = M;
+    prm.N = N;
+    prm.K = K;
+    prm.G = G;
+    prm.S = pl.S;
+    prm.chunk_cols = pl.chunk_cols;
+    prm.kt = pl.kt;
+    prm.tps = pl.tps;
+    prm.spc = pl.spc;
+    prm.cluster = pl.cluster;
+    prm.spl = pl.spl;
+    prm.cps = pl.cps;
+    prm.mode = pl.mode;
+    prm.timeout_ns = opt.timeout_ns;
+    prm.skip_loads = opt.skip_loads;
+    prm.status = status_word();
+    if (!prm.status) return cudaErrorInvalidSymbol;
+
+    const size_t smem = (size_t)kRingBytes + 1024;
+    static int configured[64] = {0};
+    static int cap[64] = {0};
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!__atomic_load_n(&configured[dev], __ATOMIC_ACQUIRE)) {
+        e = cudaFuncSetAttribute(lowm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        // two blocks an SM need the largest shared-memory carve-out
+        e = cudaFuncSetAttribute(lowm_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        // Persistent grid: two blocks an SM, the most that fit (shared memory, registers
+        // under the launch bounds, and two blocks of 256 TMEM columns fill tensor memory).
+        // The occupancy query is not used: it reports one block for this kernel although
+        // two are resident at once.  If fewer fit, the blocks simply run in turn.
+        __atomic_store_n(&cap[dev], sms * (512 / kTmemCols), __ATOMIC_RELEASE);
+        __atomic_store_n(&configured[dev], 1, __ATOMIC_RELEASE);
+    }
+    cudaLaunchConfig_t cfg = {};
+    int gx = pl.grid_x;
+    if (pl.mode == kStreamInCta) gx = std::min(gx, __atomic_load_n(&cap[dev], __ATOMIC_ACQUIRE));
+    cfg.gridDim = dim3((unsigned)gx, (unsigned)G, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    if (pl.mode == kStreamCluster) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = (unsigned)pl.cluster;
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (opt.pdl) {
+        attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, lowm_kernel, prm);
+}
+
+}  // namespace bsf8

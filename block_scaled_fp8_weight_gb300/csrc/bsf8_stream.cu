@@ -441,7 +441,8 @@ StreamPlan plan_stream(int M, int N, int K, int G, int S, bool partials) {
     return plan_stream_ks(M, N, K, G, S, partials, nt8 == 1 ? 128 : 64, 4);
 }
 
-StreamPlan plan_stream_ks(int M, int N, int K, int G, int S, bool partials, int ks, int max_nt8) {
+StreamPlan plan_stream_ks(int M, int N, int K, int G, int S, bool partials, int ks, int max_nt8,
+                          int max_kt) {
     StreamPlan pl{};
     pl.nt8 = std::min(max_nt8, (M + 7) / 8);
     pl.m_chunks = (M + 8 * pl.nt8 - 1) / (8 * pl.nt8);
@@ -452,6 +453,7 @@ StreamPlan plan_stream_ks(int M, int N, int K, int G, int S, bool partials, int 
     // before the dependency wait), and at most 8 tasks per split.
     int kt = std::max(512, (pl.chunk_cols + 7) / 8);
     kt = (kt + ks - 1) / ks * ks;
+    kt = std::min(kt, std::max(ks, max_kt / ks * ks));
     pl.kt = kt;
     pl.tps = (pl.chunk_cols + kt - 1) / kt;
     const int tslab = S * pl.tps;

@@ -206,8 +206,14 @@ enum {
     BSF8_OPT_WAIT_TIMEOUT_NS = 2,  /* bound of every in-kernel wait (default 2e9 ns)   */
     BSF8_OPT_DEBUG_SKIP_LOADS = 3, /* test only: the TMA-ring GEMM issues no weight    */
                                    /* loads, so its waits run out (BSF8_ERR_TIMEOUT)   */
-    BSF8_OPT_GEMM_PATH = 4         /* 0 (default): weight-streaming kernel; 1: the     */
-                                   /* shared-memory TMA-ring kernel (split_k <= 8)     */
+    BSF8_OPT_GEMM_PATH = 4         /* 0 (default): the kernel chosen by shape -- the    */
+                                   /* decode-ahead kernel up to 8 token rows, the      */
+                                   /* TMA-fed kernel up to 16, the cp.async streaming  */
+                                   /* kernel beyond; 1: the shared-memory TMA-ring     */
+                                   /* kernel (split_k <= 8); 2: the streaming kernel;  */
+                                   /* 3: the TMA-fed kernel (M <= 16); 4: the          */
+                                   /* decode-ahead kernel (M <= 8).  A forced kernel   */
+                                   /* that does not apply to a call falls back to 0.   */
 };
 /* Errors: BSF8_ERR_VALUE for an unknown option or a negative value. */
 int bsf8_set_option(int option, int64_t value);

@@ -257,3 +257,27 @@ def test_tma_ring_path_matches_oracle_and_its_two_pass(bsf8_lib, wk, M, S):
     assert np.array_equal(y, two)
     rows = [0, M - 1]
     assert_gemm_close(y[rows], oracle.gemm(x[rows], w8, ex))
+
+
+@pytest.mark.parametrize("path", [2, 3, 4])
+@pytest.mark.parametrize("wk,M,S", [(wl.WO_A, 6, 8), (wl.TINY, 4, 1), (wl.DOWN_PROJ, 6, 4),
+                                    (wl.TINY, 3, 16), (wl.WO_A, 1, 80)])
+def test_forced_kernels_match_oracle_and_each_other(bsf8_lib, path, wk, M, S):
+    """Each kernel forced through BSF8_OPT_GEMM_PATH (2: streaming, 3: TMA-fed, 4:
+    decode-ahead) in its in-block, cluster (S = 16) and partials (S = 80) modes: within
+    the tolerance of the oracle, bitwise equal to its own two-pass form, and bitwise
+    reproducible."""
+    w8, ex = wk.weights()
+    x = wk.x(M=M)
+    w8_d, ex_d, x_d = dev(w8, ex, x)
+    bsf8.set_option(bsf8.OPT_GEMM_PATH, path)
+    try:
+        y = run(x_d, w8_d, ex_d, S)
+        y2 = run(x_d, w8_d, ex_d, S)
+        two = bf16_bits(bsf8.splitk_reduce(bsf8.gemm_partials(x_d, w8_d, ex_d, S)))
+        assert bsf8.device_status() == 0
+    finally:
+        bsf8.set_option(bsf8.OPT_GEMM_PATH, 0)
+    assert np.array_equal(y, y2)
+    assert np.array_equal(y, two)
+    assert_gemm_close(y, oracle.gemm(x, w8, ex))

@@ -59,18 +59,19 @@ def test_down_proj_padding_leaves_output_bitwise_unchanged(bsf8_lib):
     assert np.array_equal(y6, y7)
 
 
-@pytest.mark.parametrize("path", [0, 1])
-def test_timeout_is_reported_without_hanging(bsf8_lib, path):
+@pytest.mark.parametrize("path,M", [(0, 4), (0, 12), (1, 4)])
+def test_timeout_is_reported_without_hanging(bsf8_lib, path, M):
     """With the test-only option that suppresses the weight loads, the mbarrier waits of
-    the TMA-fed GEMM (path 0, the default for these sizes) and of the TMA-ring GEMM
-    (path 1) run out after the shortened bound; the kernel records BSF8_ERR_TIMEOUT,
-    writes nothing and returns.  Normal calls work again afterwards."""
+    the decode-ahead GEMM (path 0, up to 8 token rows), the TMA-fed GEMM (path 0, 9 to 16
+    rows) and the TMA-ring GEMM (path 1) run out after the shortened bound; the kernel
+    records BSF8_ERR_TIMEOUT, writes nothing and returns.  Normal calls work again
+    afterwards."""
     w8, ex = wl.TINY.weights()
-    x = wl.TINY.x()
+    x = wl.TINY.x(M=M)
     w8_d, ex_d, x_d = to_dev_u8(w8), to_dev_u8(ex), to_dev_bf16(x)
     assert bsf8.device_status() == 0
     old = bsf8.get_option(bsf8.OPT_WAIT_TIMEOUT_NS)
-    y = torch.full((4, 1, 256), 7.0, dtype=torch.bfloat16, device="cuda")
+    y = torch.full((M, 1, 256), 7.0, dtype=torch.bfloat16, device="cuda")
     try:
         bsf8.set_option(bsf8.OPT_GEMM_PATH, path)
         bsf8.set_option(bsf8.OPT_WAIT_TIMEOUT_NS, 2_000_000)     # 2 ms
