@@ -12,31 +12,28 @@
 // and their exponents are static, so everything that touches only them runs before the
 // wait, while the previous kernel is still working:
 //
-//   1. each warp streams its first (up to 4) 16 x 128 weight boxes into shared memory by
-//      TMA, rebuilds them exactly to bf16 MMA fragments in registers and parks the
-//      fragments in tensor memory (tcgen05.st: 32 columns of the warp's 32 TMEM lanes per
-//      box, 128 columns per warp, 256 per block);
+//   1. each warp streams its task's weight boxes (16 rows x 128 columns, up to 4) into
+//      shared memory by TMA, rebuilds them exactly to bf16 MMA fragments in registers and
+//      parks the fragments in tensor memory (tcgen05.st: 32 columns of the warp's 32 TMEM
+//      lanes per box, 128 columns per warp, 256 per block);
 //   2. griddepcontrol.wait;
-//   3. x arrives by TMA (8 token rows x 128 columns per step, rows >= M zero-filled); the
-//      warp reads its fragments back (tcgen05.ld) and runs the MMAs.  Steps beyond the
-//      decoded-ahead prefix stream weights and x through the same ring and rebuild in
-//      registers as they go.
+//   3. x arrives (8 token rows x 128 columns per step, rows >= M zero-filled), the warp
+//      reads its fragments back (tcgen05.ld) and runs the MMAs, and the block sums its
+//      warps' partials in the fixed split order.
 //
-// After the wait a call then costs little more than its x round trip, its MMAs and its
-// fixed-order reduction; the rebuild work, the bulk of the instructions, overlaps the
-// previous kernel.  Two blocks fit on an SM (96 KB of ring, 256 TMEM columns, <= 128
-// registers a thread), so the next call's blocks become resident and start streaming
-// while this call finishes.
+// After the wait a call costs its x round trip, a few MMAs and the reduction; the rebuild,
+// the bulk of the instructions, overlaps the previous kernel.  Two blocks fit on an SM
+// (256 TMEM columns each; the shared-memory request keeps a third out), so the next call's
+// blocks become resident and rebuild while this call finishes.
 //
-// Work decomposition (bsf8_stream.cu): a warp task is 16 weight rows (one slab) x a
-// column range inside one split; a block's 8 warps hold a group of tasks and walk groups
-// persistently (in-block mode), or a block is one group of a cluster (cluster mode, the
-// splits of a slab summed over DSMEM) or writes fp32 partials (partials mode).
+// Work decomposition (bsf8_stream.cu) with tasks of at most 512 columns: a warp task is 16
+// weight rows (one slab) x a column range inside one split; a block's 8 warps hold one
+// group of tasks (in-block mode: the splits of its slabs summed in the block), or a block
+// is one group of a cluster (cluster mode, the splits of a slab summed over DSMEM) or
+// writes fp32 partials (partials mode).  Every block holds exactly one group.
 //
-// Each warp owns a private ring of 6 slots of 2 KB (a weight box or an x tile each) with
-// one mbarrier per slot; its lane 0 issues the copies, so no warp ever waits for another
-// until the group's reduction.  Every wait is bounded: on timeout the block records
-// BSF8_ERR_TIMEOUT, stores nothing, lets its copies land and returns.
+// Every wait is bounded: on timeout the block records BSF8_ERR_TIMEOUT, stores nothing,
+// lets its copies land and returns.
 #include "bsf8_device.cuh"
 #include "bsf8_internal.h"
 
@@ -53,16 +50,20 @@ constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kKS = 128;           // columns per step
 constexpr int kSlotBytes = 2048;   // a 16 x 128 weight box, or an 8 x 128 bf16 x tile
-constexpr int kRing = 6;           // slots per warp
-constexpr int kPre = 4;            // steps per warp rebuilt ahead into tensor memory
+constexpr int kPre = 4;            // steps per task, all rebuilt ahead into tensor memory
+constexpr int kMaxKt = kPre * kKS; // task columns
 constexpr int kTmemCols = 256;     // per block: 128 columns for each of two warps a quarter
-constexpr int kRingBytes = kWarps * kRing * kSlotBytes;
-constexpr int kMaxKt = 1024;       // task columns: at most 32 exponent blocks (one per lane)
-static_assert(2 * (kRingBytes + 1024 + 6 * 1024) <= 228 * 1024, "two blocks fit an SM");
+// Shared-memory request: 8 warps x 4 slots, padded so that a third block never fits an SM
+// (its tensor-memory allocation would wait for one of the other two to finish).
+constexpr int kSmemBytes = 80 * 1024;
+static_assert(kWarps * kPre * kSlotBytes + 1024 <= kSmemBytes, "slots fit the request");
+static_assert(3 * (kSmemBytes + 1024) > 228 * 1024, "at most two blocks an SM");
+static_assert(2 * (kSmemBytes + 1024 + 6 * 1024) <= 228 * 1024, "two blocks fit an SM");
 
 struct LowParams {
     CUtensorMap wmap;  // w8 as a [G*N rows][K columns] byte matrix, box 128 x 16
-    CUtensorMap xmap;  // x as a [M rows][G*K columns] bf16 matrix (row pitch ldx), box 64 x 8
+    const uint16_t *x;  // [M][ldx] bf16
+    long long ldx;
     const uint8_t *ex;
     uint16_t *y;
     float *partials;
@@ -81,15 +82,6 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
     return pol;
 }
 
-__device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, int c0, int c1,
-                                       uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
-        : "memory");
-}
-
 __device__ __forceinline__ void tma_2d_hint(void *dst, const CUtensorMap *map, int c0, int c1,
                                             uint64_t *bar, uint64_t policy) {
     asm volatile(
@@ -103,10 +95,17 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// Orders this thread's earlier generic-proxy shared-memory accesses before its later
-// async-proxy ones (a TMA copy into a slot the warp has just read).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+// 16-byte global -> shared copy through the load/store path (cp.async); src_bytes < 16
+// zero-fills the rest (0: nothing is read).
+__device__ __forceinline__ void cp_async_16_zfill(void *dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
+// Waits until this thread's cp.async copies have landed.
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
@@ -390,20 +389,24 @@ __device__ __forceinline__ void group_epilogue(const LowParams &p, float (*red)[
 
 }  // namespace
 
-// One block: 8 warps, each with a private ring of kRing slots and kRing mbarriers.  Load
-// sequence of a warp with U steps (U = groups x steps per group) and P = min(steps per
-// group, kPre) steps rebuilt ahead:
-//     W(0) .. W(P-1) | X(0) .. X(P-1) | W(P) X(P) W(P+1) X(P+1) .. W(U-1) X(U-1)
-// (W = weight box, X = x tile of a step).  Load n goes to slot n % kRing and completes
-// phase n / kRing of that slot's barrier; the warp consumes loads in the same order and
-// issues load n + kRing once load n is consumed.  X loads are issued only after the
-// dependency wait.
+// One block: 8 warps.  Warp w owns an 8 KB region of shared memory (4 slots of 2 KB) and
+// one mbarrier.  Its task has nst <= 4 steps of 128 columns.
+//   before the wait: lane 0 arms the barrier with the task's weight bytes and issues one TMA
+//     box (16 rows x 128 columns, 128-byte swizzle) per step into slot t; the warp waits,
+//     rebuilds each box into its 32 fragment registers and parks them in tensor memory;
+//   after the wait: every lane copies its share of the task's x tiles (8 token rows x 128
+//     columns a step, 16 bytes a copy) into the same slots with cp.async, in the layout of
+//     a 128-byte-swizzled box; then, step by step, the fragments come back from tensor
+//     memory (tcgen05.ld) and meet x in the MMAs.
+// One barrier covers all of a warp's boxes: the copies complete in one transaction count,
+// far faster than a barrier per box.  x goes through the load/store path, not the TMA unit,
+// so the post-wait copies of all 8 warps run in parallel.
 __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant__ LowParams p) {
     extern __shared__ uint8_t dyn_smem[];
     // the swizzled boxes need 1024-byte alignment
     uint8_t *ring = dyn_smem + ((1024u - (smem_u32(dyn_smem) & 1023u)) & 1023u);
     __shared__ __align__(16) float red[kWarps][16][8];
-    __shared__ __align__(8) uint64_t bars[kWarps][kRing];
+    __shared__ __align__(8) uint64_t wbar[kWarps];
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
 
@@ -412,23 +415,19 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
     const int q = lane & 3, r = lane >> 2;
     const int g = blockIdx.y;
     const int nslabs = p.N / 16;
-    const int nst = p.kt / kKS;  // steps per group
+    const int nst = p.kt / kKS;  // steps of a task (<= kPre)
     const Task me = task_of(p, warp);
-    const int U = me.ngroups * nst;
-    const int P = U > 0 ? min(nst, kPre) : 0;
-    const int L = 2 * U;
-    uint8_t *const wring = ring + warp * (kRing * kSlotBytes);
-    uint64_t *const wbar = bars[warp];
+    uint8_t *const region = ring + warp * (kPre * kSlotBytes);
+    // every block holds exactly one group (the grid is the plan's, not capped)
+    const int slab = me.slab0;
+    const bool slab_ok = me.active && me.ngroups > 0 && slab < nslabs;
 
     if (lane == 0) {
-        for (int s = 0; s < kRing; ++s) mbar_init(&wbar[s], 1);
+        mbar_init(&wbar[warp], 1);
         fence_mbar_init();
     }
     if (threadIdx.x == 0) s_err = 0;
-    if (threadIdx.x == 32) {  // the descriptors' first use should not wait for their fetch
-        prefetch_tensormap(&p.wmap);
-        prefetch_tensormap(&p.xmap);
-    }
+    if (threadIdx.x == 32) prefetch_tensormap(&p.wmap);
     if (warp == 0) tmem_alloc(&s_tmem, kTmemCols);
     tc_fence_before();
     __syncthreads();
@@ -437,101 +436,103 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
     // this warp's 128 TMEM columns in its lane quarter
     const uint32_t tbase = s_tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (warp >= 4 ? 128u : 0u);
 
-    // ---------------------------------------------------------------- copy issue (lane 0)
-    int issued = 0;
-    int i_kind = 0, i_gi = 0, i_t = 0, i_slot = 0;  // next load: kind (0 W, 1 X), group, step
-    bool waited = false;                            // dependency wait done (X loads allowed)
-    const uint64_t pol = evict_first_policy();
-    auto issue_upto = [&](int limit) {  // lane 0: issue loads while fewer than `limit`
-        limit = min(limit, L);
-        if (issued < limit) fence_proxy_async_smem();  // the warp's reads of the slots first
-        while (issued < limit) {
-            if (i_kind == 1 && !waited) break;
-            const int slab = me.slab0 + i_gi * me.slab_step;
-            const int col = me.k0 + i_t * kKS;
-            const bool valid = me.active && i_gi < me.ngroups && slab < nslabs && col < me.k1;
-            uint64_t *bar = &wbar[i_slot];
-            uint8_t *dst = wring + i_slot * kSlotBytes;
-            mbar_arrive_expect_tx(bar, valid ? (uint32_t)kSlotBytes : 0u);
-            if (valid && !p.skip_loads) {
-                if (i_kind == 1) {
-                    tma_2d(dst, &p.xmap, g * p.K + col, 0, bar);
-                    tma_2d(dst + 1024, &p.xmap, g * p.K + col + 64, 0, bar);
-                } else {
-                    tma_2d_hint(dst, &p.wmap, col, g * p.N + slab * 16, bar, pol);
-                }
-            }
-            const int n = issued++;
-            i_slot = i_slot + 1 == kRing ? 0 : i_slot + 1;
-            if (n == P - 1) {               // rebuilt-ahead weights done: their x tiles next
-                i_kind = 1;
-                i_gi = 0;
-                i_t = 0;
-            } else if (n == 2 * P - 1) {    // then the streamed steps, from step P
-                i_kind = 0;
-                i_gi = P == nst ? 1 : 0;
-                i_t = P == nst ? 0 : P;
-            } else if (n >= 2 * P && i_kind == 0) {
-                i_kind = 1;                 // the x tile of the same step
-            } else {
-                i_kind = n >= 2 * P ? 0 : i_kind;
-                if (++i_t == nst) {
-                    i_t = 0;
-                    ++i_gi;
-                }
-            }
+    // ---- weights (static): all of the task's boxes on one barrier
+    int nbox = 0;  // boxes issued (steps whose first column is inside the task)
+    if (slab_ok)
+        for (int t = 0; t < nst; ++t) nbox += me.k0 + t * kKS < me.k1 ? 1 : 0;
+    if (lane == 0) {
+        mbar_arrive_expect_tx(&wbar[warp], (uint32_t)(nbox * kSlotBytes));
+        if (!p.skip_loads) {
+            const uint64_t pol = evict_first_policy();
+            for (int t = 0; t < nbox; ++t)
+                tma_2d_hint(region + t * kSlotBytes, &p.wmap, me.k0 + t * kKS, g * p.N + slab * 16,
+                            &wbar[warp], pol);
         }
-    };
-
-    // ---------------------------------------------------------------- consumption
-    int err = 0, first_bad = 0;
-    int c_slot = 0, consumed = 0;
-    uint32_t c_par = 0;
-    auto wait_next = [&]() -> const uint8_t * {
-        const uint8_t *slot = wring + c_slot * kSlotBytes;
-        if (!err) {
-            const bool ok = mbar_wait_bounded(&wbar[c_slot], c_par, p.timeout_ns);
-            if (!__all_sync(0xFFFFFFFFu, ok)) {
-                err = 1;
-                first_bad = consumed;
-                *(volatile int *)&s_err = 1;
-                if (lane == 0) report_timeout(p.status);
-            }
-        }
-        return slot;
-    };
-    auto release = [&]() {
-        ++consumed;
-        if (++c_slot == kRing) {
-            c_slot = 0;
-            c_par ^= 1u;
-        }
-        __syncwarp();
-        if (lane == 0 && !err) issue_upto(consumed + kRing);
-    };
-    // exponent bytes of a group's task: lane l holds block (k0 / 32 + l) of the slab's row
-    // block (127 past the task); static, so read before the wait
+    }
+    // The task's x rows, pulled into L2 while the previous kernel runs.  They may still
+    // change before the wait; a prefetch only moves lines into L2, where the producer's
+    // writes land as well, and x is read after the wait from L2 (cp.async.cg), so the
+    // copies see the producer's values.  Where x is already in L2 this costs nothing.
+    if (slab_ok && lane < p.M && lane < 8 && me.k1 > me.k0)
+        prefetch_l2(p.x + (size_t)lane * p.ldx + (size_t)g * p.K + me.k0,
+                    (uint32_t)((me.k1 - me.k0) * 2));
+    // exponent bytes of the task: lane l holds block k0/32 + l of the slab's row block
     const int nkb = (me.k1 - me.k0) / 32;
-    auto load_exps = [&](int gi_) -> uint32_t {
-        const int slab = me.slab0 + gi_ * me.slab_step;
-        if (me.active && gi_ < me.ngroups && slab < nslabs && lane < nkb)
-            return (uint32_t)__ldg(p.ex + (size_t)g * (p.N / 32) * (p.K / 32) +
-                                   (size_t)(slab / 2) * (p.K / 32) + me.k0 / 32 + lane);
-        return 127u;
-    };
+    const uint32_t ereg =
+        slab_ok && lane < nkb
+            ? (uint32_t)__ldg(p.ex + (size_t)g * (p.N / 32) * (p.K / 32) +
+                              (size_t)(slab / 2) * (p.K / 32) + me.k0 / 32 + lane)
+            : 127u;
+    const bool two = __any_sync(0xFFFFFFFFu, ereg > 134u);
+    const BoxOffs bo = box_offsets(r, q);
 
-    uint32_t ereg = load_exps(0), enext = load_exps(1);
-    if (lane == 0) issue_upto(kRing);
-    bool two = __any_sync(0xFFFFFFFFu, ereg > 134u);
+    // ---- before the wait: rebuild every step into tensor memory
+    int err = 0;
     uint32_t mxa = 0, mxb = 0;
+    {
+        const bool ok = mbar_wait_bounded(&wbar[warp], 0u, p.timeout_ns);
+        if (!__all_sync(0xFFFFFFFFu, ok)) {
+            err = 1;
+            *(volatile int *)&s_err = 1;
+            if (lane == 0) report_timeout(p.status);
+        }
+    }
+    for (int t = 0; t < nst; ++t) {
+        const int col = me.k0 + t * kKS;
+        const bool mine = !err && slab_ok && col + q * 32 < me.k1;
+        const uint32_t e = __shfl_sync(0xFFFFFFFFu, ereg, (4 * t + q) & 31);
+        uint32_t a[32];
+        if (two)
+            decode_box<true>(region + t * kSlotBytes, bo, mine, e, a, mxa, mxb);
+        else
+            decode_box<false>(region + t * kSlotBytes, bo, mine, e, a, mxa, mxb);
+        tmem_st32(tbase + 32u * t, a);
+    }
+    tmem_wait_st();
+    __syncwarp();
+
+    // ---- the dependency wait: x (and y) belong to the kernels before this one
+    pdl_wait();
+
+    // ---- x tiles of the task's steps into the slots (16-byte copies, rows >= M as zeros)
+    {
+        const int unit = lane & 15;  // 16-byte unit of a 256-byte tile row
+        const long long gk = (long long)p.G * p.K;
+        for (int t = 0; t < nst; ++t) {
+            const int col = me.k0 + t * kKS + unit * 8;  // first of the copy's 8 columns
+            uint8_t *tile = region + t * kSlotBytes + (unit >> 3) * 1024;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int row = (lane >> 4) + 2 * i;
+                const bool in = slab_ok && row < p.M && (long long)g * p.K + col < gk;
+                const uint16_t *src = p.x + (in ? (size_t)row * p.ldx + (size_t)g * p.K + col : 0);
+                cp_async_16_zfill(tile + row * 128 + (((unit & 7) ^ row) << 4), src, in ? 16u : 0u);
+            }
+        }
+        cp_async_wait_all();
+        __syncwarp();
+    }
+
+    // ---- MMAs: fragments back from tensor memory, x from the slots
     float acc[2][4];
 #pragma unroll
     for (int a = 0; a < 2; ++a)
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[a][c] = 0.0f;
-    const BoxOffs bo = box_offsets(r, q);
+    for (int t = 0; t < nst; ++t) {
+        uint32_t a[32];
+        tmem_ld32(tbase + 32u * t, a);
+        const int col = me.k0 + t * kKS;
+        const bool boxed = slab_ok && col < me.k1;
+        const bool mine = boxed && col + q * 32 < me.k1;
+        uint4 xv[4];
+        load_xfrag(region + t * kSlotBytes, r, q, mine, xv);
+        tmem_wait_ld();
+        if (!err && boxed) mma_step(a, xv, acc);
+    }
 
-    auto end_group = [&](int gi_done) {
+    // ---- the group's fixed-order reduction and store
+    {
         uint32_t fa = nan_code_seen(mxa) ? 1u : 0u, fb = nan_code_seen(mxb) ? 1u : 0u;
         fa |= __shfl_xor_sync(0xFFFFFFFFu, fa, 1);
         fa |= __shfl_xor_sync(0xFFFFFFFFu, fa, 2);
@@ -543,91 +544,16 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
         for (int c = 0; c < 4; ++c) {
             v[c] = acc[0][c] + acc[1][c];
             if ((c < 2 && fa) || (c >= 2 && fb)) v[c] = qnan;
-            acc[0][c] = acc[1][c] = 0.0f;
         }
         *reinterpret_cast<float2 *>(&red[warp][r][2 * q]) = make_float2(v[0], v[1]);
         *reinterpret_cast<float2 *>(&red[warp][r + 8][2 * q]) = make_float2(v[2], v[3]);
-        mxa = mxb = 0;
-        const int gslab = p.mode == kStreamInCta ? ((int)blockIdx.x + gi_done * (int)gridDim.x) * p.spc
-                                                 : me.slab0;
+        const int gslab = p.mode == kStreamInCta ? (int)blockIdx.x * p.spc : me.slab0;
         group_epilogue(p, red, &s_err, g, gslab);
-        ereg = enext;
-        enext = load_exps(gi_done + 2);
-        two = __any_sync(0xFFFFFFFFu, ereg > 134u);
-    };
-
-    // ---- phase A (before the wait): rebuild the first P steps of group 0 into TMEM
-    for (int u = 0; u < P; ++u) {
-        const uint8_t *slot = wait_next();
-        const int col = me.k0 + u * kKS;
-        const bool mine = me.active && me.slab0 < nslabs && col + q * 32 < me.k1;
-        const uint32_t e = __shfl_sync(0xFFFFFFFFu, ereg, (4 * u + q) & 31);
-        uint32_t a[32];
-        if (two)
-            decode_box<true>(slot, bo, mine, e, a, mxa, mxb);
-        else
-            decode_box<false>(slot, bo, mine, e, a, mxa, mxb);
-        tmem_st32(tbase + 32u * u, a);
-        release();
-    }
-    tmem_wait_st();
-
-    // ---- the dependency wait: x (and y) belong to the kernels before this one
-    pdl_wait();
-    waited = true;
-    __syncwarp();
-    if (lane == 0 && !err) issue_upto(consumed + kRing);
-
-    // ---- phase B: x tiles for the rebuilt-ahead steps, fragments back from TMEM
-    for (int u = 0; u < P; ++u) {
-        uint32_t a[32];
-        tmem_ld32(tbase + 32u * u, a);
-        const uint8_t *slot = wait_next();
-        const int col = me.k0 + u * kKS;
-        const bool boxed = me.active && me.slab0 < nslabs && col < me.k1;
-        const bool mine = boxed && col + q * 32 < me.k1;
-        uint4 xv[4];
-        load_xfrag(slot, r, q, mine, xv);
-        tmem_wait_ld();
-        if (!err && boxed) mma_step(a, xv, acc);
-        release();
-        if (u + 1 == nst) end_group(0);
     }
 
-    // ---- phase C: the remaining steps stream weights and x and rebuild in registers
-    {
-        int gi = P == nst ? 1 : 0, t = P == nst ? 0 : P;
-        for (int u = P; u < U; ++u) {
-            const int slab = me.slab0 + gi * me.slab_step;
-            const int col = me.k0 + t * kKS;
-            const bool boxed = me.active && slab < nslabs && col < me.k1;
-            const bool mine = boxed && col + q * 32 < me.k1;
-            const uint32_t e = __shfl_sync(0xFFFFFFFFu, ereg, (4 * t + q) & 31);
-            uint32_t a[32];
-            const uint8_t *wslot = wait_next();
-            if (two)
-                decode_box<true>(wslot, bo, mine, e, a, mxa, mxb);
-            else
-                decode_box<false>(wslot, bo, mine, e, a, mxa, mxb);
-            release();
-            const uint8_t *xslot = wait_next();
-            uint4 xv[4];
-            load_xfrag(xslot, r, q, mine, xv);
-            if (!err && boxed) mma_step(a, xv, acc);
-            release();
-            if (++t == nst) {
-                end_group(gi);
-                t = 0;
-                ++gi;
-            }
-        }
-    }
-
-    // After an error, let every copy this warp issued land before the block exits.
-    if (err && lane == 0) {
-        for (int n = first_bad; n < issued; ++n)
-            (void)mbar_wait_bounded(&wbar[n % kRing], (uint32_t)((n / kRing) & 1), p.timeout_ns);
-    }
+    // After an error, let the weight boxes this warp issued land before the block exits.
+    if (err && lane == 0 && nbox > 0 && !p.skip_loads)
+        (void)mbar_wait_bounded(&wbar[warp], 0u, p.timeout_ns);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -659,49 +585,38 @@ EncodeTiledFn encode_tiled_fn() {
     return fn;
 }
 
-// A small cache of encoded maps, keyed by everything the encoding depends on.
+// Tensor maps of recently used weights ([rows][K] bytes, box 128 x 16, 128-byte swizzle).
+// A map encodes only the address and the shape.
 struct MapKey {
     const void *ptr;
-    long long d0, d1, pitch;
-    int kind;
-    bool operator==(const MapKey &o) const {
-        return ptr == o.ptr && d0 == o.d0 && d1 == o.d1 && pitch == o.pitch && kind == o.kind;
-    }
+    long long rows;
+    int K;
 };
 
-cudaError_t cached_map(const MapKey &key, CUtensorMap *out) {
+cudaError_t weight_map(const uint8_t *w8, long long rows, int K, CUtensorMap *out) {
     static std::mutex mu;
     static MapKey keys[64];
     static CUtensorMap maps[64];
     static int used = 0, next = 0;
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < used; ++i)
-        if (keys[i] == key) {
+        if (keys[i].ptr == w8 && keys[i].rows == rows && keys[i].K == K) {
             *out = maps[i];
             return cudaSuccess;
         }
     EncodeTiledFn fn = encode_tiled_fn();
     if (!fn) return cudaErrorNotSupported;
     CUtensorMap m;
-    CUresult res;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K};
+    const cuuint32_t box[2] = {(cuuint32_t)kKS, 16u};
     const cuuint32_t estr[2] = {1u, 1u};
-    if (key.kind == 0) {  // weights: [rows][K] bytes, box 128 x 16
-        const cuuint64_t dims[2] = {(cuuint64_t)key.d0, (cuuint64_t)key.d1};
-        const cuuint64_t strides[1] = {(cuuint64_t)key.pitch};
-        const cuuint32_t box[2] = {(cuuint32_t)kKS, 16u};
-        res = fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(key.ptr), dims, strides, box,
-                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    } else {              // x: [M][G*K] bf16 with row pitch ldx, box 64 x 8 (rows >= M read 0)
-        const cuuint64_t dims[2] = {(cuuint64_t)key.d0, (cuuint64_t)key.d1};
-        const cuuint64_t strides[1] = {(cuuint64_t)key.pitch * 2u};
-        const cuuint32_t box[2] = {64u, 8u};
-        res = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(key.ptr), dims, strides,
-                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                 CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    }
+    const CUresult res = fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(w8), dims,
+                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (res != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    keys[next] = key;
+    keys[next] = MapKey{w8, rows, K};
     maps[next] = m;
     next = (next + 1) % 64;
     if (used < 64) ++used;
@@ -721,10 +636,10 @@ cudaError_t launch_lowm(const StreamPlan &pl, const void *x, long long ldx, cons
     if (M < 1 || M > 8 || pl.nt8 != 1 || pl.m_chunks != 1 || pl.kt > kMaxKt) return cudaErrorInvalidValue;
     const Options opt = options();
     LowParams prm;
-    cudaError_t e = cached_map(MapKey{w8, K, (long long)G * N, K, 0}, &prm.wmap);
+    cudaError_t e = weight_map(w8, (long long)G * N, K, &prm.wmap);
     if (e != cudaSuccess) return e;
-    e = cached_map(MapKey{x, (long long)G * K, M, ldx, 1}, &prm.xmap);
-    if (e != cudaSuccess) return e;
+    prm.x = static_cast<const uint16_t *>(x);
+    prm.ldx = ldx;
     prm.ex = ex;
     prm.y = static_cast<uint16_t *>(y);
     prm.partials = partials;
@@ -746,9 +661,8 @@ cudaError_t launch_lowm(const StreamPlan &pl, const void *x, long long ldx, cons
     prm.status = status_word();
     if (!prm.status) return cudaErrorInvalidSymbol;
 
-    const size_t smem = (size_t)kRingBytes + 1024;
+    const size_t smem = (size_t)kSmemBytes;
     static int configured[64] = {0};
-    static int cap[64] = {0};
     int dev = 0;
     e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -760,20 +674,11 @@ cudaError_t launch_lowm(const StreamPlan &pl, const void *x, long long ldx, cons
         e = cudaFuncSetAttribute(lowm_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
-        int sms = 0;
-        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        // Persistent grid: two blocks an SM, the most that fit (shared memory, registers
-        // under the launch bounds, and two blocks of 256 TMEM columns fill tensor memory).
-        // The occupancy query is not used: it reports one block for this kernel although
-        // two are resident at once.  If fewer fit, the blocks simply run in turn.
-        __atomic_store_n(&cap[dev], sms * (512 / kTmemCols), __ATOMIC_RELEASE);
         __atomic_store_n(&configured[dev], 1, __ATOMIC_RELEASE);
     }
     cudaLaunchConfig_t cfg = {};
-    int gx = pl.grid_x;
-    if (pl.mode == kStreamInCta) gx = std::min(gx, __atomic_load_n(&cap[dev], __ATOMIC_ACQUIRE));
-    cfg.gridDim = dim3((unsigned)gx, (unsigned)G, 1);
+    // one group a block: the grid is the plan's (blocks beyond two an SM run in turn)
+    cfg.gridDim = dim3((unsigned)pl.grid_x, (unsigned)G, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
