@@ -46,12 +46,13 @@ struct GemmPlan {
 };
 
 // Weight-streaming kernel (bsf8_stream.cu): warp tasks of 16 rows x a column range.
-enum StreamMode { kStreamInCta = 0, kStreamCluster = 1, kStreamPartials = 2 };
+enum StreamMode { kStreamInCta = 0, kStreamCluster = 1, kStreamPartials = 2, kStreamGroup = 3 };
 
 struct StreamPlan {
     int S, chunk_cols, kt, tps;  // splits, columns per split, per task, tasks per split
     int nt8, m_chunks;           // token tiles of 8 per pass, passes over the tokens
     int mode, spc, cluster, spl, cps, grid_x;
+    int tpc;  // group mode (decode-ahead kernel): tasks of each slab a block holds
 };
 
 StreamPlan plan_stream(int M, int N, int K, int G, int S, bool partials);

@@ -52,11 +52,16 @@ constexpr int kKS = 128;           // columns per step
 constexpr int kSlotBytes = 2048;   // a 16 x 128 weight box, or an 8 x 128 bf16 x tile
 constexpr int kPre = 4;            // steps per task, all rebuilt ahead into tensor memory
 constexpr int kMaxKt = kPre * kKS; // task columns
+constexpr int kRegionBytes = kPre * kSlotBytes;  // a warp's slots
 constexpr int kTmemCols = 256;     // per block: 128 columns for each of two warps a quarter
+constexpr int kLowTasksPerBlock = 2;  // group mode: tasks of a slab a block holds (see plan_lowm)
 // Shared-memory request: 8 warps x 4 slots, padded so that a third block never fits an SM
 // (its tensor-memory allocation would wait for one of the other two to finish).
-constexpr int kSmemBytes = 80 * 1024;
-static_assert(kWarps * kPre * kSlotBytes + 1024 <= kSmemBytes, "slots fit the request");
+constexpr int kRingBytes = kWarps * kPre * kSlotBytes;  // the warps' slots
+constexpr int kGatherTiles = 32;   // group mode: [16 rows][8 tokens] fp32 partial tiles a
+                                   // block can receive for the slabs it reduces
+constexpr int kSmemBytes = 84 * 1024;
+static_assert(kRingBytes + kGatherTiles * 512 + 1024 <= kSmemBytes, "slots fit the request");
 static_assert(3 * (kSmemBytes + 1024) > 228 * 1024, "at most two blocks an SM");
 static_assert(2 * (kSmemBytes + 1024 + 6 * 1024) <= 228 * 1024, "two blocks fit an SM");
 
@@ -68,7 +73,7 @@ struct LowParams {
     uint16_t *y;
     float *partials;
     int M, N, K, G, S;
-    int chunk_cols, kt, tps, spc, cluster, spl, cps, mode;
+    int chunk_cols, kt, tps, spc, cluster, spl, cps, mode, tpc;
     unsigned long long timeout_ns;
     int skip_loads;
     int *status;
@@ -193,30 +198,22 @@ struct Task {
 
 __device__ __forceinline__ Task task_of(const LowParams &p, int w) {
     Task t;
-    const int nslabs = p.N / 16;
     const int tslab = p.S * p.tps;
     t.ngroups = 1;
     t.slab_step = 0;
-    if (p.mode == kStreamCluster) {
-        t.slab0 = blockIdx.x / p.cluster;
-        const int tau = (blockIdx.x % p.cluster) * kWarps + w;
-        t.s = tau / p.tps;
-        t.u = tau % p.tps;
-        t.active = tau < tslab;
-    } else if (p.mode == kStreamPartials) {
+    if (p.mode == kStreamPartials) {
         t.slab0 = blockIdx.x / p.cps;
         t.s = (blockIdx.x % p.cps) * p.spl + w / p.tps;
         t.u = w % p.tps;
         t.active = w < p.spl * p.tps && t.s < p.S;
-    } else {
-        const int groups_total = (nslabs + p.spc - 1) / p.spc;
-        t.ngroups = (int)blockIdx.x < groups_total
-                        ? (groups_total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-        t.slab0 = blockIdx.x * p.spc + w / tslab;
-        t.slab_step = gridDim.x * p.spc;
-        t.s = (w % tslab) / p.tps;
-        t.u = (w % tslab) % p.tps;
-        t.active = w < p.spc * tslab;
+    } else {  // group mode: a cluster of p.cluster blocks holds spc slabs x all their tasks
+        const int spc = kWarps / p.tpc;
+        const int rank = blockIdx.x % p.cluster;
+        t.slab0 = (blockIdx.x / p.cluster) * spc + w / p.tpc;
+        const int tau = rank * p.tpc + w % p.tpc;
+        t.s = tau / p.tps;
+        t.u = tau % p.tps;
+        t.active = tau < tslab;
     }
     t.k0 = t.k1 = 0;
     if (t.active) {
@@ -319,72 +316,29 @@ __device__ __forceinline__ void mma_step(const uint32_t (&a)[32], const uint4 (&
     }
 }
 
-// End of a group.  red[w] holds warp w's task partial [16 rows][8 tokens]; sums them in
-// the fixed order (tasks of a split in task order, splits in split order) and stores y,
-// or stores the per-split partials.  Stores are skipped when the block met an error.
-__device__ __forceinline__ void group_epilogue(const LowParams &p, float (*red)[16][8],
-                                               const volatile int *err, int g, int gslab) {
-    const int nslabs = p.N / 16, tslab = p.S * p.tps;
+__device__ __forceinline__ void st_cluster_v2f32(uint32_t addr, float a, float b) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
+
+// Partials mode: red[w] holds warp w's task partial [16 rows][8 tokens]; the block stores
+// its splits' fp32 partials (tasks of a split summed in task order).  Stores are skipped
+// when the block met an error.
+__device__ __forceinline__ void partials_epilogue(const LowParams &p, float (*red)[16][8],
+                                                  const volatile int *err, int g) {
     const int mrows = min(8, p.M);
-    const int tid = threadIdx.x;
-    if (p.mode == kStreamCluster) {
-        cluster_sync();
-        if (!*err) {
-            const int total = 16 * mrows;
-            const int c = blockIdx.x % p.cluster;
-            const int per = (total + p.cluster - 1) / p.cluster;
-            const int lo = c * per, hi = min(total, lo + per);
-            for (int i = lo + tid; i < hi; i += kThreads) {
-                const int m = i / 16, row = i - m * 16;
-                float y = 0.0f;
-                for (int ss = 0; ss < p.S; ++ss) {
-                    float ps = 0.0f;
-                    for (int uu = 0; uu < p.tps; ++uu) {
-                        const int tau = ss * p.tps + uu;
-                        const float v = ld_cluster_f32(
-                            map_to_rank(&red[tau % kWarps][row][m], (uint32_t)(tau / kWarps)));
-                        ps = uu == 0 ? v : ps + v;
-                    }
-                    y = ss == 0 ? ps : y + ps;
-                }
-                p.y[((size_t)m * p.G + g) * p.N + gslab * 16 + row] = f32_to_bf16_rn(y);
-            }
-        }
-        cluster_sync();  // keep this block's shared memory alive until the others are done
-        return;
-    }
     __syncthreads();
-    if (!*err) {
-        if (p.mode == kStreamInCta) {
-            const int per_slab = 16 * mrows;
-            for (int i = tid; i < p.spc * per_slab; i += kThreads) {
-                const int sl = i / per_slab, rem = i - sl * per_slab;
-                const int m = rem / 16, row = rem - m * 16;
-                const int sb = gslab + sl;
-                if (sb >= nslabs) continue;
-                const int w0 = sl * tslab;
-                float y = 0.0f;
-                for (int ss = 0; ss < p.S; ++ss) {
-                    float ps = red[w0 + ss * p.tps][row][m];
-                    for (int uu = 1; uu < p.tps; ++uu) ps = ps + red[w0 + ss * p.tps + uu][row][m];
-                    y = ss == 0 ? ps : y + ps;
-                }
-                p.y[((size_t)m * p.G + g) * p.N + sb * 16 + row] = f32_to_bf16_rn(y);
-            }
-        } else {
-            const int per_split = 16 * mrows;
-            for (int i = tid; i < p.spl * per_split; i += kThreads) {
-                const int ls = i / per_split, rem = i - ls * per_split;
-                const int m = rem / 16, row = rem - m * 16;
-                const int ss = (blockIdx.x % p.cps) * p.spl + ls;
-                if (ss >= p.S) continue;
-                float ps = red[ls * p.tps][row][m];
-                for (int uu = 1; uu < p.tps; ++uu) ps = ps + red[ls * p.tps + uu][row][m];
-                p.partials[(((size_t)ss * p.M + m) * p.G + g) * p.N + gslab * 16 + row] = ps;
-            }
-        }
+    if (*err) return;
+    const int slab = blockIdx.x / p.cps;
+    const int per_split = 16 * mrows;
+    for (int i = threadIdx.x; i < p.spl * per_split; i += kThreads) {
+        const int ls = i / per_split, rem = i - ls * per_split;
+        const int m = rem / 16, row = rem - m * 16;
+        const int ss = (blockIdx.x % p.cps) * p.spl + ls;
+        if (ss >= p.S) continue;
+        float ps = red[ls * p.tps][row][m];
+        for (int uu = 1; uu < p.tps; ++uu) ps = ps + red[ls * p.tps + uu][row][m];
+        p.partials[(((size_t)ss * p.M + m) * p.G + g) * p.N + slab * 16 + row] = ps;
     }
-    __syncthreads();  // red is rewritten by the next group
 }
 
 }  // namespace
@@ -405,6 +359,7 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
     extern __shared__ uint8_t dyn_smem[];
     // the swizzled boxes need 1024-byte alignment
     uint8_t *ring = dyn_smem + ((1024u - (smem_u32(dyn_smem) & 1023u)) & 1023u);
+    float *const gather = reinterpret_cast<float *>(ring + kRingBytes);  // group mode tiles
     __shared__ __align__(16) float red[kWarps][16][8];
     __shared__ __align__(8) uint64_t wbar[kWarps];
     __shared__ uint32_t s_tmem;
@@ -417,7 +372,11 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
     const int nslabs = p.N / 16;
     const int nst = p.kt / kKS;  // steps of a task (<= kPre)
     const Task me = task_of(p, warp);
-    uint8_t *const region = ring + warp * (kPre * kSlotBytes);
+    uint8_t *const region = ring + warp * kRegionBytes;
+    // warps that share a task (column range) share its x tiles, kept in the region of the
+    // first of them (warp w % tpc); each copies a part
+    const int xl = warp % p.tpc, xj = warp / p.tpc, xn = kWarps / p.tpc;
+    uint8_t *const xregion = ring + xl * kRegionBytes;
     // every block holds exactly one group (the grid is the plan's, not capped)
     const int slab = me.slab0;
     const bool slab_ok = me.active && me.ngroups > 0 && slab < nslabs;
@@ -453,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
     // change before the wait; a prefetch only moves lines into L2, where the producer's
     // writes land as well, and x is read after the wait from L2 (cp.async.cg), so the
     // copies see the producer's values.  Where x is already in L2 this costs nothing.
-    if (slab_ok && lane < p.M && lane < 8 && me.k1 > me.k0)
+    if (xj == 0 && lane < p.M && lane < 8 && me.k1 > me.k0)
         prefetch_l2(p.x + (size_t)lane * p.ldx + (size_t)g * p.K + me.k0,
                     (uint32_t)((me.k1 - me.k0) * 2));
     // exponent bytes of the task: lane l holds block k0/32 + l of the slab's row block
@@ -489,28 +448,27 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
         tmem_st32(tbase + 32u * t, a);
     }
     tmem_wait_st();
-    __syncwarp();
+    __syncthreads();  // every warp's weight boxes are rebuilt: the regions may take x
 
     // ---- the dependency wait: x (and y) belong to the kernels before this one
     pdl_wait();
 
-    // ---- x tiles of the task's steps into the slots (16-byte copies, rows >= M as zeros)
+    // ---- x tiles of the task's steps (16-byte copies, rows >= M as zeros), in the layout of
+    //      a 128-byte-swizzled 8 x 64 box pair per step
     {
-        const int unit = lane & 15;  // 16-byte unit of a 256-byte tile row
         const long long gk = (long long)p.G * p.K;
-        for (int t = 0; t < nst; ++t) {
+        const bool task_ok = me.k1 > me.k0;
+        for (int c = xj * 32 + lane; c < nst * 128; c += xn * 32) {
+            const int t = c >> 7, row = (c >> 4) & 7, unit = c & 15;
             const int col = me.k0 + t * kKS + unit * 8;  // first of the copy's 8 columns
-            uint8_t *tile = region + t * kSlotBytes + (unit >> 3) * 1024;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int row = (lane >> 4) + 2 * i;
-                const bool in = slab_ok && row < p.M && (long long)g * p.K + col < gk;
-                const uint16_t *src = p.x + (in ? (size_t)row * p.ldx + (size_t)g * p.K + col : 0);
-                cp_async_16_zfill(tile + row * 128 + (((unit & 7) ^ row) << 4), src, in ? 16u : 0u);
-            }
+            const bool in = task_ok && row < p.M && (long long)g * p.K + col < gk;
+            const uint16_t *src = p.x + (in ? (size_t)row * p.ldx + (size_t)g * p.K + col : 0);
+            cp_async_16_zfill(xregion + t * kSlotBytes + (unit >> 3) * 1024 + row * 128 +
+                                  (((unit & 7) ^ row) << 4),
+                              src, in ? 16u : 0u);
         }
         cp_async_wait_all();
-        __syncwarp();
+        __syncthreads();
     }
 
     // ---- MMAs: fragments back from tensor memory, x from the slots
@@ -526,12 +484,12 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
         const bool boxed = slab_ok && col < me.k1;
         const bool mine = boxed && col + q * 32 < me.k1;
         uint4 xv[4];
-        load_xfrag(region + t * kSlotBytes, r, q, mine, xv);
+        load_xfrag(xregion + t * kSlotBytes, r, q, mine, xv);
         tmem_wait_ld();
         if (!err && boxed) mma_step(a, xv, acc);
     }
 
-    // ---- the group's fixed-order reduction and store
+    // ---- the fixed-order reduction and store
     {
         uint32_t fa = nan_code_seen(mxa) ? 1u : 0u, fb = nan_code_seen(mxb) ? 1u : 0u;
         fa |= __shfl_xor_sync(0xFFFFFFFFu, fa, 1);
@@ -545,10 +503,58 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
             v[c] = acc[0][c] + acc[1][c];
             if ((c < 2 && fa) || (c >= 2 && fb)) v[c] = qnan;
         }
-        *reinterpret_cast<float2 *>(&red[warp][r][2 * q]) = make_float2(v[0], v[1]);
-        *reinterpret_cast<float2 *>(&red[warp][r + 8][2 * q]) = make_float2(v[2], v[3]);
-        const int gslab = p.mode == kStreamInCta ? (int)blockIdx.x * p.spc : me.slab0;
-        group_epilogue(p, red, &s_err, g, gslab);
+        if (p.mode == kStreamPartials) {
+            *reinterpret_cast<float2 *>(&red[warp][r][2 * q]) = make_float2(v[0], v[1]);
+            *reinterpret_cast<float2 *>(&red[warp][r + 8][2 * q]) = make_float2(v[2], v[3]);
+            partials_epilogue(p, red, &s_err, g);
+        } else {
+            // Group mode: every warp pushes its partial tile to the block of the cluster that
+            // reduces its slab (slab sl of the cluster's spc goes to rank sl % C, local tile
+            // index sl / C), then each block folds its slabs' tiles in the fixed order.
+            const int C = p.cluster, spc = kWarps / p.tpc, tslab = p.S * p.tps;
+            const int rank = blockIdx.x % C;
+            const int sl = warp / p.tpc;
+            const int rr = sl % C, li = sl / C;
+            const int tau = rank * p.tpc + warp % p.tpc;
+            if (me.active) {
+                float *tile = gather + (size_t)(li * tslab + tau) * 128;
+                float *d0 = tile + r * 8 + 2 * q, *d1 = tile + (r + 8) * 8 + 2 * q;
+                if (C == 1) {
+                    *reinterpret_cast<float2 *>(d0) = make_float2(v[0], v[1]);
+                    *reinterpret_cast<float2 *>(d1) = make_float2(v[2], v[3]);
+                    if (err) s_err = 1;
+                } else {
+                    st_cluster_v2f32(map_to_rank(d0, (uint32_t)rr), v[0], v[1]);
+                    st_cluster_v2f32(map_to_rank(d1, (uint32_t)rr), v[2], v[3]);
+                    if (err && lane == 0) {  // the reducer must not store a sum with garbage in it
+                        const uint32_t ea = map_to_rank((const void *)&s_err, (uint32_t)rr);
+                        asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(ea), "r"(1u) : "memory");
+                    }
+                }
+            }
+            if (C > 1)
+                cluster_sync();
+            else
+                __syncthreads();
+            if (!s_err) {
+                const int nslabs = p.N / 16, mrows = min(8, p.M), per_slab = 16 * mrows;
+                const int nmine = (spc - rank + C - 1) / C;  // slabs rank, rank + C, ...
+                for (int i = threadIdx.x; i < nmine * per_slab; i += kThreads) {
+                    const int lj = i / per_slab, rem = i - lj * per_slab;
+                    const int m = rem / 16, row = rem - m * 16;
+                    const int slab = (blockIdx.x / C) * spc + lj * C + rank;
+                    if (slab >= nslabs) continue;
+                    const float *tiles = gather + (size_t)lj * tslab * 128 + row * 8 + m;
+                    float y = 0.0f;
+                    for (int ss = 0; ss < p.S; ++ss) {
+                        float ps = tiles[(ss * p.tps) * 128];
+                        for (int uu = 1; uu < p.tps; ++uu) ps = ps + tiles[(ss * p.tps + uu) * 128];
+                        y = ss == 0 ? ps : y + ps;
+                    }
+                    p.y[((size_t)m * p.G + g) * p.N + slab * 16 + row] = f32_to_bf16_rn(y);
+                }
+            }
+        }
     }
 
     // After an error, let the weight boxes this warp issued land before the block exits.
@@ -627,7 +633,31 @@ cudaError_t weight_map(const uint8_t *w8, long long rows, int K, CUtensorMap *ou
 }  // namespace
 
 StreamPlan plan_lowm(int M, int N, int K, int G, int S, bool partials) {
-    return plan_stream_ks(M, N, K, G, S, partials, kKS, 1, kMaxKt);
+    StreamPlan pl = plan_stream_ks(M, N, K, G, S, partials, kKS, 1, kMaxKt);
+    if (pl.mode == kStreamPartials) {
+        pl.tpc = kWarps;
+        return pl;
+    }
+    // Group mode.  A block holds tpc tasks of each of 8 / tpc slabs (the slabs' warps share
+    // the tasks' x tiles) and a cluster of ceil(tslab / tpc) blocks holds all of the slabs'
+    // tasks.  Fewer tasks a block means less x to fetch after the wait per block, but a
+    // larger cluster; kLowTasksPerBlock is the balance, raised until the cluster fits 8.
+    const int tslab = S * pl.tps;
+    int tpc = kLowTasksPerBlock;
+    while (tpc < kWarps && (tslab + tpc - 1) / tpc > kMaxClusterSplits) tpc *= 2;
+    while (tpc > 1 && tpc / 2 >= tslab) tpc /= 2;  // no more than the slab has
+    const int spc = kWarps / tpc, cluster = (tslab + tpc - 1) / tpc;
+    if ((spc + cluster - 1) / cluster * tslab > kGatherTiles) {  // too many tiles to gather
+        StreamPlan pp = plan_stream_ks(M, N, K, G, S, true, kKS, 1, kMaxKt);
+        pp.tpc = kWarps;
+        return pp;
+    }
+    pl.tpc = tpc;
+    pl.spc = spc;
+    pl.cluster = cluster;
+    pl.mode = kStreamGroup;
+    pl.grid_x = (N / 16 + pl.spc - 1) / pl.spc * pl.cluster;
+    return pl;
 }
 
 cudaError_t launch_lowm(const StreamPlan &pl, const void *x, long long ldx, const uint8_t *w8,
@@ -656,6 +686,7 @@ cudaError_t launch_lowm(const StreamPlan &pl, const void *x, long long ldx, cons
     prm.spl = pl.spl;
     prm.cps = pl.cps;
     prm.mode = pl.mode;
+    prm.tpc = pl.tpc;
     prm.timeout_ns = opt.timeout_ns;
     prm.skip_loads = opt.skip_loads;
     prm.status = status_word();
@@ -684,7 +715,7 @@ cudaError_t launch_lowm(const StreamPlan &pl, const void *x, long long ldx, cons
     cfg.stream = stream;
     cudaLaunchAttribute attrs[2];
     int na = 0;
-    if (pl.mode == kStreamCluster) {
+    if (pl.mode == kStreamGroup && pl.cluster > 1) {
         attrs[na].id = cudaLaunchAttributeClusterDimension;
         attrs[na].val.clusterDim.x = (unsigned)pl.cluster;
         attrs[na].val.clusterDim.y = 1;
