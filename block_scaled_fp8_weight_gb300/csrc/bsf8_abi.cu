@@ -87,7 +87,27 @@ constexpr size_t kMaxSmem = 227 * 1024;
 // 8 token rows and at most two blocks an SM.  Larger calls stream (the cp.async kernel
 // sustains more bandwidth once the rebuild can no longer run ahead).  TMA coordinates are
 // 32-bit, so the TMA kernels need G*N < 2^31.
-enum MainKernel { kKernelStream = 0, kKernelTma = 1, kKernelLowM = 2 };
+enum MainKernel { kKernelStream = 0, kKernelTma = 1, kKernelLowM = 2, kKernelUmma = 3 };
+
+// Above this many token rows the tensor-core kernel (tcgen05) runs: its MMAs are cheap
+// there, while the mma.sync kernels become bound by their MMA issue.  Measured on a GB300:
+// mid-row wo_a (G = 4, 1024 x 4096) at M = 64 takes 14 us against 35 us, at M = 192
+// 23 us against 92 us; at M = 16 the streaming kernel is ahead (9 us against 14 us).
+constexpr int kUmmaMinRows = 24;
+
+// The split count when the caller leaves it to the library (split_k = 0).
+inline int call_auto_split(int M, int N, int K, int G) {
+    if (M > kUmmaMinRows && (long long)G * N < (1LL << 31)) {
+        int sms = 0;
+        int dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0) {
+            const int S = umma_auto_split(M, N, K, G, sms);
+            if (plan_umma(M, N, K, G, S, false).ok) return S;
+        }
+    }
+    return auto_split(M, N, K, G);
+}
 
 inline int sm_count() {
     static int count[64] = {0};
@@ -105,28 +125,50 @@ inline MainKernel main_kernel(int M, int N, int K, int G, int S, bool partials) 
         case 2: return kKernelStream;
         case 3: if (M <= 16) return kKernelTma; break;
         case 4: if (M <= 8) return kKernelLowM; break;
+        case 5: if (plan_umma(M, N, K, G, S, partials).ok) return kKernelUmma; break;
         default: break;
     }
+    if (M > kUmmaMinRows) return plan_umma(M, N, K, G, S, partials).ok ? kKernelUmma : kKernelStream;
     if (M > 8) return kKernelStream;
     const StreamPlan pl = plan_lowm(M, N, K, G, S, partials);
     return (long long)pl.grid_x * G <= 2LL * sm_count() ? kKernelLowM : kKernelStream;
 }
 
-inline StreamPlan main_plan(int M, int N, int K, int G, int S, bool partials) {
-    switch (main_kernel(M, N, K, G, S, partials)) {
-        case kKernelLowM: return plan_lowm(M, N, K, G, S, partials);
-        case kKernelTma: return plan_tma(M, N, K, G, S, partials);
-        default: return plan_stream(M, N, K, G, S, partials);
+// How one call runs: the kernel, its plan, and whether it writes fp32 partials (then the
+// fixed-order reduce follows, or the caller asked for the partials).
+struct Call {
+    MainKernel kernel;
+    StreamPlan sp;
+    UmmaPlan up;
+    bool partials_out;
+};
+
+inline Call plan_call(int M, int N, int K, int G, int S, bool partials) {
+    Call c{};
+    c.kernel = main_kernel(M, N, K, G, S, partials);
+    switch (c.kernel) {
+        case kKernelUmma:
+            c.up = plan_umma(M, N, K, G, S, partials);
+            c.partials_out = c.up.partials;
+            return c;
+        case kKernelLowM: c.sp = plan_lowm(M, N, K, G, S, partials); break;
+        case kKernelTma: c.sp = plan_tma(M, N, K, G, S, partials); break;
+        default: c.sp = plan_stream(M, N, K, G, S, partials); break;
     }
+    c.partials_out = c.sp.mode == kStreamPartials;
+    return c;
 }
 
-inline cudaError_t main_launch(const StreamPlan &pl, const void *x, long long ldx, const uint8_t *w8,
+inline cudaError_t launch_call(const Call &c, const void *x, long long ldx, const uint8_t *w8,
                                const uint8_t *ex, void *y, float *P, int M, int N, int K, int G,
-                               cudaStream_t s, int S, bool partials) {
-    switch (main_kernel(M, N, K, G, S, partials)) {
-        case kKernelLowM: return launch_lowm(pl, x, ldx, w8, ex, y, P, M, N, K, G, s);
-        case kKernelTma: return launch_tma(pl, x, ldx, w8, ex, y, P, M, N, K, G, s);
-        default: return launch_stream(pl, x, ldx, w8, ex, y, P, M, N, K, G, s);
+                               cudaStream_t s) {
+    // the output the plan writes must be there (fp32 partials, or y)
+    if (c.partials_out ? P == nullptr : y == nullptr) return cudaErrorInvalidValue;
+    switch (c.kernel) {
+        case kKernelUmma: return launch_umma(c.up, x, ldx, w8, ex, y, P, M, N, K, G, s);
+        case kKernelLowM: return launch_lowm(c.sp, x, ldx, w8, ex, y, P, M, N, K, G, s);
+        case kKernelTma: return launch_tma(c.sp, x, ldx, w8, ex, y, P, M, N, K, G, s);
+        default: return launch_stream(c.sp, x, ldx, w8, ex, y, P, M, N, K, G, s);
     }
 }
 
@@ -175,13 +217,13 @@ int bsf8_gemm_auto_split(int M, int N, int K, int G) {
     int st = check_gnk(G, N, K);
     if (st) return -st;
     if (M < 1 || M > BSF8_MAX_M) return -BSF8_ERR_SHAPE;
-    return auto_split(M, N, K, G);
+    return call_auto_split(M, N, K, G);
 }
 
 size_t bsf8_gemm_workspace_bytes(int M, int N, int K, int G, int split_k) {
     if (check_gnk(G, N, K) || M < 1 || M > BSF8_MAX_M || split_k < 0 || split_k > K / 32) return 0;
-    const int S = split_k == 0 ? auto_split(M, N, K, G) : split_k;
-    if (main_plan(M, N, K, G, S, false).mode != kStreamPartials) return 0;
+    const int S = split_k == 0 ? call_auto_split(M, N, K, G) : split_k;
+    if (!plan_call(M, N, K, G, S, false).partials_out) return 0;
     return (size_t)S * M * G * N * sizeof(float);
 }
 
@@ -190,17 +232,16 @@ int bsf8_gemm(const void *x, const uint8_t *w8, const uint8_t *exp, void *y, int
               bsf8_stream_t stream) {
     int st = check_gemm_args(x, w8, exp, y, M, N, K, G, split_k, ldx);
     if (st) return st;
-    const int S = split_k == 0 ? auto_split(M, N, K, G) : split_k;
+    const int S = split_k == 0 ? call_auto_split(M, N, K, G) : split_k;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (options().gemm_path != 1 || S > kMaxClusterSplits) {
-        const StreamPlan pl = main_plan(M, N, K, G, S, false);
-        if (pl.mode != kStreamPartials)
-            return from_cuda(main_launch(pl, x, ldx, w8, exp, y, nullptr, M, N, K, G, s, S, false));
+        const Call c = plan_call(M, N, K, G, S, false);
+        if (!c.partials_out) return from_cuda(launch_call(c, x, ldx, w8, exp, y, nullptr, M, N, K, G, s));
         const size_t need = (size_t)S * M * G * N * sizeof(float);
         if (!workspace || workspace_bytes < need) return BSF8_ERR_WORKSPACE;
         if (!aligned16(workspace)) return BSF8_ERR_ALIGN;
         float *P = static_cast<float *>(workspace);
-        st = from_cuda(main_launch(pl, x, ldx, w8, exp, nullptr, P, M, N, K, G, s, S, false));
+        st = from_cuda(launch_call(c, x, ldx, w8, exp, nullptr, P, M, N, K, G, s));
         if (st) return st;
         return from_cuda(launch_splitk_reduce(P, y, S, (long long)M * G * N, s));
     }
@@ -220,8 +261,8 @@ int bsf8_gemm_partials(const void *x, const uint8_t *w8, const uint8_t *exp, flo
     if (!aligned16(partials)) return BSF8_ERR_ALIGN;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (options().gemm_path != 1) {
-        const StreamPlan pl = main_plan(M, N, K, G, split_k, true);
-        return from_cuda(main_launch(pl, x, ldx, w8, exp, nullptr, partials, M, N, K, G, s, split_k, true));
+        const Call c = plan_call(M, N, K, G, split_k, true);
+        return from_cuda(launch_call(c, x, ldx, w8, exp, nullptr, partials, M, N, K, G, s));
     }
     const GemmPlan pl = plan_gemm(M, N, K, G, split_k, kModePartials);
     if (pl.smem_bytes > kMaxSmem) return BSF8_ERR_SHAPE;
@@ -280,7 +321,7 @@ int bsf8_set_option(int option, int64_t value) {
         case BSF8_OPT_WAIT_TIMEOUT_NS: g_opt_timeout_ns.store((long long)value); return BSF8_OK;
         case BSF8_OPT_DEBUG_SKIP_LOADS: g_opt_skip_loads.store(value ? 1 : 0); return BSF8_OK;
         case BSF8_OPT_GEMM_PATH:
-            if (value > 4) return BSF8_ERR_VALUE;
+            if (value > 5) return BSF8_ERR_VALUE;
             g_opt_gemm_path.store((int)value);
             return BSF8_OK;
         default: return BSF8_ERR_VALUE;

@@ -13,7 +13,8 @@ struct Options {
     int pdl;
     unsigned long long timeout_ns;
     int skip_loads;
-    int gemm_path;  // 0: by shape; 1: TMA-ring; 2: streaming; 3: TMA-fed; 4: decode-ahead
+    int gemm_path;  // 0: by shape; 1: TMA-ring; 2: streaming; 3: TMA-fed; 4: decode-ahead;
+                    // 5: tensor-core
 };
 Options options();
 
@@ -76,6 +77,18 @@ cudaError_t launch_tma(const StreamPlan &plan, const void *x, long long ldx, con
 cudaError_t launch_stream(const StreamPlan &plan, const void *x, long long ldx, const uint8_t *w8,
                           const uint8_t *ex, void *y, float *partials, int M, int N, int K, int G,
                           cudaStream_t stream);
+
+// Tensor-core kernel (bsf8_umma.cu): 128-row blocks, one split a block; up to 192 token
+// rows.  With more than one split it writes fp32 partials (the fixed-order reduce follows).
+struct UmmaPlan {
+    int S, chunk_cols, ntok, row_blocks, grid_x;
+    bool partials, tmem_ok, ok;  // ok: the kernel can run this call (else another kernel)
+};
+UmmaPlan plan_umma(int M, int N, int K, int G, int S, bool partials);
+int umma_auto_split(int M, int N, int K, int G, int sms);
+cudaError_t launch_umma(const UmmaPlan &plan, const void *x, long long ldx, const uint8_t *w8,
+                        const uint8_t *ex, void *y, float *partials, int M, int N, int K, int G,
+                        cudaStream_t stream);
 
 int auto_split(int M, int N, int K, int G);
 GemmPlan plan_gemm(int M, int N, int K, int G, int S, int mode);

@@ -212,7 +212,8 @@ enum {
                                    /* kernel beyond; 1: the shared-memory TMA-ring     */
                                    /* kernel (split_k <= 8); 2: the streaming kernel;  */
                                    /* 3: the TMA-fed kernel (M <= 16); 4: the          */
-                                   /* decode-ahead kernel (M <= 8).  A forced kernel   */
+                                   /* decode-ahead kernel (M <= 8); 5: the tensor-core */
+                                   /* (tcgen05) kernel (M <= 192).  A forced kernel    */
                                    /* that does not apply to a call falls back to 0.   */
 };
 /* Errors: BSF8_ERR_VALUE for an unknown option or a negative value. */

@@ -29,8 +29,9 @@ def run(x_d, w8_d, ex_d, S, **kw):
 
 # ---------------------------------------------------------------- exact cases
 
+@pytest.mark.parametrize("path", [0, 5])
 @pytest.mark.parametrize("M", [8, 32])
-def test_one_hot_every_code_and_exponent(bsf8_lib, M):
+def test_one_hot_every_code_and_exponent(bsf8_lib, M, path):
     """x rows are unit vectors: every output is one exact product, so the GEMM must
     reproduce the oracle bit for bit (zeros by value, NaN as NaN) for all 256 codes x
     256 exponent bytes -- this checks the in-register rebuild, including subnormal
@@ -38,13 +39,17 @@ def test_one_hot_every_code_and_exponent(bsf8_lib, M):
     N, K = 256 * 32, 32
     w8 = (np.arange(N * K) % 256).astype(np.uint8).reshape(1, N, K)
     ex = np.arange(256, dtype=np.uint8).reshape(1, 256, 1)
-    for k0 in range(0, K, M):
-        x = np.zeros((M, K), dtype=np.uint16)
-        for m in range(M):
-            x[m, (k0 + m) % K] = 0x3F80
-        y = bf16_bits(bsf8.gemm(to_dev_bf16(x), to_dev_u8(w8), to_dev_u8(ex), split_k=1))
-        ref = oracle.gemm(x, w8, ex)
-        assert np.all(same_bits(y, ref, zero_sign=True))
+    bsf8.set_option(bsf8.OPT_GEMM_PATH, path)
+    try:
+        for k0 in range(0, K, M):
+            x = np.zeros((M, K), dtype=np.uint16)
+            for m in range(M):
+                x[m, (k0 + m) % K] = 0x3F80
+            y = bf16_bits(bsf8.gemm(to_dev_bf16(x), to_dev_u8(w8), to_dev_u8(ex), split_k=1))
+            ref = oracle.gemm(x, w8, ex)
+            assert np.all(same_bits(y, ref, zero_sign=True))
+    finally:
+        bsf8.set_option(bsf8.OPT_GEMM_PATH, 0)
 
 
 def test_integer_data_is_exact(bsf8_lib):
@@ -259,13 +264,14 @@ def test_tma_ring_path_matches_oracle_and_its_two_pass(bsf8_lib, wk, M, S):
     assert_gemm_close(y[rows], oracle.gemm(x[rows], w8, ex))
 
 
-@pytest.mark.parametrize("path", [2, 3, 4])
+@pytest.mark.parametrize("path", [2, 3, 4, 5])
 @pytest.mark.parametrize("wk,M,S", [(wl.WO_A, 6, 8), (wl.TINY, 4, 1), (wl.DOWN_PROJ, 6, 4),
-                                    (wl.TINY, 3, 16), (wl.WO_A, 1, 80)])
+                                    (wl.TINY, 3, 16), (wl.WO_A, 1, 80), (wl.DOWN_PROJ, 6, 7)])
 def test_forced_kernels_match_oracle_and_each_other(bsf8_lib, path, wk, M, S):
     """Each kernel forced through BSF8_OPT_GEMM_PATH (2: streaming, 3: TMA-fed, 4:
-    decode-ahead) in its in-block, cluster (S = 16) and partials (S = 80) modes: within
-    the tolerance of the oracle, bitwise equal to its own two-pass form, and bitwise
+    decode-ahead, 5: tensor-core) in its in-block, cluster (S = 16) and partials (S = 80)
+    modes, and with splits that end inside a 64-column step (K = 576, S = 7): within the
+    tolerance of the oracle, bitwise equal to its own two-pass form, and bitwise
     reproducible."""
     w8, ex = wk.weights()
     x = wk.x(M=M)
@@ -281,3 +287,27 @@ def test_forced_kernels_match_oracle_and_each_other(bsf8_lib, path, wk, M, S):
     assert np.array_equal(y, y2)
     assert np.array_equal(y, two)
     assert_gemm_close(y, oracle.gemm(x, w8, ex))
+
+
+@pytest.mark.parametrize("M", [9, 16, 32, 64, 96, 128, 192])
+@pytest.mark.parametrize("S", [1, 2, 4])
+def test_tensor_core_kernel_mid_rows(bsf8_lib, M, S):
+    """The tensor-core kernel on the mid-row workload (G = 4 groups of W[1024, 4096]):
+    sampled token rows within the oracle's tolerance, the fused call bitwise equal to its
+    two-pass form, and run-to-run bitwise reproducible."""
+    wk = wl.MID
+    w8, ex = wk.weights()
+    x = wk.x(M=M)
+    w8_d, ex_d, x_d = dev(w8, ex, x)
+    bsf8.set_option(bsf8.OPT_GEMM_PATH, 5)
+    try:
+        y = run(x_d, w8_d, ex_d, S)
+        y2 = run(x_d, w8_d, ex_d, S)
+        two = bf16_bits(bsf8.splitk_reduce(bsf8.gemm_partials(x_d, w8_d, ex_d, S)))
+        assert bsf8.device_status() == 0
+    finally:
+        bsf8.set_option(bsf8.OPT_GEMM_PATH, 0)
+    assert np.array_equal(y, y2)
+    assert np.array_equal(y, two)
+    rows = sorted({0, M // 2, M - 1})
+    assert_gemm_close(y[rows], oracle.gemm(x[rows], w8, ex))
