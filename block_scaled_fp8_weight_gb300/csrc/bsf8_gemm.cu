@@ -310,11 +310,14 @@ __global__ void __launch_bounds__(kGemmThreads) gemm_kernel(const __grid_constan
 
 // -------------------------------------------------------- fixed-order split-K sum
 //   y[i] = bf16( ((P[0][i] + P[1][i]) + P[2][i]) + ... ),  fp32, left to right.
+// Writes nothing while the device status word holds a timeout: the partials a first pass
+// left after giving up a wait are incomplete (the status stays until the host reads it).
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restrict__ P,
                                                             uint16_t *__restrict__ y, int S,
-                                                            long long count) {
+                                                            long long count, const int *status) {
     pdl_trigger();
     pdl_wait();
+    if (*(const volatile int *)status == kStatusTimeout) return;
     const long long stride = (long long)gridDim.x * blockDim.x;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += stride) {
         float v = __ldcg(P + i);
@@ -439,7 +442,9 @@ cudaError_t launch_splitk_reduce(const float *P, void *y, int S, long long count
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = opt.pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, P, static_cast<uint16_t *>(y), S, count);
+    const int *status = status_word();
+    if (!status) return cudaErrorInvalidSymbol;
+    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, P, static_cast<uint16_t *>(y), S, count, status);
 }
 
 }  // namespace bsf8

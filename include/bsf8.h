@@ -107,9 +107,11 @@ int bsf8_dequant(const uint8_t *w8, const uint8_t *exp, void *out, int G, int N,
  *   M         1 .. BSF8_MAX_M
  *   split_k   0 = the library chooses (bsf8_gemm_auto_split), else 1 .. K/32
  *   workspace device scratch of at least bsf8_gemm_workspace_bytes(...) bytes, or
- *             NULL when that is 0 (it is 0 unless a slab of 16 rows needs more than 64
- *             column tasks, e.g. split_k > 64): fp32 partials between the two passes.
- *             No zeroing is needed; it must not be shared by calls that can overlap.
+ *             NULL when that is 0: fp32 partials between the two passes, which the call
+ *             runs when its kernel writes partials (the tensor-core kernel, M > 24, with
+ *             more than one split; the other kernels when a slab of 16 rows needs more
+ *             than 64 column tasks, e.g. split_k > 64).  No zeroing is needed; it must not
+ *             be shared by calls that can overlap.
  * The partials of a 16-row slab are summed inside one thread block, or across a cluster
  * of up to 8 blocks through distributed shared memory, in the same fixed order as
  * bsf8_gemm_partials followed by bsf8_splitk_reduce, which give the same bits.
@@ -144,6 +146,9 @@ int bsf8_gemm_partials(const void *x, const uint8_t *w8, const uint8_t *exp,
  * in fp32, left to right.
  *   partials device, fp32 [S][count]
  *   y        device, out, bf16 [count]
+ * While the device status word holds BSF8_ERR_TIMEOUT (a first pass gave up a wait and
+ * left incomplete partials) the kernel writes nothing; bsf8_device_status reads and
+ * clears the word.
  * Errors: BSF8_ERR_NULL, BSF8_ERR_SHAPE, BSF8_ERR_CUDA. */
 int bsf8_splitk_reduce(const float *partials, void *y, int S, int64_t count,
                        bsf8_stream_t stream);

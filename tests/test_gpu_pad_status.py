@@ -59,12 +59,13 @@ def test_down_proj_padding_leaves_output_bitwise_unchanged(bsf8_lib):
     assert np.array_equal(y6, y7)
 
 
-@pytest.mark.parametrize("path,M", [(0, 4), (3, 12), (1, 4)])
+@pytest.mark.parametrize("path,M", [(0, 4), (3, 12), (1, 4), (0, 40)])
 def test_timeout_is_reported_without_hanging(bsf8_lib, path, M):
     """With the test-only option that suppresses the weight loads, the mbarrier waits of
-    the decode-ahead GEMM (path 0: the default for this call), the TMA-fed GEMM (path 3)
-    and the TMA-ring GEMM (path 1) run out after the shortened bound; the kernel records
-    BSF8_ERR_TIMEOUT, writes nothing and returns.  Normal calls work again afterwards."""
+    the decode-ahead GEMM (path 0 at M = 4), the TMA-fed GEMM (path 3), the TMA-ring GEMM
+    (path 1) and the tensor-core GEMM (path 0 at M = 40) run out after the shortened
+    bound; the kernel records BSF8_ERR_TIMEOUT, writes nothing and returns.  Normal calls
+    work again afterwards."""
     w8, ex = wl.TINY.weights()
     x = wl.TINY.x(M=M)
     w8_d, ex_d, x_d = to_dev_u8(w8), to_dev_u8(ex), to_dev_bf16(x)
