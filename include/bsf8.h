@@ -112,14 +112,16 @@ int bsf8_dequant(const uint8_t *w8, const uint8_t *exp, void *out, int G, int N,
  *             more than one split; the other kernels when a slab of 16 rows needs more
  *             than 64 column tasks, e.g. split_k > 64).  No zeroing is needed; it must not
  *             be shared by calls that can overlap.
- * The partials of a 16-row slab are summed inside one thread block, or across a cluster
- * of up to 8 blocks through distributed shared memory, in the same fixed order as
- * bsf8_gemm_partials followed by bsf8_splitk_reduce, which give the same bits.
+ * The splits are summed inside one thread block, across a cluster of up to 8 blocks
+ * through distributed shared memory, or by the fixed-order reduce of a second pass, always
+ * in the same fixed order as bsf8_gemm_partials followed by bsf8_splitk_reduce, which give
+ * the same bits.
  * The twin is treated as a static parameter: with programmatic dependent launch
  * (BSF8_OPT_PDL) the kernel starts reading w8 and exp while the kernel before it on the
  * stream may still run, if that kernel allows it (the library's kernels that write a
  * twin -- make_twin, pad_k -- never do; a caller's kernel that writes w8 or exp must not
- * trigger its dependents early).  x is read and y written only after that kernel ends.
+ * trigger its dependents early).  x is read and y written only after that kernel ends
+ * (before, x's rows may be prefetched into L2, which reads nothing into the call).
  * Errors: BSF8_ERR_NULL, BSF8_ERR_SHAPE, BSF8_ERR_ALIGN, BSF8_ERR_STRIDE,
  *         BSF8_ERR_WORKSPACE, BSF8_ERR_CUDA. */
 int bsf8_gemm(const void *x, const uint8_t *w8, const uint8_t *exp, void *y,
@@ -129,8 +131,10 @@ int bsf8_gemm(const void *x, const uint8_t *w8, const uint8_t *exp, void *y,
 /* Workspace bsf8_gemm needs for these sizes (0 for most shapes; see bsf8_gemm). */
 size_t bsf8_gemm_workspace_bytes(int M, int N, int K, int G, int split_k);
 
-/* The split count bsf8_gemm uses for split_k = 0 (host only; no GPU needed).  Returns
- * a value in 1 .. min(8, K/32), or a negative status for invalid sizes. */
+/* The split count bsf8_gemm uses for split_k = 0.  Returns a value in 1 .. K/32, or a
+ * negative status for invalid sizes.  For M <= 24 it depends on the sizes only (at most
+ * 8); for M > 24 (the tensor-core kernel) on the current device's SM count too, and with
+ * no device the M <= 24 rule applies. */
 int bsf8_gemm_auto_split(int M, int N, int K, int G);
 
 /* First pass alone: writes the fp32 partials P[S][M][G][N] (S = split_k >= 1, every
