@@ -54,7 +54,7 @@ constexpr int kPre = 4;            // steps per task, all rebuilt ahead into ten
 constexpr int kMaxKt = kPre * kKS; // task columns
 constexpr int kRegionBytes = kPre * kSlotBytes;  // a warp's slots
 constexpr int kTmemCols = 256;     // per block: 128 columns for each of two warps a quarter
-constexpr int kLowTasksPerBlock = 2;  // group mode: tasks of a slab a block holds (see plan_lowm)
+constexpr int kLowTasksPerBlock = 1;  // group mode: tasks of a slab a block holds (see plan_lowm)
 // Shared-memory request: 8 warps x 4 slots, padded so that a third block never fits an SM
 // (its tensor-memory allocation would wait for one of the other two to finish).
 constexpr int kRingBytes = kWarps * kPre * kSlotBytes;  // the warps' slots

@@ -45,11 +45,10 @@ constexpr int kHalf = 64;            // columns of one 128-byte swizzle atom of 
 constexpr int kCodesBytes = kRows * kKB;        // 16 KB of codes a step
 constexpr int kAHalfBytes = kRows * kHalf * 2;  // 16 KB: A tile of one atom column
 constexpr int kABytes = 2 * kAHalfBytes;        // 32 KB of bf16 a step
-constexpr int kDa = 2;                          // A ring depth
-constexpr int kDcMax = 8, kDxMax = 16;          // codes and x ring depths: set per call
-// Dynamic shared memory a block: the A ring, then the x and codes rings sized per call
-// (x tiles grow with the tokens: 2 .. 16 of them, up to 48 KB unless two need more; the
-// codes ring takes the rest, 2 .. 8 steps).
+constexpr int kDaMax = 3, kDcMax = 8, kDxMax = 12;  // ring depths, set per call
+// Dynamic shared memory a block: the A, x and codes rings, sized per call (x tiles grow
+// with the tokens): x 2 .. 12 tiles within 48 KB unless two need more, A 2 steps of
+// 32 KB, the codes ring the rest, 2 .. 8 steps.
 constexpr int kSmemU = 208 * 1024;
 constexpr int kRebuildWarps = 8;                // 16 weight rows each
 constexpr int kThreadsU = (2 + kRebuildWarps) * 32;  // warp 0 copies, warp 1 MMA, 2.. rebuild
@@ -71,7 +70,7 @@ struct UmmaParams {
     float *partials;
     int M, N, K, G, S, chunk_cols, ntok;
     int to_partials;  // 1: store fp32 partials P[s] (even with one split), 0: store y
-    int dx, dc;       // x and codes ring depths
+    int dx, dc, da;   // x, codes and A ring depths
     unsigned long long timeout_ns;
     int skip_loads;
     int *status;
@@ -188,10 +187,10 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64
 __global__ void __launch_bounds__(kThreadsU, 1) umma_kernel(const __grid_constant__ UmmaParams p) {
     extern __shared__ uint8_t dyn_smem[];
     uint8_t *const base = dyn_smem + ((1024u - (smem_u32(dyn_smem) & 1023u)) & 1023u);
-    uint8_t *const sA = base;                                   // kDa x 16 KB, 128B swizzle
-    uint8_t *const sX = sA + kDa * kABytes;                     // dx x ntok x 128 B
+    uint8_t *const sA = base;                                   // da x 32 KB, 128B swizzle
+    uint8_t *const sX = sA + p.da * kABytes;                    // dx x ntok x 256 B
     uint8_t *const sC = sX + p.dx * p.ntok * 256;                 // dc x 16 KB
-    __shared__ __align__(8) uint64_t full_c[kDcMax], empty_c[kDcMax], full_a[kDa], empty_a[kDa];
+    __shared__ __align__(8) uint64_t full_c[kDcMax], empty_c[kDcMax], full_a[kDaMax], empty_a[kDaMax];
     __shared__ __align__(8) uint64_t full_x[kDxMax], empty_x[kDxMax], d_full;
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
@@ -208,14 +207,14 @@ __global__ void __launch_bounds__(kThreadsU, 1) umma_kernel(const __grid_constan
     uint32_t tcols = 32;
     while ((int)tcols < max(1, nrun) * p.ntok) tcols *= 2;   // the plan keeps this <= 512
     const int xbytes = p.ntok * 256;  // a step's x tile: two 64-column atoms
-    const int kDx = p.dx, kDc = p.dc;  // ring depths of this call
+    const int kDx = p.dx, kDc = p.dc, kDa = p.da;  // ring depths of this call
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kDcMax; ++i) {
             mbar_init(&full_c[i], 1);
             mbar_init(&empty_c[i], kRebuildWarps);
         }
-        for (int i = 0; i < kDa; ++i) {
+        for (int i = 0; i < kDaMax; ++i) {
             mbar_init(&full_a[i], kRebuildWarps);
             mbar_init(&empty_a[i], 1);
         }
@@ -576,8 +575,11 @@ int umma_x_depth(const UmmaPlan &pl) {
     return std::max(2, std::min(kDxMax, (48 * 1024) / (pl.ntok * 256)));
 }
 
+// A third A slot measured slower (the codes ring loses a step); two it is.
+int umma_a_depth(const UmmaPlan &) { return 2; }
+
 int umma_codes_depth(const UmmaPlan &pl) {
-    const int left = kSmemU - 1024 - kDa * kABytes - umma_x_depth(pl) * pl.ntok * 256;
+    const int left = kSmemU - 1024 - umma_a_depth(pl) * kABytes - umma_x_depth(pl) * pl.ntok * 256;
     return std::min(kDcMax, left / kCodesBytes);
 }
 
@@ -606,6 +608,7 @@ cudaError_t launch_umma(const UmmaPlan &pl, const void *x, long long ldx, const 
     prm.to_partials = pl.partials ? 1 : 0;
     prm.dx = umma_x_depth(pl);
     prm.dc = umma_codes_depth(pl);
+    prm.da = umma_a_depth(pl);
     if (prm.dc < 2) return cudaErrorInvalidValue;
     prm.timeout_ns = opt.timeout_ns;
     prm.skip_loads = opt.skip_loads;
