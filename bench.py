@@ -62,6 +62,9 @@ def parse_args(argv=None):
     p.add_argument("--workload", choices=("wo_a", "down_proj", "mid", "gate_up", "head"),
                    default="wo_a", help="profiling mode only: which workload to run")
     p.add_argument("--m", type=int, default=None, help="profiling mode only: token rows")
+    p.add_argument("--suite", action="store_true",
+                   help="time every hot-path row (make_twin, dequant, pad-K, the GEMM at every "
+                        "config) and print one JSON line per row instead of the headline line")
     return p.parse_args(argv)
 
 
@@ -395,6 +398,134 @@ def time_e2e(layers, wk, steps, stream):
     return e0.elapsed_time(e1) / 1e3, h2d, d2h
 
 
+def run_suite(device, peak):
+    """Every hot-path row timed on the GPU: each call of a row in a CUDA graph over enough
+    distinct seeded copies that the inputs exceed the L2 (PDL on), reported as us/call and
+    as bytes moved per call (the row's algorithmic bytes) over time, against the HBM peak."""
+    import ctypes
+    import torch
+    import block_scaled_fp8_weight_gb300 as bsf8
+    from block_scaled_fp8_weight_gb300 import workloads as wl
+    lib = bsf8.load()
+    stream = torch.cuda.Stream(device=device)
+    out = []
+
+    def graph_time(calls, reps):
+        with torch.cuda.stream(stream):
+            for c in calls:
+                c()
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for c in calls:
+                    c()
+            for _ in range(3):
+                g.replay()
+            stream.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+            stream.synchronize()
+        if bsf8.device_status() != 0:
+            raise RuntimeError("a kernel reported a timeout")
+        return e0.elapsed_time(e1) * 1e-3 / (reps * len(calls))
+
+    def emit(row, config, t, nbytes, weight_bytes=None):
+        line = {"row": row, "config": config, "us_per_call": t * 1e6,
+                "GBps": nbytes / t / 1e9, "frac_of_hbm_peak": nbytes / t / 1e9 / peak,
+                "bytes_per_call": nbytes}
+        if weight_bytes is not None:
+            line["weight_stream_GBps"] = weight_bytes / t / 1e9
+            line["weight_frac"] = weight_bytes / t / 1e9 / peak
+        out.append(line)
+        print(json.dumps(line), flush=True)
+
+    sp = lambda: ctypes.c_void_p(stream.cuda_stream)
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr())
+    # make_twin and dequant on the wo_a shape, 43 copies (cold)
+    wk = wl.WO_A
+    G, N, K = wk.G, wk.N, wk.K
+    twins = [wk.weights(copy=c) for c in range(LAYERS)]
+    w8s = [torch.from_numpy(a).to(device) for a, _ in twins]
+    exs = [torch.from_numpy(b).to(device) for _, b in twins]
+    wbf = [bsf8.dequant(a, b) for a, b in zip(w8s, exs)]
+    o8 = [torch.empty_like(a) for a in w8s]
+    oe = [torch.empty_like(b) for b in exs]
+    ok = [torch.empty_like(b) for b in exs]
+    acc = torch.empty((LAYERS,), dtype=torch.int32, device=device)
+    calls = [lambda i=i: lib.bsf8_make_twin(ptr(wbf[i]), ptr(o8[i]), ptr(oe[i]), ptr(ok[i]),
+                                            ctypes.c_void_p(acc.data_ptr() + 4 * i), G, N, K, sp())
+             for i in range(LAYERS)]
+    t = graph_time(calls, 20)
+    emit("a1 make_twin", f"G={G} N={N} K={K} bf16 -> twin, {LAYERS} copies", t,
+         2 * G * N * K + G * N * K + 2 * G * (N // 32) * (K // 32))
+    outs = [torch.empty((G, N, K), dtype=torch.bfloat16, device=device) for _ in range(LAYERS)]
+    calls = [lambda i=i: lib.bsf8_dequant(ptr(w8s[i]), ptr(exs[i]), ptr(outs[i]), G, N, K, sp())
+             for i in range(LAYERS)]
+    t = graph_time(calls, 20)
+    emit("a2' dequant", f"G={G} N={N} K={K} twin -> bf16, {LAYERS} copies", t,
+         G * N * K + G * (N // 32) * (K // 32) + 2 * G * N * K)
+    del wbf, o8, oe, ok, outs
+    # pad-K on the down_proj twin (576 -> 640), 43 copies
+    dk = wl.DOWN_PROJ
+    dt = [dk.weights(copy=c) for c in range(LAYERS)]
+    dw = [torch.from_numpy(a).to(device) for a, _ in dt]
+    de = [torch.from_numpy(b).to(device) for _, b in dt]
+    Kp = 640
+    pw = [torch.empty((1, dk.N, Kp), dtype=torch.uint8, device=device) for _ in range(LAYERS)]
+    pe = [torch.empty((1, dk.N // 32, Kp // 32), dtype=torch.uint8, device=device) for _ in range(LAYERS)]
+    calls = [lambda i=i: lib.bsf8_pad_k(ptr(dw[i]), ptr(de[i]), ptr(pw[i]), ptr(pe[i]), 1, dk.N, dk.K,
+                                        Kp, 127, sp()) for i in range(LAYERS)]
+    t = graph_time(calls, 50)
+    emit("a7 pad_k", f"N={dk.N} K={dk.K} -> {Kp}, {LAYERS} copies", t,
+         dk.N * dk.K + dk.N * Kp + (dk.N // 32) * (dk.K // 32 + Kp // 32))
+    del w8s, exs, twins
+
+    cache = {}
+
+    def weights_of(wk, copies):
+        key = (wk.name, wk.K, copies)
+        if key not in cache:
+            cache.clear()
+            cache[key] = [tuple(torch.from_numpy(a).to(device) for a in wk.weights(copy=c))
+                          for c in range(copies)]
+        return cache[key]
+
+    def gemm_row(name, wk, M, S, copies):
+        layers = []
+        for c, (w8, ex) in enumerate(weights_of(wk, copies)):
+            x = wk.x(copy=c, M=M)
+            layers.append((w8, ex, torch.from_numpy(x.view("int16")).view(torch.bfloat16).to(device)))
+        ys = [torch.empty((M, wk.G, wk.N), dtype=torch.bfloat16, device=device) for _ in layers]
+        need = bsf8.workspace_bytes(M, wk.N, wk.K, wk.G, S)
+        wss = [torch.empty(max(16, need), dtype=torch.uint8, device=device) for _ in layers] if need else [None] * copies
+        calls = [lambda l=l, y=y, w=w: bsf8.gemm(l[2], l[0], l[1], split_k=S, out=y, workspace=w)
+                 for l, y, w in zip(layers, ys, wss)]
+        t = graph_time(calls, min(200, max(3, int(2e-3 / max(1e-6, wk.weight_bytes / 4e12)))))
+        xy = M * wk.G * wk.K * 2 + M * wk.G * wk.N * 2
+        emit(name, f"G={wk.G} N={wk.N} K={wk.K} M={M} split_k={S or 'auto'}, {copies} copies", t,
+             wk.weight_bytes + xy, wk.weight_bytes)
+
+    gemm_row("a3-a6 gemm tiny", wl.TINY, 4, 1, LAYERS)
+    gemm_row("a3-a6 gemm tiny", wl.TINY, 4, 4, LAYERS)
+    for M in (2, 4, 6, 8):
+        gemm_row("a3-a6 gemm wo_a", wl.WO_A, M, 8, LAYERS)
+    gemm_row("a3-a6 gemm down_proj K=576", wl.DOWN_PROJ, 6, 0, LAYERS)
+    import dataclasses
+    gemm_row("a3-a6 gemm down_proj K=640", dataclasses.replace(wl.DOWN_PROJ, K=640), 6, 0, LAYERS)
+    for M in (9, 16, 32, 64, 96, 128, 192):
+        for S in (1, 2, 4, 8):
+            gemm_row("a3-a6 gemm mid", wl.MID, M, S, LAYERS)
+    for M in (1, 2, 6, 16, 64, 128):
+        gemm_row("a3-a6 gemm gate_up", wl.GATE_UP, M, 0, LAYERS)
+    for M in (1, 2, 6, 16, 64, 128):
+        gemm_row("a3-a6 gemm head", wl.HEAD, M, 0, 3)
+    return out
+
+
 def main(argv=None):
     args = parse_args(argv)
     world, rank, local = dist_env()
@@ -415,6 +546,9 @@ def main(argv=None):
     dist = init_dist(world, True)
     bsf8_build.build()
     bsf8.load()
+    if args.suite:
+        run_suite(device, measured_peaks()[0])
+        return 0
     wk = workload()
     if args.profile_calls:
         from block_scaled_fp8_weight_gb300 import workloads as wl

@@ -129,12 +129,14 @@ def test_workspace_and_auto_split(lib):
     assert lib.bsf8_gemm_workspace_bytes(6, 1024, 4096, 2, 65) == 65 * 6 * 2 * 1024 * 4
     # very long splits need more than 8 tasks each: K = 65536 in 16 splits
     assert lib.bsf8_gemm_workspace_bytes(6, 64, 65536, 1, 16) == 16 * 6 * 64 * 4
-    # wo_a (16 tiles x 2 groups): 8 splits, as on the page (grid (16, G, 8))
-    assert lib.bsf8_gemm_auto_split(6, 1024, 4096, 2) == 8
-    # the head-like shape has enough tiles for one split
+    # up to 8 token rows: one split (the kernels cut it into column tasks themselves; for
+    # wo_a one split sums its 8 tasks in the same left-to-right order as the page's 8 splits)
+    assert lib.bsf8_gemm_auto_split(6, 1024, 4096, 2) == 1
     assert lib.bsf8_gemm_auto_split(6, 32768, 5120, 1) == 1
+    # 9..24 rows: mid-row wo_a (16 tiles x 2 groups) gets 8 splits, as on the page
+    assert lib.bsf8_gemm_auto_split(12, 1024, 4096, 2) == 8
     # never more splits than 32-column blocks
-    assert lib.bsf8_gemm_auto_split(1, 32, 64, 1) == 2
+    assert lib.bsf8_gemm_auto_split(12, 32, 64, 1) == 2
     assert lib.bsf8_gemm_auto_split(0, 1024, 4096, 2) == -SHAPE
     for M in (1, 2, 8, 9, 64, 192):
         s = lib.bsf8_gemm_auto_split(M, 5120, 576, 1)
