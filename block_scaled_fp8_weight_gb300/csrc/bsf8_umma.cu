@@ -184,7 +184,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64
 
 }  // namespace
 
-__global__ void __launch_bounds__(kThreadsU, 1) umma_kernel(const __grid_constant__ UmmaParams p) {
+__global__ void __launch_bounds__(kThreadsU, 2) umma_kernel(const __grid_constant__ UmmaParams p) {
     extern __shared__ uint8_t dyn_smem[];
     uint8_t *const base = dyn_smem + ((1024u - (smem_u32(dyn_smem) & 1023u)) & 1023u);
     uint8_t *const sA = base;                                   // da x 32 KB, 128B swizzle
@@ -571,15 +571,26 @@ int umma_auto_split(int M, int N, int K, int G, int sms) {
     return S;
 }
 
+// Up to 16 tokens two blocks share an SM (rings within ~106 KB, accumulators within half of
+// tensor memory): more blocks in flight to cover the per-step latency of one block's
+// pipeline, and no second wave on large N.
+bool umma_two_per_sm(const UmmaPlan &pl) {
+    const int nrun = ((pl.chunk_cols + kKB - 1) / kKB + kChunkSteps - 1) / kChunkSteps;
+    return pl.ntok <= 16 && nrun * pl.ntok <= kTmemMax / 2;
+}
+
+int umma_smem_budget(const UmmaPlan &pl) { return umma_two_per_sm(pl) ? 106 * 1024 : kSmemU; }
+
 int umma_x_depth(const UmmaPlan &pl) {
-    return std::max(2, std::min(kDxMax, (48 * 1024) / (pl.ntok * 256)));
+    const int bytes = umma_two_per_sm(pl) ? 8 * 1024 : 48 * 1024;
+    return std::max(2, std::min(kDxMax, bytes / (pl.ntok * 256)));
 }
 
 // A third A slot measured slower (the codes ring loses a step); two it is.
 int umma_a_depth(const UmmaPlan &) { return 2; }
 
 int umma_codes_depth(const UmmaPlan &pl) {
-    const int left = kSmemU - 1024 - umma_a_depth(pl) * kABytes - umma_x_depth(pl) * pl.ntok * 256;
+    const int left = umma_smem_budget(pl) - 1024 - umma_a_depth(pl) * kABytes - umma_x_depth(pl) * pl.ntok * 256;
     return std::min(kDcMax, left / kCodesBytes);
 }
 
@@ -614,14 +625,14 @@ cudaError_t launch_umma(const UmmaPlan &pl, const void *x, long long ldx, const 
     prm.skip_loads = opt.skip_loads;
     prm.status = status_word();
     if (!prm.status) return cudaErrorInvalidSymbol;
-    const size_t smem = (size_t)kSmemU;
+    const size_t smem = (size_t)umma_smem_budget(pl);
     static int configured[64] = {0};
     int dev = 0;
     e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!__atomic_load_n(&configured[dev], __ATOMIC_ACQUIRE)) {
-        e = cudaFuncSetAttribute(umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = cudaFuncSetAttribute(umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemU);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(umma_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);

@@ -216,14 +216,17 @@ enum {
     BSF8_OPT_DEBUG_SKIP_LOADS = 3, /* test only: the TMA-ring GEMM issues no weight    */
                                    /* loads, so its waits run out (BSF8_ERR_TIMEOUT)   */
     BSF8_OPT_GEMM_PATH = 4         /* 0 (default): the kernel chosen by shape -- the    */
-                                   /* decode-ahead kernel up to 8 token rows, the      */
-                                   /* TMA-fed kernel up to 16, the cp.async streaming  */
-                                   /* kernel beyond; 1: the shared-memory TMA-ring     */
-                                   /* kernel (split_k <= 8); 2: the streaming kernel;  */
-                                   /* 3: the TMA-fed kernel (M <= 16); 4: the          */
-                                   /* decode-ahead kernel (M <= 8); 5: the tensor-core */
-                                   /* (tcgen05) kernel (M <= 192).  A forced kernel    */
-                                   /* that does not apply to a call falls back to 0.   */
+                                   /* decode-ahead kernel up to 8 token rows (when its */
+                                   /* grid fits two blocks an SM), the tensor-core     */
+                                   /* kernel for 9..16 rows at split_k 1 over at least */
+                                   /* one 128-row block per SM and beyond 24 rows, the */
+                                   /* cp.async streaming kernel otherwise; 1: the      */
+                                   /* shared-memory TMA-ring kernel (split_k <= 8);    */
+                                   /* 2: the streaming kernel; 3: the TMA-fed kernel   */
+                                   /* (M <= 16); 4: the decode-ahead kernel (M <= 8);  */
+                                   /* 5: the tensor-core (tcgen05) kernel (M <= 192).  */
+                                   /* A forced kernel that does not apply to a call    */
+                                   /* falls back to 0.                                 */
 };
 /* Errors: BSF8_ERR_VALUE for an unknown option or a negative value. */
 int bsf8_set_option(int option, int64_t value);

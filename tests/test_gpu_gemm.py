@@ -117,7 +117,7 @@ def test_gate_up_sweep(bsf8_lib, M):
     check(wl.GATE_UP, M, 0, rows=rows)
 
 
-@pytest.mark.parametrize("M", [1, 6, 128])
+@pytest.mark.parametrize("M", [1, 6, 12, 16, 128])
 def test_head_sweep_sampled(bsf8_lib, M):
     rows = sorted({0, M - 1})
     check(wl.HEAD, M, 0, rows=rows, n_range=(32768 - 2048, 32768))
