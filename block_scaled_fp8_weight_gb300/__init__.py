@@ -40,6 +40,8 @@ class Bsf8Error(RuntimeError):
         self.status = status
         name = STATUS.get(status, str(status))
         msg = _lib.bsf8_strerror(status).decode() if _lib is not None else name
+        if _lib is not None and name in ("ERR_CUDA", "ERR_DEVICE"):
+            msg += f" (cudaError {_lib.bsf8_last_cuda_error()})"
         super().__init__(f"{where}: BSF8_{name}: {msg}")
 
 
@@ -63,6 +65,7 @@ def load(build_if_missing: bool = True):
         sig = {
             "bsf8_strerror": (ctypes.c_char_p, [I]),
             "bsf8_version": (I, []),
+            "bsf8_last_cuda_error": (I, []),
             "bsf8_make_twin": (I, [P, P, P, P, P, I, I, I, P]),
             "bsf8_dequant": (I, [P, P, P, I, I, I, P]),
             "bsf8_gemm": (I, [P, P, P, P, I, I, I, I, I, I64, P, SZ, P]),

@@ -52,8 +52,11 @@ namespace {
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+std::atomic<int> g_last_cuda_error{0};
+
 inline int from_cuda(cudaError_t e) {
     if (e == cudaSuccess) return BSF8_OK;
+    g_last_cuda_error.store((int)e, std::memory_order_relaxed);
     if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction ||
         e == cudaErrorUnsupportedPtxVersion)
         return BSF8_ERR_DEVICE;
@@ -87,7 +90,7 @@ constexpr size_t kMaxSmem = 227 * 1024;
 // 8 token rows and at most two blocks an SM.  Larger calls stream (the cp.async kernel
 // sustains more bandwidth once the rebuild can no longer run ahead).  TMA coordinates are
 // 32-bit, so the TMA kernels need G*N < 2^31.
-enum MainKernel { kKernelStream = 0, kKernelTma = 1, kKernelLowM = 2, kKernelUmma = 3 };
+enum MainKernel { kKernelStream = 0, kKernelTma = 1, kKernelLowM = 2, kKernelUmma = 3, kKernelWide = 4 };
 
 // Above this many token rows the tensor-core kernel (tcgen05) runs: its MMAs are cheap
 // there, while the mma.sync kernels become bound by their MMA issue.  Measured on a GB300:
@@ -130,6 +133,7 @@ inline MainKernel main_kernel(int M, int N, int K, int G, int S, bool partials) 
         case 3: if (M <= 16) return kKernelTma; break;
         case 4: if (M <= 8) return kKernelLowM; break;
         case 5: if (plan_umma(M, N, K, G, S, partials).ok) return kKernelUmma; break;
+        case 6: if (plan_wide(M, N, K, G, S, partials).ok) return kKernelWide; break;
         default: break;
     }
     if (M > kUmmaMinRows) return plan_umma(M, N, K, G, S, partials).ok ? kKernelUmma : kKernelStream;
@@ -143,7 +147,10 @@ inline MainKernel main_kernel(int M, int N, int K, int G, int S, bool partials) 
         return kKernelStream;
     }
     const StreamPlan pl = plan_lowm(M, N, K, G, S, partials);
-    return (long long)pl.grid_x * G <= 2LL * sm_count() ? kKernelLowM : kKernelStream;
+    if ((long long)pl.grid_x * G <= 2LL * sm_count()) return kKernelLowM;
+    // more weight than the decode-ahead grid holds: the wide-weight kernel streams it
+    // (one split: more would add the reduce pass the streaming kernel does without)
+    return S == 1 && plan_wide(M, N, K, G, S, partials).ok ? kKernelWide : kKernelStream;
 }
 
 // How one call runs: the kernel, its plan, and whether it writes fp32 partials (then the
@@ -152,6 +159,7 @@ struct Call {
     MainKernel kernel;
     StreamPlan sp;
     UmmaPlan up;
+    WidePlan wp;
     bool partials_out;
 };
 
@@ -162,6 +170,10 @@ inline Call plan_call(int M, int N, int K, int G, int S, bool partials) {
         case kKernelUmma:
             c.up = plan_umma(M, N, K, G, S, partials);
             c.partials_out = c.up.partials;
+            return c;
+        case kKernelWide:
+            c.wp = plan_wide(M, N, K, G, S, partials);
+            c.partials_out = c.wp.partials;
             return c;
         case kKernelLowM: c.sp = plan_lowm(M, N, K, G, S, partials); break;
         case kKernelTma: c.sp = plan_tma(M, N, K, G, S, partials); break;
@@ -178,6 +190,7 @@ inline cudaError_t launch_call(const Call &c, const void *x, long long ldx, cons
     if (c.partials_out ? P == nullptr : y == nullptr) return cudaErrorInvalidValue;
     switch (c.kernel) {
         case kKernelUmma: return launch_umma(c.up, x, ldx, w8, ex, y, P, M, N, K, G, s);
+        case kKernelWide: return launch_wide(c.wp, x, ldx, w8, ex, y, P, M, N, K, G, s);
         case kKernelLowM: return launch_lowm(c.sp, x, ldx, w8, ex, y, P, M, N, K, G, s);
         case kKernelTma: return launch_tma(c.sp, x, ldx, w8, ex, y, P, M, N, K, G, s);
         default: return launch_stream(c.sp, x, ldx, w8, ex, y, P, M, N, K, G, s);
@@ -205,6 +218,8 @@ const char *bsf8_strerror(int status) {
 }
 
 int bsf8_version(void) { return 100; }
+
+int bsf8_last_cuda_error(void) { return g_last_cuda_error.load(std::memory_order_relaxed); }
 
 int bsf8_make_twin(const void *w, uint8_t *w8, uint8_t *exp, uint8_t *block_ok, int32_t *accepted,
                    int G, int N, int K, bsf8_stream_t stream) {
@@ -333,7 +348,7 @@ int bsf8_set_option(int option, int64_t value) {
         case BSF8_OPT_WAIT_TIMEOUT_NS: g_opt_timeout_ns.store((long long)value); return BSF8_OK;
         case BSF8_OPT_DEBUG_SKIP_LOADS: g_opt_skip_loads.store(value ? 1 : 0); return BSF8_OK;
         case BSF8_OPT_GEMM_PATH:
-            if (value > 5) return BSF8_ERR_VALUE;
+            if (value > 6) return BSF8_ERR_VALUE;
             g_opt_gemm_path.store((int)value);
             return BSF8_OK;
         default: return BSF8_ERR_VALUE;

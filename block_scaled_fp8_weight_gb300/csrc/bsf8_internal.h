@@ -14,7 +14,7 @@ struct Options {
     unsigned long long timeout_ns;
     int skip_loads;
     int gemm_path;  // 0: by shape; 1: TMA-ring; 2: streaming; 3: TMA-fed; 4: decode-ahead;
-                    // 5: tensor-core
+                    // 5: tensor-core; 6: wide-weight
 };
 Options options();
 
@@ -87,6 +87,19 @@ struct UmmaPlan {
 UmmaPlan plan_umma(int M, int N, int K, int G, int S, bool partials);
 int umma_auto_split(int M, int N, int K, int G, int sms);
 cudaError_t launch_umma(const UmmaPlan &plan, const void *x, long long ldx, const uint8_t *w8,
+                        const uint8_t *ex, void *y, float *partials, int M, int N, int K, int G,
+                        cudaStream_t stream);
+
+// Wide-weight kernel (bsf8_wide.cu) for up to 8 token rows: tasks of 128 rows x one
+// split, one block an SM; codes widened to f16, x converted once a split into shared memory.
+// With more than one split it writes fp32 partials (the fixed-order reduce follows).
+struct WidePlan {
+    int S, chunk_cols, tasks, pitch, depth;
+    size_t smem;
+    bool partials, ok;  // ok: the kernel can run this call (else another kernel)
+};
+WidePlan plan_wide(int M, int N, int K, int G, int S, bool partials);
+cudaError_t launch_wide(const WidePlan &plan, const void *x, long long ldx, const uint8_t *w8,
                         const uint8_t *ex, void *y, float *partials, int M, int N, int K, int G,
                         cudaStream_t stream);
 

@@ -65,6 +65,11 @@ const char *bsf8_strerror(int status);
 /* Library version as major*10000 + minor*100 + patch. */
 int bsf8_version(void);
 
+/* The CUDA runtime error code (a cudaError_t value) behind the most recent
+ * BSF8_ERR_CUDA or BSF8_ERR_DEVICE returned by any call of this process, 0 if none
+ * has occurred.  Kept process-wide (not per thread); for diagnostics only. */
+int bsf8_last_cuda_error(void);
+
 /* --------------------------------------------------------------------- make_twin
  * "wo_a_w8.py", make_twin(): per 32x32 block of the bf16 weight w[G][N][K]
  *   amax = max |w| (raised to at least 2^-126),  e = ceil(log2(amax/448)) in [-127,127],
@@ -220,11 +225,16 @@ enum {
                                    /* grid fits two blocks an SM), the tensor-core     */
                                    /* kernel for 9..16 rows at split_k 1 over at least */
                                    /* one 128-row block per SM and beyond 24 rows, the */
-                                   /* cp.async streaming kernel otherwise; 1: the      */
-                                   /* shared-memory TMA-ring kernel (split_k <= 8);    */
-                                   /* 2: the streaming kernel; 3: the TMA-fed kernel   */
-                                   /* (M <= 16); 4: the decode-ahead kernel (M <= 8);  */
-                                   /* 5: the tensor-core (tcgen05) kernel (M <= 192).  */
+                                   /* wide-weight kernel up to 8 rows at split_k 1     */
+                                   /* where the decode-ahead grid does not fit, the    */
+                                   /* cp.async streaming                               */
+                                   /* kernel otherwise; 1: the shared-memory TMA-ring  */
+                                   /* kernel (split_k <= 8); 2: the streaming kernel;  */
+                                   /* 3: the TMA-fed kernel (M <= 16); 4: the decode-  */
+                                   /* ahead kernel (M <= 8); 5: the tensor-core        */
+                                   /* (tcgen05) kernel (M <= 192); 6: the wide-weight  */
+                                   /* kernel (M <= 8; K and the split's columns        */
+                                   /* multiples of 128, at most 6144 columns a split). */
                                    /* A forced kernel that does not apply to a call    */
                                    /* falls back to 0.                                 */
 };

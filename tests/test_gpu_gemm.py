@@ -29,7 +29,7 @@ def run(x_d, w8_d, ex_d, S, **kw):
 
 # ---------------------------------------------------------------- exact cases
 
-@pytest.mark.parametrize("path", [0, 5])
+@pytest.mark.parametrize("path", [0, 5, 6])
 @pytest.mark.parametrize("M", [8, 32])
 def test_one_hot_every_code_and_exponent(bsf8_lib, M, path):
     """x rows are unit vectors: every output is one exact product, so the GEMM must
@@ -264,12 +264,12 @@ def test_tma_ring_path_matches_oracle_and_its_two_pass(bsf8_lib, wk, M, S):
     assert_gemm_close(y[rows], oracle.gemm(x[rows], w8, ex))
 
 
-@pytest.mark.parametrize("path", [2, 3, 4, 5])
+@pytest.mark.parametrize("path", [2, 3, 4, 5, 6])
 @pytest.mark.parametrize("wk,M,S", [(wl.WO_A, 6, 8), (wl.TINY, 4, 1), (wl.DOWN_PROJ, 6, 4),
                                     (wl.TINY, 3, 16), (wl.WO_A, 1, 80), (wl.DOWN_PROJ, 6, 7)])
 def test_forced_kernels_match_oracle_and_each_other(bsf8_lib, path, wk, M, S):
     """Each kernel forced through BSF8_OPT_GEMM_PATH (2: streaming, 3: TMA-fed, 4:
-    decode-ahead, 5: tensor-core) in its in-block, cluster (S = 16) and partials (S = 80)
+    decode-ahead, 5: tensor-core, 6: wide-weight) in its in-block, cluster (S = 16) and partials (S = 80)
     modes, and with splits that end inside a 64-column step (K = 576, S = 7): within the
     tolerance of the oracle, bitwise equal to its own two-pass form, and bitwise
     reproducible."""
