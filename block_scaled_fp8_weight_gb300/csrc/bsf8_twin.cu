@@ -19,6 +19,23 @@ int grid_for(long long work, int threads) {
     return (int)std::max(1LL, std::min(b, 152LL * 16));
 }
 
+// Launches with programmatic dependent launch when enabled: a kernel may start while the
+// previous one in the stream finishes; each kernel here waits (griddepcontrol.wait) before
+// it touches memory, so only the launch overlaps.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), int grid, int block, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3((unsigned)block, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = options().pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ make_twin
@@ -35,7 +52,11 @@ int grid_for(long long work, int threads) {
 //  check:  the rebuild bf16(code * 2^e) -- the GEMM's own rebuild4 -- compared by value
 //          with w (so -0 == +0).
 
-__global__ void set_i32_kernel(int32_t *p, int32_t v) { *p = v; }
+__global__ void set_i32_kernel(int32_t *p, int32_t v) {
+    pdl_trigger();
+    pdl_wait();
+    *p = v;
+}
 
 __device__ __forceinline__ uint16_t cvt_e4m3x2(float hi, float lo) {
     uint16_t r;
@@ -56,6 +77,8 @@ __global__ void __launch_bounds__(256) make_twin_kernel(const uint16_t *__restri
                                                         uint8_t *__restrict__ ok,
                                                         int32_t *__restrict__ accepted, int G,
                                                         int N, int K) {
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int nb = N / 32, kb = K / 32;
     const long long nblocks = (long long)G * nb * kb;
@@ -130,12 +153,13 @@ __global__ void __launch_bounds__(256) make_twin_kernel(const uint16_t *__restri
 
 cudaError_t launch_make_twin(const void *w, uint8_t *w8, uint8_t *ex, uint8_t *ok,
                              int32_t *accepted, int G, int N, int K, cudaStream_t stream) {
-    set_i32_kernel<<<1, 1, 0, stream>>>(accepted, 1);
+    cudaError_t e = launch_pdl(set_i32_kernel, 1, 1, stream, accepted, 1);
+    if (e != cudaSuccess) return e;
     const long long nblocks = (long long)G * (N / 32) * (K / 32);
     if (nblocks > 0)
-        make_twin_kernel<<<grid_for(nblocks * 32, 256), 256, 0, stream>>>(
-            static_cast<const uint16_t *>(w), w8, ex, ok, accepted, G, N, K);
-    return cudaGetLastError();
+        e = launch_pdl(make_twin_kernel, grid_for(nblocks * 32, 256), 256, stream, static_cast<const uint16_t *>(w),
+                       w8, ex, ok, accepted, G, N, K);
+    return e;
 }
 
 // -------------------------------------------------------------------- dequant
@@ -145,6 +169,8 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict_
                                                       const uint8_t *__restrict__ ex,
                                                       uint16_t *__restrict__ out, int K,
                                                       long long chunks) {
+    pdl_trigger();
+    pdl_wait();
     const int kb = K / 32;
     const long long stride = (long long)gridDim.x * blockDim.x;
     for (long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x; c < chunks; c += stride) {
@@ -171,40 +197,44 @@ cudaError_t launch_dequant(const uint8_t *w8, const uint8_t *ex, void *out, int 
                            cudaStream_t stream) {
     const long long chunks = (long long)G * N * K / 16;
     if (chunks > 0)
-        dequant_kernel<<<grid_for(chunks, 256), 256, 0, stream>>>(w8, ex, static_cast<uint16_t *>(out),
-                                                                   K, chunks);
-    return cudaGetLastError();
+        return launch_pdl(dequant_kernel, grid_for(chunks, 256), 256, stream, w8, ex, static_cast<uint16_t *>(out),
+                          K, chunks);
+    return cudaSuccess;
 }
 
 // ---------------------------------------------------------------------- pad-K
-__global__ void __launch_bounds__(256) pad_w8_kernel(const uint8_t *__restrict__ w8,
-                                                     uint8_t *__restrict__ w8_out, int K, int Kp,
-                                                     long long chunks) {
-    const int cpr = Kp / 16;
+// One launch pads both arrays: threads 0 .. chunks-1 copy 16-byte pieces of the codes
+// (zeros past K), the threads after them the exponent bytes (pad_exp past K/32).
+__global__ void __launch_bounds__(256) pad_k_kernel(const uint8_t *__restrict__ w8,
+                                                    uint8_t *__restrict__ w8_out,
+                                                    const uint8_t *__restrict__ ex,
+                                                    uint8_t *__restrict__ ex_out, int K, int Kp,
+                                                    uint8_t pad_exp, long long chunks, long long n) {
+    pdl_trigger();
+    pdl_wait();
+    const int cpr = Kp / 16, kb = K / 32, kbp = Kp / 32;
     const long long stride = (long long)gridDim.x * blockDim.x;
-    for (long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x; c < chunks; c += stride) {
-        const long long row = c / cpr;
-        const int k = (int)(c - row * cpr) * 16;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (k < K) v = *reinterpret_cast<const uint4 *>(w8 + (size_t)row * K + k);
-        *reinterpret_cast<uint4 *>(w8_out + (size_t)row * Kp + k) = v;
-    }
-}
-
-__global__ void __launch_bounds__(256) pad_exp_kernel(const uint8_t *__restrict__ ex,
-                                                      uint8_t *__restrict__ ex_out, int kb,
-                                                      int kbp, uint8_t pad_exp, long long n) {
-    const long long stride = (long long)gridDim.x * blockDim.x;
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
-        const long long row = i / kbp;
-        const int j = (int)(i - row * kbp);
-        ex_out[i] = j < kb ? ex[(size_t)row * kb + j] : pad_exp;
+    for (long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x; c < chunks + n; c += stride) {
+        if (c < chunks) {
+            const long long row = c / cpr;
+            const int k = (int)(c - row * cpr) * 16;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (k < K) v = *reinterpret_cast<const uint4 *>(w8 + (size_t)row * K + k);
+            *reinterpret_cast<uint4 *>(w8_out + (size_t)row * Kp + k) = v;
+        } else {
+            const long long i = c - chunks;
+            const long long row = i / kbp;
+            const int j = (int)(i - row * kbp);
+            ex_out[i] = j < kb ? ex[(size_t)row * kb + j] : pad_exp;
+        }
     }
 }
 
 __global__ void __launch_bounds__(256) pad_x_kernel(const uint16_t *__restrict__ x, long long ldx,
                                                     uint16_t *__restrict__ x_out, int G, int K,
                                                     int Kp, long long chunks) {
+    pdl_trigger();
+    pdl_wait();
     const int cpg = Kp / 8;  // 16-byte chunks per group row
     const long long stride = (long long)gridDim.x * blockDim.x;
     for (long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x; c < chunks; c += stride) {
@@ -221,22 +251,20 @@ __global__ void __launch_bounds__(256) pad_x_kernel(const uint16_t *__restrict__
 cudaError_t launch_pad_k(const uint8_t *w8, const uint8_t *ex, uint8_t *w8_out, uint8_t *ex_out,
                          int G, int N, int K, int Kp, int pad_exp, cudaStream_t stream) {
     const long long chunks = (long long)G * N * (Kp / 16);
-    if (chunks > 0)
-        pad_w8_kernel<<<grid_for(chunks, 256), 256, 0, stream>>>(w8, w8_out, K, Kp, chunks);
     const long long n = (long long)G * (N / 32) * (Kp / 32);
-    if (n > 0)
-        pad_exp_kernel<<<grid_for(n, 256), 256, 0, stream>>>(ex, ex_out, K / 32, Kp / 32,
-                                                              (uint8_t)pad_exp, n);
-    return cudaGetLastError();
+    if (chunks + n > 0)
+        return launch_pdl(pad_k_kernel, grid_for(chunks + n, 256), 256, stream, w8, w8_out, ex, ex_out, K, Kp,
+                          (uint8_t)pad_exp, chunks, n);
+    return cudaSuccess;
 }
 
 cudaError_t launch_pad_x(const void *x, long long ldx, void *x_out, int M, int G, int K, int Kp,
                          cudaStream_t stream) {
     const long long chunks = (long long)M * G * (Kp / 8);
     if (chunks > 0)
-        pad_x_kernel<<<grid_for(chunks, 256), 256, 0, stream>>>(
-            static_cast<const uint16_t *>(x), ldx, static_cast<uint16_t *>(x_out), G, K, Kp, chunks);
-    return cudaGetLastError();
+        return launch_pdl(pad_x_kernel, grid_for(chunks, 256), 256, stream, static_cast<const uint16_t *>(x), ldx,
+                          static_cast<uint16_t *>(x_out), G, K, Kp, chunks);
+    return cudaSuccess;
 }
 
 }  // namespace bsf8
