@@ -59,8 +59,10 @@ def parse_args(argv=None):
     p.add_argument("--profile-calls", type=int, default=0,
                    help="profiling mode: run this many eager layer calls and exit (no JSON)")
     p.add_argument("--split-k", type=int, default=None, help="override the workload's split_k")
-    p.add_argument("--workload", choices=("wo_a", "down_proj", "mid", "gate_up", "head"),
-                   default="wo_a", help="profiling mode only: which workload to run")
+    p.add_argument("--workload", choices=("wo_a", "down_proj", "mid", "gate_up", "head",
+                                          "make_twin", "dequant", "pad_k"),
+                   default="wo_a", help="profiling mode only: which workload to run (a GEMM shape, "
+                                        "or make_twin / dequant on the wo_a shape, pad_k on down_proj)")
     p.add_argument("--m", type=int, default=None, help="profiling mode only: token rows")
     p.add_argument("--suite", action="store_true",
                    help="time every hot-path row (make_twin, dequant, pad-K, the GEMM at every "
@@ -398,6 +400,30 @@ def time_e2e(layers, wk, steps, stream):
     return e0.elapsed_time(e1) / 1e3, h2d, d2h
 
 
+def profile_load_time(which, calls, device):
+    """Profiling mode for the load-time rows: `calls` eager calls over distinct copies."""
+    import torch
+    import block_scaled_fp8_weight_gb300 as bsf8
+    from block_scaled_fp8_weight_gb300 import workloads as wl
+    wk = wl.DOWN_PROJ if which == "pad_k" else wl.WO_A
+    copies = min(calls, 8)
+    twins = [wk.weights(copy=c) for c in range(copies)]
+    w8s = [torch.from_numpy(a).to(device) for a, _ in twins]
+    exs = [torch.from_numpy(b).to(device) for _, b in twins]
+    wbf = [bsf8.dequant(a, b) for a, b in zip(w8s, exs)] if which == "make_twin" else None
+    torch.cuda.synchronize(device)
+    for i in range(calls):
+        c = i % copies
+        if which == "make_twin":
+            bsf8.make_twin(wbf[c])
+        elif which == "dequant":
+            bsf8.dequant(w8s[c], exs[c])
+        else:
+            bsf8.pad_k(w8s[c], exs[c], 640, pad_exp=127)
+    torch.cuda.synchronize(device)
+    return 0
+
+
 def run_suite(device, peak):
     """Every hot-path row timed on the GPU: each call of a row in a CUDA graph over enough
     distinct seeded copies that the inputs exceed the L2 (PDL on), reported as us/call and
@@ -550,6 +576,8 @@ def main(argv=None):
         run_suite(device, measured_peaks()[0])
         return 0
     wk = workload()
+    if args.profile_calls and args.workload in ("make_twin", "dequant", "pad_k"):
+        return profile_load_time(args.workload, args.profile_calls, device)
     if args.profile_calls:
         from block_scaled_fp8_weight_gb300 import workloads as wl
         wk = {"wo_a": wl.WO_A, "down_proj": wl.DOWN_PROJ, "mid": wl.MID, "gate_up": wl.GATE_UP,
