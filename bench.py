@@ -121,6 +121,15 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def measured_bf16_tflops():
+    """Dense bf16 tensor throughput to compare large-M GEMMs with (burst, measured)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"])
+    return 1900.0
+
+
 def kernel_hash():
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
@@ -549,6 +558,31 @@ def run_suite(device, peak):
         gemm_row("a3-a6 gemm gate_up", wl.GATE_UP, M, 0, LAYERS)
     for M in (1, 2, 6, 16, 64, 128):
         gemm_row("a3-a6 gemm head", wl.HEAD, M, 0, 3)
+
+    # Past 192 rows (prefill-sized calls, the pages' drop mode served from the twin): bound by
+    # the tensor cores, so reported against the measured dense bf16 peak too.  The calls of a
+    # row share one workspace: they run one after another on the stream.
+    bf16_peak = measured_bf16_tflops()
+    for wk, M, copies in ((wl.MID, 1024, 8), (wl.MID, 4096, 4), (wl.HEAD, 512, 2), (wl.HEAD, 2048, 2)):
+        layers = []
+        for c, (w8, ex) in enumerate(weights_of(wk, copies)):
+            x = wk.x(copy=c, M=M)
+            layers.append((w8, ex, torch.from_numpy(x.view("int16")).view(torch.bfloat16).to(device)))
+        ys = [torch.empty((M, wk.G, wk.N), dtype=torch.bfloat16, device=device) for _ in layers]
+        need = bsf8.workspace_bytes(M, wk.N, wk.K, wk.G, 0)
+        ws = torch.empty(max(16, need), dtype=torch.uint8, device=device)
+        calls = [lambda l=l, y=y: bsf8.gemm(l[2], l[0], l[1], split_k=0, out=y, workspace=ws)
+                 for l, y in zip(layers, ys)]
+        t = graph_time(calls, 5)
+        flops = 2.0 * M * wk.G * wk.N * wk.K
+        xy = M * wk.G * wk.K * 2 + M * wk.G * wk.N * 2
+        emit("f1 gemm large-M", f"G={wk.G} N={wk.N} K={wk.K} M={M} split_k=auto, {copies} copies", t,
+             wk.weight_bytes + xy, wk.weight_bytes)
+        out[-1]["TFLOPs"] = flops / t / 1e12
+        out[-1]["frac_of_bf16_peak"] = flops / t / 1e12 / bf16_peak
+        print(json.dumps({"row": "f1 gemm large-M", "M": M, "TFLOPs": out[-1]["TFLOPs"],
+                          "frac_of_bf16_peak": out[-1]["frac_of_bf16_peak"]}), flush=True)
+        del layers, ys, ws
     return out
 
 

@@ -26,7 +26,7 @@ __all__ = [
     "MAX_M", "STATUS",
 ]
 
-MAX_M = 192
+MAX_M = 16384
 OPT_PDL, OPT_WAIT_TIMEOUT_NS, OPT_DEBUG_SKIP_LOADS, OPT_GEMM_PATH = 1, 2, 3, 4
 STATUS = {0: "OK", 1: "ERR_SHAPE", 2: "ERR_ALIGN", 3: "ERR_STRIDE", 4: "ERR_WORKSPACE",
           5: "ERR_NULL", 6: "ERR_CUDA", 7: "ERR_TIMEOUT", 8: "ERR_DEVICE", 9: "ERR_VALUE"}

@@ -78,10 +78,11 @@ cudaError_t launch_stream(const StreamPlan &plan, const void *x, long long ldx, 
                           const uint8_t *ex, void *y, float *partials, int M, int N, int K, int G,
                           cudaStream_t stream);
 
-// Tensor-core kernel (bsf8_umma.cu): 128-row blocks, one split a block; up to 192 token
-// rows.  With more than one split it writes fp32 partials (the fixed-order reduce follows).
+// Tensor-core kernel (bsf8_umma.cu): 128-row blocks, one split and one token tile (up to 192
+// rows) a block.  With more than one split it writes fp32 partials (the fixed-order reduce
+// follows).
 struct UmmaPlan {
-    int S, chunk_cols, ntok, row_blocks, grid_x;
+    int S, chunk_cols, ntok, row_blocks, grid_x, ttiles;  // ttiles: token tiles of ntok rows
     bool partials, tmem_ok, ok;  // ok: the kernel can run this call (else another kernel)
 };
 UmmaPlan plan_umma(int M, int N, int K, int G, int S, bool partials);

@@ -7,7 +7,10 @@
 // Page: "recipes/docker-images/mia-tp4/adapter/wo_a_w8.py" -- _wo_a_partial_w8() and
 // _wo_a_mid_kernel() with their fixed-order split-K sums.
 //
-// A block owns 128 weight rows (a row block of one group) and the columns of one split.
+// A block owns 128 weight rows (a row block of one group), the columns of one split and a
+// tile of up to 192 token rows (calls with more rows run one tile a grid z-index, each
+// rebuilding the weights it streams: past a few hundred rows the product is bound by the
+// tensor cores, not by the weight stream).
 // Per 64-column step:
 //   * the copy warp loads the step's codes (128 rows x 64 bytes, one TMA box; lane 0, up to
 //     10 steps ahead, before the dependency wait too) and the step's x tile (lane 1: the M
@@ -52,7 +55,8 @@ constexpr int kDaMax = 3, kDcMax = 8, kDxMax = 12;  // ring depths, set per call
 constexpr int kSmemU = 208 * 1024;
 constexpr int kRebuildWarps = 8;                // 16 weight rows each
 constexpr int kThreadsU = (2 + kRebuildWarps) * 32;  // warp 0 copies, warp 1 MMA, 2.. rebuild
-constexpr int kMaxTok = 192;
+constexpr int kMaxTok = 192;  // tokens a block (a token tile; more rows take more tiles)
+constexpr int kMaxRowsU = 16384;  // token rows a call (BSF8_MAX_M)
 constexpr int kMaxSplitBlocks = 1024;  // 32-column exponent blocks of a split kept in smem
 // The tensor core's fp32 accumulation into tensor memory loses accuracy with the number of
 // products accumulated in place (measured: the error grows linearly with the steps
@@ -200,6 +204,7 @@ __global__ void __launch_bounds__(kThreadsU, 2) umma_kernel(const __grid_constan
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = blockIdx.y;
     const int rb = blockIdx.x / p.S, split = blockIdx.x % p.S;
+    const int tok0 = blockIdx.z * p.ntok;  // first token row of this block's tile
     const int row0 = rb * kRows;  // first weight row of the block inside group g
     const int k0 = min(p.K, split * p.chunk_cols), k1 = min(p.K, k0 + p.chunk_cols);
     const int nkb = (k1 - k0 + kKB - 1) / kKB;
@@ -272,8 +277,8 @@ __global__ void __launch_bounds__(kThreadsU, 2) umma_kernel(const __grid_constan
                 }
                 mbar_arrive_expect_tx(&full_x[xs], (uint32_t)xbytes);
                 if (!p.skip_loads) {
-                    tma_3d_u(sX + xs * xbytes, &p.xmap, k0 + kb * kKB, g, 0, &full_x[xs]);
-                    tma_3d_u(sX + xs * xbytes + xbytes / 2, &p.xmap, k0 + kb * kKB + kHalf, g, 0, &full_x[xs]);
+                    tma_3d_u(sX + xs * xbytes, &p.xmap, k0 + kb * kKB, g, tok0, &full_x[xs]);
+                    tma_3d_u(sX + xs * xbytes + xbytes / 2, &p.xmap, k0 + kb * kKB + kHalf, g, tok0, &full_x[xs]);
                 }
                 ++n;
             }
@@ -443,7 +448,7 @@ __global__ void __launch_bounds__(kThreadsU, 2) umma_kernel(const __grid_constan
             }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                const int m = c0 + j;
+                const int m = tok0 + c0 + j;
                 if (!store || m >= p.M) continue;
                 float v = acc[j];
                 if (poison) v = __uint_as_float(0x7FC00000u);
@@ -525,7 +530,7 @@ cudaError_t umma_map(const UKey &key, bool codes, CUtensorMap *out) {
     } else {      // x: [M = a][G = b][K = c] bf16, row pitch d elements; box 64 x 1 x ntok (two a step)
         const cuuint64_t dims[3] = {(cuuint64_t)key.c, (cuuint64_t)key.b, (cuuint64_t)key.a};
         const cuuint64_t strides[2] = {(cuuint64_t)key.c * 2u, (cuuint64_t)key.d * 2u};
-        const int ntok = (int)((key.a + 15) / 16 * 16);
+        const int ntok = (int)std::min<long long>(kMaxTok, (key.a + 15) / 16 * 16);  // a token tile
         const cuuint32_t box[3] = {(cuuint32_t)kHalf, 1u, (cuuint32_t)ntok};
         const cuuint32_t es[3] = {1u, 1u, 1u};
         r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(key.ptr), dims, strides, box, es,
@@ -548,14 +553,15 @@ UmmaPlan plan_umma(int M, int N, int K, int G, int S, bool partials) {
     UmmaPlan pl{};
     pl.S = S;
     pl.chunk_cols = ((K / 32 + S - 1) / S) * 32;
-    pl.ntok = (M + 15) / 16 * 16;
+    pl.ntok = std::min(kMaxTok, (M + 15) / 16 * 16);  // tokens a tile
+    pl.ttiles = (M + pl.ntok - 1) / std::max(1, pl.ntok);
     // the split's runs of steps each need ntok accumulator columns of tensor memory
     const int nrun = ((pl.chunk_cols + kKB - 1) / kKB + kChunkSteps - 1) / kChunkSteps;
     pl.tmem_ok = (long long)nrun * pl.ntok <= kTmemMax;
     pl.row_blocks = (N + kRows - 1) / kRows;
     pl.grid_x = pl.row_blocks * S;
     pl.partials = partials || S > 1;
-    pl.ok = M >= 1 && M <= kMaxTok && (long long)G * N < (1LL << 31) && K < (1 << 30) && pl.tmem_ok &&
+    pl.ok = M >= 1 && M <= kMaxRowsU && (long long)G * N < (1LL << 31) && K < (1 << 30) && pl.tmem_ok &&
             pl.chunk_cols / 32 <= kMaxSplitBlocks;
     return pl;
 }
@@ -563,7 +569,8 @@ UmmaPlan plan_umma(int M, int N, int K, int G, int S, bool partials) {
 // Splits for the tensor-core kernel: about one block an SM (the blocks stream, so more
 // blocks than SMs add a wave), then enough that the runs' accumulators fit tensor memory.
 int umma_auto_split(int M, int N, int K, int G, int sms) {
-    const long long blocks = (long long)((N + kRows - 1) / kRows) * G;
+    const long long ttiles = (M + kMaxTok - 1) / kMaxTok;
+    const long long blocks = (long long)((N + kRows - 1) / kRows) * G * ttiles;
     const int smax = std::max(1, K / 32);
     int S = (int)std::max(1LL, (sms + blocks / 2) / std::max(1LL, blocks));
     S = std::min(S, smax);
@@ -640,7 +647,7 @@ cudaError_t launch_umma(const UmmaPlan &pl, const void *x, long long ldx, const 
         __atomic_store_n(&configured[dev], 1, __ATOMIC_RELEASE);
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)pl.grid_x, (unsigned)G, 1);
+    cfg.gridDim = dim3((unsigned)pl.grid_x, (unsigned)G, (unsigned)pl.ttiles);
     cfg.blockDim = dim3(kThreadsU, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;

@@ -55,9 +55,11 @@ enum {
     BSF8_ERR_VALUE = 9      /* an option or scalar argument is out of range             */
 };
 
-/* Largest row count a single bsf8_gemm call accepts (decode, verify and draft batches;
- * the pages serve 2..8 and 9..192 rows from the twin). */
-#define BSF8_MAX_M 192
+/* Largest row count a single bsf8_gemm call accepts.  The pages serve 2..8 and 9..192
+ * decode / verify / draft rows from the twin and prefill through a rebuilt bf16 copy (the
+ * drop mode); here prefill-sized calls run from the twin too: past 192 rows the
+ * tensor-core kernel takes the tokens in tiles of 192. */
+#define BSF8_MAX_M 16384
 
 /* Returns a static, human-readable name for a status code. */
 const char *bsf8_strerror(int status);
@@ -114,7 +116,9 @@ int bsf8_dequant(const uint8_t *w8, const uint8_t *exp, void *out, int G, int N,
  *   workspace device scratch of at least bsf8_gemm_workspace_bytes(...) bytes, or
  *             NULL when that is 0: fp32 partials between the two passes, which the call
  *             runs when its kernel writes partials (the tensor-core kernel, M > 24, with
- *             more than one split; the other kernels when a slab of 16 rows needs more
+ *             more than one split -- past 192 rows at least ceil(K/1024) splits, as a
+ *             token tile's accumulators must fit tensor memory; the other kernels when a
+ *             slab of 16 rows needs more
  *             than 64 column tasks, e.g. split_k > 64).  No zeroing is needed; it must not
  *             be shared by calls that can overlap.
  * The splits are summed inside one thread block, across a cluster of up to 8 blocks

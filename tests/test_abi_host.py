@@ -67,7 +67,7 @@ def test_gemm_validation(lib):
     assert _gemm(lib, x=0) == NULL
     assert _gemm(lib, y=0) == NULL
     assert _gemm(lib, M=0) == SHAPE
-    assert _gemm(lib, M=193) == SHAPE
+    assert _gemm(lib, M=16385) == SHAPE  # past BSF8_MAX_M
     assert _gemm(lib, N=1000) == SHAPE
     assert _gemm(lib, K=4016) == SHAPE          # 4016 = 125.5 * 32
     assert _gemm(lib, G=0) == SHAPE
@@ -161,3 +161,4 @@ def test_binding_rejects_cpu_tensors():
     ex = torch.zeros((1, 1, 1), dtype=torch.uint8)
     with pytest.raises(ValueError, match="CUDA tensor"):
         bsf8.dequant(w8, ex)
+

@@ -30,7 +30,7 @@ def run(x_d, w8_d, ex_d, S, **kw):
 # ---------------------------------------------------------------- exact cases
 
 @pytest.mark.parametrize("path", [0, 5, 6])
-@pytest.mark.parametrize("M", [8, 32])
+@pytest.mark.parametrize("M", [8, 32, 256])
 def test_one_hot_every_code_and_exponent(bsf8_lib, M, path):
     """x rows are unit vectors: every output is one exact product, so the GEMM must
     reproduce the oracle bit for bit (zeros by value, NaN as NaN) for all 256 codes x
@@ -311,3 +311,30 @@ def test_tensor_core_kernel_mid_rows(bsf8_lib, M, S):
     assert np.array_equal(y, two)
     rows = sorted({0, M // 2, M - 1})
     assert_gemm_close(y[rows], oracle.gemm(x[rows], w8, ex))
+
+
+@pytest.mark.parametrize("M,S", [(193, 0), (256, 4), (1024, 0)])
+def test_large_m_token_tiles(bsf8_lib, M, S):
+    """Past 192 rows (prefill-sized calls) the tensor-core kernel takes the tokens in tiles
+    of 192 (a grid index each): the mid-row weight (G = 4 groups of W[1024, 4096]) with the
+    last tile partly filled, sampled token rows within the oracle's tolerance, the fused
+    call bitwise equal to its two-pass form and run-to-run reproducible."""
+    wk = wl.MID
+    w8, ex = wk.weights()
+    x = wk.x(M=M)
+    w8_d, ex_d, x_d = dev(w8, ex, x)
+    S_used = S or bsf8.auto_split(M, wk.N, wk.K, wk.G)
+    y = run(x_d, w8_d, ex_d, S)
+    y2 = run(x_d, w8_d, ex_d, S)
+    two = bf16_bits(bsf8.splitk_reduce(bsf8.gemm_partials(x_d, w8_d, ex_d, S_used)))
+    assert bsf8.device_status() == 0
+    assert np.array_equal(y, y2)
+    assert np.array_equal(y, two)
+    rows = sorted({0, 191, 192, M // 2, M - 1})
+    assert_gemm_close(y[rows], oracle.gemm(x[rows], w8, ex), f"mid M={M}")
+
+
+def test_large_m_head_with_row_stride(bsf8_lib):
+    """The head-like weight (N = 32768, K = 5120) at 512 token rows with padded x rows:
+    two token rows and the last 2048 weight rows against the oracle."""
+    check(wl.HEAD, 512, 0, ldx_pad=64, rows=[0, 511], n_range=(32768 - 2048, 32768))
