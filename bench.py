@@ -559,6 +559,26 @@ def run_suite(device, peak):
     for M in (1, 2, 6, 16, 64, 128):
         gemm_row("a3-a6 gemm head", wl.HEAD, M, 0, 3)
 
+    # fp32 output (the draft head's fp32 logits): partials of the kernel the shape selects,
+    # summed over the splits in fp32
+    for M in (6, 64, 128):
+        wk = wl.HEAD
+        layers = []
+        for c, (w8, ex) in enumerate(weights_of(wk, 3)):
+            x = wk.x(copy=c, M=M)
+            layers.append((w8, ex, torch.from_numpy(x.view("int16")).view(torch.bfloat16).to(device)))
+        S = bsf8.auto_split(M, wk.N, wk.K, wk.G)
+        Ps = [torch.empty((S, M, wk.G, wk.N), dtype=torch.float32, device=device) for _ in layers]
+        ys = [torch.empty((M, wk.G, wk.N), dtype=torch.float32, device=device) for _ in layers]
+        calls = [lambda l=l, P=P, y=y: (bsf8.gemm_partials(l[2], l[0], l[1], S, out=P),
+                                        bsf8.splitk_reduce_f32(P, out=y) if S > 1 else None)
+                 for l, P, y in zip(layers, Ps, ys)]
+        t = graph_time(calls, 20)
+        xy = M * wk.G * wk.K * 2 + M * wk.G * wk.N * 4
+        emit("f2 gemm fp32 out", f"G={wk.G} N={wk.N} K={wk.K} M={M} split_k={S}, 3 copies", t,
+             wk.weight_bytes + xy, wk.weight_bytes)
+        del layers, Ps, ys
+
     # Past 192 rows (prefill-sized calls, the pages' drop mode served from the twin): bound by
     # the tensor cores, so reported against the measured dense bf16 peak too.  The calls of a
     # row share one workspace: they run one after another on the stream.

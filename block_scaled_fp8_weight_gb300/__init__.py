@@ -19,7 +19,7 @@ import threading
 from . import build as _build
 
 __all__ = [
-    "Bsf8Error", "load", "make_twin", "twin_or_none", "dequant", "gemm", "gemm_partials",
+    "Bsf8Error", "load", "make_twin", "twin_or_none", "dequant", "gemm", "gemm_partials", "gemm_f32", "splitk_reduce_f32",
     "splitk_reduce", "pad_k", "pad_x", "workspace_bytes", "auto_split", "device_status",
     "set_option", "get_option", "OPT_PDL", "OPT_WAIT_TIMEOUT_NS", "OPT_DEBUG_SKIP_LOADS",
     "OPT_GEMM_PATH",
@@ -73,6 +73,7 @@ def load(build_if_missing: bool = True):
             "bsf8_gemm_auto_split": (I, [I, I, I, I]),
             "bsf8_gemm_partials": (I, [P, P, P, P, I, I, I, I, I, I64, P]),
             "bsf8_splitk_reduce": (I, [P, P, I, I64, P]),
+            "bsf8_splitk_reduce_f32": (I, [P, P, I, I64, P]),
             "bsf8_pad_k": (I, [P, P, P, P, I, I, I, I, I, P]),
             "bsf8_pad_x": (I, [P, I64, P, I, I, I, I, P]),
             "bsf8_device_status": (I, [P, P]),
@@ -234,6 +235,30 @@ def splitk_reduce(P, out=None):
     _check(lib.bsf8_splitk_reduce(_dev(P, torch.float32, "partials"), _dev(out, torch.bfloat16, "y"),
                                   S, count, _stream(P)), "bsf8_splitk_reduce")
     return out
+
+
+def splitk_reduce_f32(P, out=None):
+    """The fixed-order sum over the leading axis kept in fp32."""
+    torch = _torch()
+    lib = load()
+    _contig(P, "partials")
+    S = P.shape[0]
+    count = P[0].numel()
+    if out is None:
+        out = torch.empty(P.shape[1:], dtype=torch.float32, device=P.device)
+    _check(lib.bsf8_splitk_reduce_f32(_dev(P, torch.float32, "partials"), _dev(out, torch.float32, "y"),
+                                      S, count, _stream(P)), "bsf8_splitk_reduce_f32")
+    return out
+
+
+def gemm_f32(x, w8, ex, split_k: int = 0):
+    """The GEMM with fp32 output [M,G,N] (the head's fp32-logits variant): the partials of
+    the kernel the shape selects, summed over the splits in fixed order in fp32."""
+    G, N, K = w8.shape
+    M, _ = _x_view(x, G, K)
+    S = split_k or auto_split(M, N, K, G)
+    P = gemm_partials(x, w8, ex, S)
+    return P[0] if S == 1 else splitk_reduce_f32(P)
 
 
 # ----------------------------------------------------------------------- pad-K

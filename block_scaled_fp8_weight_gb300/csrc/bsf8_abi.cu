@@ -304,6 +304,14 @@ int bsf8_splitk_reduce(const float *partials, void *y, int S, int64_t count, bsf
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int bsf8_splitk_reduce_f32(const float *partials, float *y, int S, int64_t count, bsf8_stream_t stream) {
+    if (S < 1 || count < 0) return BSF8_ERR_SHAPE;
+    if (count == 0) return BSF8_OK;
+    if (!partials || !y) return BSF8_ERR_NULL;
+    return from_cuda(launch_splitk_reduce_f32(partials, y, S, (long long)count,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int bsf8_pad_k(const uint8_t *w8, const uint8_t *exp, uint8_t *w8_out, uint8_t *exp_out, int G,
                int N, int K, int Kp, int pad_exp, bsf8_stream_t stream) {
     if (!w8 || !exp || !w8_out || !exp_out) return BSF8_ERR_NULL;

@@ -312,8 +312,11 @@ __global__ void __launch_bounds__(kGemmThreads) gemm_kernel(const __grid_constan
 //   y[i] = bf16( ((P[0][i] + P[1][i]) + P[2][i]) + ... ),  fp32, left to right.
 // Writes nothing while the device status word holds a timeout: the partials a first pass
 // left after giving up a wait are incomplete (the status stays until the host reads it).
+// OUT is uint16_t (bf16 y, one RNE) or float (the fp32 sums themselves: the head's fp32
+// logits variant).
+template <typename OUT>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restrict__ P,
-                                                            uint16_t *__restrict__ y, int S,
+                                                            OUT *__restrict__ y, int S,
                                                             long long count, const int *status) {
     pdl_trigger();
     pdl_wait();
@@ -322,7 +325,10 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restr
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += stride) {
         float v = __ldcg(P + i);
         for (int s = 1; s < S; ++s) v = v + __ldcg(P + (size_t)s * count + i);
-        y[i] = f32_to_bf16_rn(v);
+        if constexpr (sizeof(OUT) == 2)
+            y[i] = f32_to_bf16_rn(v);
+        else
+            y[i] = v;
     }
 }
 
@@ -428,8 +434,10 @@ cudaError_t launch_gemm(const GemmPlan &pl, const void *x, long long ldx, const 
     }
 }
 
-cudaError_t launch_splitk_reduce(const float *P, void *y, int S, long long count,
-                                 cudaStream_t stream) {
+namespace {
+
+template <typename OUT>
+cudaError_t launch_reduce(const float *P, OUT *y, int S, long long count, cudaStream_t stream) {
     if (count == 0) return cudaSuccess;
     const Options opt = options();
     cudaLaunchConfig_t cfg = {};
@@ -444,7 +452,17 @@ cudaError_t launch_splitk_reduce(const float *P, void *y, int S, long long count
     cfg.numAttrs = opt.pdl ? 1 : 0;
     const int *status = status_word();
     if (!status) return cudaErrorInvalidSymbol;
-    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, P, static_cast<uint16_t *>(y), S, count, status);
+    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<OUT>, P, y, S, count, status);
+}
+
+}  // namespace
+
+cudaError_t launch_splitk_reduce(const float *P, void *y, int S, long long count, cudaStream_t stream) {
+    return launch_reduce(P, static_cast<uint16_t *>(y), S, count, stream);
+}
+
+cudaError_t launch_splitk_reduce_f32(const float *P, float *y, int S, long long count, cudaStream_t stream) {
+    return launch_reduce(P, y, S, count, stream);
 }
 
 }  // namespace bsf8

@@ -113,6 +113,7 @@ cudaError_t launch_gemm(const GemmPlan &plan, const void *x, long long ldx, cons
                         cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const float *P, void *y, int S, long long count,
                                  cudaStream_t stream);
+cudaError_t launch_splitk_reduce_f32(const float *P, float *y, int S, long long count, cudaStream_t stream);
 cudaError_t launch_dequant(const uint8_t *w8, const uint8_t *ex, void *out, int G, int N, int K,
                            cudaStream_t stream);
 cudaError_t launch_make_twin(const void *w, uint8_t *w8, uint8_t *ex, uint8_t *ok,

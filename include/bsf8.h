@@ -166,6 +166,14 @@ int bsf8_gemm_partials(const void *x, const uint8_t *w8, const uint8_t *exp,
 int bsf8_splitk_reduce(const float *partials, void *y, int S, int64_t count,
                        bsf8_stream_t stream);
 
+/* The same fixed-order sum kept in fp32: y[i] = ((P[0][i] + P[1][i]) + ...) + P[S-1][i],
+ * y a device float array of `count` values.  With bsf8_gemm_partials it gives the GEMM's
+ * fp32 output -- the head variant of "docs/tp4-adapters.md" (draft_head_fp8: the block
+ * logits of up to 64..128 rows as fp32, the head streamed once per call); with one split
+ * the partials are that output already.  Errors and the timeout rule as bsf8_splitk_reduce. */
+int bsf8_splitk_reduce_f32(const float *partials, float *y, int S, int64_t count,
+                           bsf8_stream_t stream);
+
 /* --------------------------------------------------- GEMM without a workspace
  * The pages have no counterpart for this entry point; it serves callers that cannot
  * allocate device memory for a workspace -- e.g. a serving engine that has reserved all of

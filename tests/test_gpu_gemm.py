@@ -338,3 +338,26 @@ def test_large_m_head_with_row_stride(bsf8_lib):
     """The head-like weight (N = 32768, K = 5120) at 512 token rows with padded x rows:
     two token rows and the last 2048 weight rows against the oracle."""
     check(wl.HEAD, 512, 0, ldx_pad=64, rows=[0, 511], n_range=(32768 - 2048, 32768))
+
+
+@pytest.mark.parametrize("M,S", [(6, 0), (64, 0), (128, 2)])
+def test_fp32_output_head_variant(bsf8_lib, M, S):
+    """fp32 logits (the draft head's variant) on the head-like weight: against the exact
+    (binary64) sums of the same products, within the worst-case error of any fp32
+    summation order, |y - y64| <= K * 2^-23 * sum|x*w| (each product is exact in fp32);
+    and the bf16 GEMM is these sums rounded once."""
+    wk = wl.HEAD
+    w8, ex = wk.weights()
+    x = wk.x(M=M)
+    w8_d, ex_d, x_d = dev(w8, ex, x)
+    y32 = bsf8.gemm_f32(x_d, w8_d, ex_d, split_k=S).cpu().numpy()
+    assert y32.dtype == np.float32 and y32.shape == (M, 1, wk.N)
+    n0 = wk.N - 1024
+    rows = sorted({0, M - 1})
+    y64, a64 = oracle.gemm_f64(x[rows], w8[:, n0:], ex[:, n0 // 32:])
+    err = np.abs(y32[rows][:, :, n0:].astype(np.float64) - y64)
+    assert np.all(err <= wk.K * 2.0 ** -23 * a64)
+    S_used = S or bsf8.auto_split(M, wk.N, wk.K, wk.G)
+    yb = bf16_bits(bsf8.gemm(x_d, w8_d, ex_d, split_k=S_used))
+    yr = torch.from_numpy(y32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(yb, yr)
