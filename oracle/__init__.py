@@ -77,6 +77,9 @@ def _load():
             "bsfo_splitk_reduce": (None, [P, P, L, I]),
             "bsfo_pad_k": (None, [P, P, P, P, I, I, I, I, ctypes.c_uint8]),
             "bsfo_pad_x": (None, [P, L, P, I, I, I, I]),
+            "bsfo_dequant_rows": (None, [P, P, P, I, I, I]),
+            "bsfo_make_twin_rows": (I, [P, P, P, P, I, I, I]),
+            "bsfo_gemm_rows": (None, [P, L, P, P, P, I, I, I, I]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -185,6 +188,39 @@ def gemm(x: np.ndarray, w8: np.ndarray, ex: np.ndarray, M: int | None = None) ->
     assert ldx >= G * K
     y = np.empty((M, G, N), dtype=np.uint16)
     _load().bsfo_gemm(_ptr(x), ldx, _ptr(w8), _ptr(ex), _ptr(y), M, N, K, G)
+    return y
+
+
+def dequant_rows(w8: np.ndarray, ex: np.ndarray) -> np.ndarray:
+    """w8 uint8 [G,N,K], ex uint8 [G,N,K/32] (one exponent per row and 32 columns) -> bf16
+    bits uint16 [G,N,K]."""
+    w8, ex = _u8(w8), _u8(ex)
+    G, N, K = w8.shape
+    assert ex.shape == (G, N, K // 32)
+    out = np.empty((G, N, K), dtype=np.uint16)
+    _load().bsfo_dequant_rows(_ptr(w8), _ptr(ex), _ptr(out), G, N, K)
+    return out
+
+
+def make_twin_rows(w: np.ndarray):
+    """make_twin with 1 x 32 blocks: (accepted, w8 [G,N,K], ex [G,N,K/32], ok [G,N,K/32])."""
+    w = _u16(w)
+    G, N, K = w.shape
+    w8 = np.empty((G, N, K), dtype=np.uint8)
+    ex = np.empty((G, N, K // 32), dtype=np.uint8)
+    ok = np.empty((G, N, K // 32), dtype=np.uint8)
+    acc = _load().bsfo_make_twin_rows(_ptr(w), _ptr(w8), _ptr(ex), _ptr(ok), G, N, K)
+    return bool(acc), w8, ex, ok
+
+
+def gemm_rows(x: np.ndarray, w8: np.ndarray, ex: np.ndarray) -> np.ndarray:
+    """The GEMM with per-(row, 32-column) exponents ex [G,N,K/32]."""
+    x, w8, ex = _u16(x), _u8(w8), _u8(ex)
+    G, N, K = w8.shape
+    M, ldx = x.shape
+    assert ldx >= G * K and ex.shape == (G, N, K // 32)
+    y = np.empty((M, G, N), dtype=np.uint16)
+    _load().bsfo_gemm_rows(_ptr(x), ldx, _ptr(w8), _ptr(ex), _ptr(y), M, N, K, G)
     return y
 
 

@@ -363,6 +363,101 @@ void bsfo_pad_x(const uint16_t *x, long ldx, uint16_t *x_out, int M, int G, int 
                     k < K ? x[(size_t)m * ldx + (size_t)g * K + k] : (uint16_t)0x0000;
 }
 
+/* ------------------------------------------- per-(row, 32-column) scales */
+
+/* The pages' second twin layout ("recipes/docker-images/mia-tp4/docs/tp4-adapters.md",
+ * adapter table, draft_main_proj): e4m3 codes with one power-of-two scale per (weight
+ * row, 32 columns), checked to reproduce the bf16 weight exactly.  The pages give no
+ * formula for it; this oracle takes make_twin's rule with the block narrowed to 1 x 32:
+ * the exponent layout is ex[G][N][K/32], everything else as above. */
+
+/* w8[G][N][K] codes, ex[G][N][K/32] exponent bytes -> out[G][N][K] bf16 bits. */
+void bsfo_dequant_rows(const uint8_t *w8, const uint8_t *ex, uint16_t *out, int G, int N, int K)
+{
+    int kb = K / 32;
+    for (int g = 0; g < G; ++g)
+        for (int n = 0; n < N; ++n)
+            for (int k = 0; k < K; ++k) {
+                size_t i = ((size_t)g * N + n) * K + k;
+                uint8_t e = ex[((size_t)g * N + n) * kb + k / 32];
+                out[i] = bsfo_dequant_one(w8[i], e);
+            }
+}
+
+/* make_twin with 1 x 32 blocks: per (row n, columns 32j .. 32j+31), amax over those 32
+ * values, the same exponent rule, codes and exact-rebuild check, and the same marking of
+ * blocks that hold NaN or Inf.  ex, ok: [G][N][K/32].  Returns 1 if every element
+ * reproduces. */
+int bsfo_make_twin_rows(const uint16_t *w, uint8_t *w8, uint8_t *ex, uint8_t *ok,
+                        int G, int N, int K)
+{
+    int kb = K / 32;
+    int accepted = 1;
+    for (int g = 0; g < G; ++g)
+        for (int n = 0; n < N; ++n)
+            for (int bj = 0; bj < kb; ++bj) {
+                size_t blk = ((size_t)g * N + n) * kb + bj;
+                size_t base = ((size_t)g * N + n) * K + (size_t)bj * 32;
+                float amax = 0.0f;
+                int nonfinite = 0;
+                for (int c = 0; c < 32; ++c) {
+                    float a = fabsf(bsfo_bf16_to_f32(w[base + c]));
+                    if (!isfinite(a))
+                        nonfinite = 1;
+                    else if (a > amax)
+                        amax = a;
+                }
+                if (nonfinite) {
+                    for (int c = 0; c < 32; ++c)
+                        w8[base + c] = 0x7F;
+                    ex[blk] = 0xFF;
+                    if (ok)
+                        ok[blk] = 0;
+                    accepted = 0;
+                    continue;
+                }
+                int e = bsfo_twin_exponent(amax);
+                float scale = ldexpf(1.0f, e);
+                int block_ok = 1;
+                for (int c = 0; c < 32; ++c) {
+                    float wf = bsfo_bf16_to_f32(w[base + c]);
+                    uint8_t q = bsfo_e4m3_rne(wf / scale);
+                    float back = bsfo_bf16_to_f32(bsfo_bf16_rne(bsfo_e4m3_decode(q) * scale));
+                    w8[base + c] = q;
+                    if (!(back == wf))
+                        block_ok = 0;
+                }
+                ex[blk] = (uint8_t)(e + 127);
+                if (ok)
+                    ok[blk] = (uint8_t)block_ok;
+                if (!block_ok)
+                    accepted = 0;
+            }
+    return accepted;
+}
+
+/* The GEMM of bsfo_gemm with the weight rebuilt from per-(row, 32-column) exponents. */
+void bsfo_gemm_rows(const uint16_t *x, long ldx, const uint8_t *w8, const uint8_t *ex,
+                    uint16_t *y, int M, int N, int K, int G)
+{
+    int kb = K / 32;
+    for (int m = 0; m < M; ++m)
+        for (int g = 0; g < G; ++g)
+            for (int n = 0; n < N; ++n) {
+                float acc = 0.0f;
+                const uint8_t *wrow = w8 + ((size_t)g * N + n) * K;
+                const uint8_t *erow = ex + ((size_t)g * N + n) * kb;
+                const uint16_t *xrow = x + (size_t)m * ldx + (size_t)g * K;
+                for (int k = 0; k < K; ++k) {
+                    float wv = bsfo_bf16_to_f32(bsfo_dequant_one(wrow[k], erow[k / 32]));
+                    float xv = bsfo_bf16_to_f32(xrow[k]);
+                    float p = xv * wv;
+                    acc = acc + p;
+                }
+                y[((size_t)m * G + g) * N + n] = bsfo_bf16_rne(acc);
+            }
+}
+
 /* ------------------------------------------------------- array wrappers */
 
 /* Element-wise loops over the scalar codecs above, so tests can sweep millions of

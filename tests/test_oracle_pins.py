@@ -507,3 +507,90 @@ def test_pad_k_keeps_groups_apart():
     for g in range(G):
         assert np.array_equal(xp[:, g * Kp:g * Kp + K], x[:, g * K:(g + 1) * K])
         assert np.array_equal(wp[g, :, :K], w8[g])
+
+
+# ------------------------------------------------ per-(row, 32-column) scale variant
+
+def _expand_rows(ex):
+    """Block exponents [G, N/32, K/32] -> the same exponent on every row [G, N, K/32]."""
+    return np.repeat(ex, 32, axis=1)
+
+
+def test_dequant_rows_equals_block_dequant_with_repeated_exponents():
+    """With each 32x32 block's exponent copied to its 32 rows, the per-row rebuild is the
+    block rebuild (pinned exhaustively above), over all codes and the whole exponent range."""
+    r = wl.rng(61)
+    G, N, K = 2, 64, 256
+    w8 = r.integers(0, 256, size=(G, N, K)).astype(np.uint8)
+    ex = r.integers(0, 256, size=(G, N // 32, K // 32)).astype(np.uint8)
+    a = oracle.dequant(w8, ex)
+    b = oracle.dequant_rows(w8, _expand_rows(ex))
+    assert np.array_equal(a, b)
+    # and each row follows its own exponent: change one row's byte, only that row moves
+    exr = _expand_rows(ex).copy()
+    exr[1, 37, 3] = 120
+    c = oracle.dequant_rows(w8, exr)
+    diff = np.argwhere(c != b)
+    assert diff.size and np.all(diff[:, 0] == 1) and np.all(diff[:, 1] == 37)
+    assert np.all((diff[:, 2] >= 96) & (diff[:, 2] < 128))
+
+
+def test_gemm_rows_equals_block_gemm_with_repeated_exponents():
+    r = wl.rng(62)
+    G, N, K, M = 2, 64, 256, 5
+    w8 = wl.codes(r, (G, N, K))
+    ex = wl.exponents(r, (G, N // 32, K // 32), 110, 130)
+    x = wl.activations(r, M, G * K + 8)
+    assert np.array_equal(oracle.gemm(x, w8, ex), oracle.gemm_rows(x, w8, _expand_rows(ex)))
+
+
+def _rows_exact_weight(seed, G=1, N=64, K=128, lo=110, hi=130):
+    """A bf16 weight built from codes and per-(row, 32-column) exponents, so that it has
+    an exact per-row twin; every 1 x 32 segment holds a +-448 code."""
+    r = wl.rng(seed)
+    w8 = wl.codes(r, (G, N, K))
+    w8[..., ::32] = np.where(r.integers(0, 2, size=w8[..., ::32].shape) == 1, 0xFE, 0x7E).astype(np.uint8)
+    ex = wl.exponents(r, (G, N, K // 32), lo, hi)
+    return w8, ex, oracle.dequant_rows(w8, ex)
+
+
+def test_make_twin_rows_recovers_the_generating_twin():
+    w8, ex, w = _rows_exact_weight(63)
+    accepted, t8, tex, ok = oracle.make_twin_rows(w)
+    assert accepted and ok.all()
+    assert np.array_equal(tex, ex) and np.array_equal(t8, w8)
+    assert np.array_equal(oracle.dequant_rows(t8, tex), w)
+
+
+def test_make_twin_rows_exponents_against_blocks_and_brute_force():
+    """On N(0,1) weights: a row segment's exponent is at most its 32x32 block's, equal in
+    the rows that hold the block maximum, and each equals the exact smallest e with
+    448 * 2^e >= the segment's largest magnitude."""
+    r = wl.rng(64)
+    w = wl.activations(r, 64, 128).reshape(1, 64, 128)
+    _, _, tex_b, _ = oracle.make_twin(w)
+    acc, t8, tex, ok = oracle.make_twin_rows(w)
+    eb = _expand_rows(tex_b).astype(int)
+    assert np.all(tex.astype(int) <= eb)
+    wf = oracle.bf16_bits_to_f32(w).astype(np.float64)
+    seg = np.abs(wf).reshape(1, 64, 4, 32).max(axis=3)
+    blk = seg.reshape(1, 2, 32, 4).max(axis=2)
+    at_max = seg == np.repeat(blk, 32, axis=1)
+    assert np.array_equal(tex[at_max], eb[at_max].astype(np.uint8))
+    for n in range(0, 64, 7):
+        for j in range(4):
+            assert tex[0, n, j] == _exact_twin_exponent(Fraction(float(seg[0, n, j]))) + 127
+
+
+def test_make_twin_rows_rejects_exactly_the_nudged_segments():
+    _, _, w = _rows_exact_weight(65)
+    G, N, K = w.shape
+    sites = [5 * K + 40, 17 * K + 3, 63 * K + 127]
+    wn = wl.apply_nudge(w, sites)
+    accepted, _, _, ok = oracle.make_twin_rows(wn)
+    assert not accepted
+    want = np.ones_like(ok)
+    for s in sites:
+        n, k = divmod(s, K)
+        want[0, n, k // 32] = 0
+    assert np.array_equal(ok, want)
