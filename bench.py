@@ -559,6 +559,38 @@ def run_suite(device, peak):
     for M in (1, 2, 6, 16, 64, 128):
         gemm_row("a3-a6 gemm head", wl.HEAD, M, 0, 3)
 
+    # per-(row, 32-column) scales (the draft main_proj's layout): twin, dequant and GEMM at
+    # its shape (1280 output rows, K = 5120), 43 copies
+    N1, K1 = 1280, 5120
+    rng = wl.rng(90)
+    rw8 = [torch.from_numpy(wl.codes(rng, (1, N1, K1))).to(device) for _ in range(LAYERS)]
+    rex = [torch.from_numpy(wl.exponents(rng, (1, N1, K1 // 32), 110, 130)).to(device) for _ in range(LAYERS)]
+    rbf = [bsf8.dequant_rows(a, b) for a, b in zip(rw8, rex)]
+    o8 = [torch.empty_like(a) for a in rw8]
+    oe = [torch.empty_like(b) for b in rex]
+    ok = [torch.empty_like(b) for b in rex]
+    acc = torch.empty((LAYERS,), dtype=torch.int32, device=device)
+    calls = [lambda i=i: lib.bsf8_make_twin_rows(ptr(rbf[i]), ptr(o8[i]), ptr(oe[i]), ptr(ok[i]),
+                                                 ctypes.c_void_p(acc.data_ptr() + 4 * i), 1, N1, K1, sp())
+             for i in range(LAYERS)]
+    t = graph_time(calls, 50)
+    emit("f3 rows make_twin", f"N={N1} K={K1} bf16 -> twin, {LAYERS} copies", t, N1 * K1 * 3 + 2 * N1 * K1 // 32)
+    calls = [lambda i=i: lib.bsf8_dequant_rows(ptr(rw8[i]), ptr(rex[i]), ptr(rbf[i]), 1, N1, K1, sp())
+             for i in range(LAYERS)]
+    t = graph_time(calls, 50)
+    emit("f3 rows dequant", f"N={N1} K={K1} twin -> bf16, {LAYERS} copies", t, N1 * K1 * 3 + N1 * K1 // 32)
+    wbytes = N1 * K1 + N1 * K1 // 32
+    for M in (1, 6, 16):
+        xs = [torch.from_numpy(wl.activations(rng, M, K1).view("int16")).view(torch.bfloat16).to(device)
+              for _ in range(LAYERS)]
+        ys = [torch.empty((M, 1, N1), dtype=torch.bfloat16, device=device) for _ in range(LAYERS)]
+        calls = [lambda i=i: bsf8.gemm_rows(xs[i], rw8[i], rex[i], out=ys[i]) for i in range(LAYERS)]
+        t = graph_time(calls, 100)
+        emit("f3 rows gemm", f"N={N1} K={K1} M={M} split_k=auto, {LAYERS} copies", t,
+             wbytes + M * K1 * 2 + M * N1 * 2, wbytes)
+        del xs, ys
+    del rw8, rex, rbf, o8, oe, ok
+
     # fp32 output (the draft head's fp32 logits): partials of the kernel the shape selects,
     # summed over the splits in fp32
     for M in (6, 64, 128):

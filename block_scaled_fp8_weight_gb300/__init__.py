@@ -19,7 +19,7 @@ import threading
 from . import build as _build
 
 __all__ = [
-    "Bsf8Error", "load", "make_twin", "twin_or_none", "dequant", "gemm", "gemm_partials", "gemm_f32", "splitk_reduce_f32",
+    "Bsf8Error", "load", "make_twin", "twin_or_none", "dequant", "gemm", "gemm_partials", "gemm_f32", "splitk_reduce_f32", "make_twin_rows", "dequant_rows", "gemm_rows",
     "splitk_reduce", "pad_k", "pad_x", "workspace_bytes", "auto_split", "device_status",
     "set_option", "get_option", "OPT_PDL", "OPT_WAIT_TIMEOUT_NS", "OPT_DEBUG_SKIP_LOADS",
     "OPT_GEMM_PATH",
@@ -72,6 +72,10 @@ def load(build_if_missing: bool = True):
             "bsf8_gemm_workspace_bytes": (SZ, [I, I, I, I, I]),
             "bsf8_gemm_auto_split": (I, [I, I, I, I]),
             "bsf8_gemm_partials": (I, [P, P, P, P, I, I, I, I, I, I64, P]),
+            "bsf8_make_twin_rows": (I, [P, P, P, P, P, I, I, I, P]),
+            "bsf8_dequant_rows": (I, [P, P, P, I, I, I, P]),
+            "bsf8_gemm_rows_workspace_bytes": (SZ, [I, I, I, I, I]),
+            "bsf8_gemm_rows": (I, [P, P, P, P, I, I, I, I, I, I64, P, SZ, P]),
             "bsf8_splitk_reduce": (I, [P, P, I, I64, P]),
             "bsf8_splitk_reduce_f32": (I, [P, P, I, I64, P]),
             "bsf8_pad_k": (I, [P, P, P, P, I, I, I, I, I, P]),
@@ -158,6 +162,64 @@ def dequant(w8, ex, out=None):
     _check(lib.bsf8_dequant(_dev(w8, torch.uint8, "w8"), _dev(ex, torch.uint8, "exp"),
                             _dev(out, torch.bfloat16, "out"), G, N, K, _stream(w8)),
            "bsf8_dequant")
+    return out
+
+
+# ------------------------------------------ per-(row, 32-column) scale variant
+
+def make_twin_rows(w):
+    """make_twin with one exponent per (row, 32 columns): (accepted, w8 [G,N,K],
+    exp [G,N,K/32], block_ok [G,N,K/32]).  Synchronises once to read `accepted`."""
+    torch = _torch()
+    lib = load()
+    w3 = w.unsqueeze(0) if w.dim() == 2 else w
+    _contig(w3, "w")
+    G, N, K = w3.shape
+    w8 = torch.empty((G, N, K), dtype=torch.uint8, device=w.device)
+    ex = torch.empty((G, N, K // 32), dtype=torch.uint8, device=w.device)
+    ok = torch.empty((G, N, K // 32), dtype=torch.uint8, device=w.device)
+    acc = torch.empty((1,), dtype=torch.int32, device=w.device)
+    _check(lib.bsf8_make_twin_rows(_dev(w3, torch.bfloat16, "w"), _dev(w8, torch.uint8, "w8"),
+                                   _dev(ex, torch.uint8, "exp"), _dev(ok, torch.uint8, "block_ok"),
+                                   _dev(acc, torch.int32, "accepted"), G, N, K, _stream(w3)),
+           "bsf8_make_twin_rows")
+    return bool(acc.item()), w8, ex, ok
+
+
+def dequant_rows(w8, ex, out=None):
+    """Twin with per-(row, 32-column) exponents -> bf16 [G,N,K]."""
+    torch = _torch()
+    lib = load()
+    _contig(w8, "w8")
+    _contig(ex, "exp")
+    G, N, K = w8.shape
+    if out is None:
+        out = torch.empty((G, N, K), dtype=torch.bfloat16, device=w8.device)
+    _check(lib.bsf8_dequant_rows(_dev(w8, torch.uint8, "w8"), _dev(ex, torch.uint8, "exp"),
+                                 _dev(out, torch.bfloat16, "out"), G, N, K, _stream(w8)),
+           "bsf8_dequant_rows")
+    return out
+
+
+def gemm_rows(x, w8, ex, split_k: int = 0, out=None, workspace=None):
+    """The GEMM with per-(row, 32-column) exponents ex [G,N,K/32]; bf16 [M,G,N]."""
+    torch = _torch()
+    lib = load()
+    _contig(w8, "w8")
+    _contig(ex, "exp")
+    G, N, K = w8.shape
+    M, ldx = _x_view(x, G, K)
+    if out is None:
+        out = torch.empty((M, G, N), dtype=torch.bfloat16, device=x.device)
+    need = int(lib.bsf8_gemm_rows_workspace_bytes(M, N, K, G, split_k)) if 1 <= M <= MAX_M else 0
+    ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
+    if need:
+        if workspace is None:
+            workspace = torch.empty((need,), dtype=torch.uint8, device=x.device)
+        ws_ptr, ws_bytes = _dev(workspace, torch.uint8, "workspace"), workspace.numel()
+    _check(lib.bsf8_gemm_rows(_dev(x, torch.bfloat16, "x"), _dev(w8, torch.uint8, "w8"),
+                              _dev(ex, torch.uint8, "exp"), _dev(out, torch.bfloat16, "y"),
+                              M, N, K, G, split_k, ldx, ws_ptr, ws_bytes, _stream(x)), "bsf8_gemm_rows")
     return out
 
 

@@ -279,6 +279,50 @@ int bsf8_gemm(const void *x, const uint8_t *w8, const uint8_t *exp, void *y, int
     }
 }
 
+int bsf8_make_twin_rows(const void *w, uint8_t *w8, uint8_t *exp, uint8_t *block_ok, int32_t *accepted,
+                        int G, int N, int K, bsf8_stream_t stream) {
+    if (!w || !w8 || !exp || !accepted) return BSF8_ERR_NULL;
+    int st = check_gnk(G, N, K);
+    if (st) return st;
+    if (!aligned16(w) || !aligned16(w8)) return BSF8_ERR_ALIGN;
+    return from_cuda(launch_make_twin_rows(w, w8, exp, block_ok, accepted, G, N, K,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int bsf8_dequant_rows(const uint8_t *w8, const uint8_t *exp, void *out, int G, int N, int K,
+                      bsf8_stream_t stream) {
+    if (!w8 || !exp || !out) return BSF8_ERR_NULL;
+    int st = check_gnk(G, N, K);
+    if (st) return st;
+    if (!aligned16(w8) || !aligned16(out)) return BSF8_ERR_ALIGN;
+    return from_cuda(launch_dequant_rows(w8, exp, out, G, N, K, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t bsf8_gemm_rows_workspace_bytes(int M, int N, int K, int G, int split_k) {
+    if (check_gnk(G, N, K) || M < 1 || M > BSF8_MAX_M || split_k < 0 || split_k > K / 32) return 0;
+    const int S = split_k == 0 ? auto_split(M, N, K, G) : split_k;
+    if (plan_stream(M, N, K, G, S, false).mode != kStreamPartials) return 0;
+    return (size_t)S * M * G * N * sizeof(float);
+}
+
+int bsf8_gemm_rows(const void *x, const uint8_t *w8, const uint8_t *exp, void *y, int M, int N, int K, int G,
+                   int split_k, int64_t ldx, void *workspace, size_t workspace_bytes, bsf8_stream_t stream) {
+    int st = check_gemm_args(x, w8, exp, y, M, N, K, G, split_k, ldx);
+    if (st) return st;
+    const int S = split_k == 0 ? auto_split(M, N, K, G) : split_k;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const StreamPlan pl = plan_stream(M, N, K, G, S, false);
+    if (pl.mode != kStreamPartials)
+        return from_cuda(launch_stream(pl, x, ldx, w8, exp, y, nullptr, M, N, K, G, s, true));
+    const size_t need = (size_t)S * M * G * N * sizeof(float);
+    if (!workspace || workspace_bytes < need) return BSF8_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return BSF8_ERR_ALIGN;
+    float *P = static_cast<float *>(workspace);
+    st = from_cuda(launch_stream(pl, x, ldx, w8, exp, nullptr, P, M, N, K, G, s, true));
+    if (st) return st;
+    return from_cuda(launch_splitk_reduce(P, y, S, (long long)M * G * N, s));
+}
+
 int bsf8_gemm_partials(const void *x, const uint8_t *w8, const uint8_t *exp, float *partials,
                        int M, int N, int K, int G, int split_k, int64_t ldx,
                        bsf8_stream_t stream) {

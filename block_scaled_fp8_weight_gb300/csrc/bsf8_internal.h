@@ -74,9 +74,10 @@ StreamPlan plan_tma(int M, int N, int K, int G, int S, bool partials);
 cudaError_t launch_tma(const StreamPlan &plan, const void *x, long long ldx, const uint8_t *w8,
                        const uint8_t *ex, void *y, float *partials, int M, int N, int K, int G,
                        cudaStream_t stream);
+// rows_exp: exponents per (weight row, 32 columns), [G][N][K/32], instead of per 32 x 32 block
 cudaError_t launch_stream(const StreamPlan &plan, const void *x, long long ldx, const uint8_t *w8,
                           const uint8_t *ex, void *y, float *partials, int M, int N, int K, int G,
-                          cudaStream_t stream);
+                          cudaStream_t stream, bool rows_exp = false);
 
 // Tensor-core kernel (bsf8_umma.cu): 128-row blocks, one split and one token tile (up to 192
 // rows) a block.  With more than one split it writes fp32 partials (the fixed-order reduce
@@ -118,6 +119,11 @@ cudaError_t launch_dequant(const uint8_t *w8, const uint8_t *ex, void *out, int 
                            cudaStream_t stream);
 cudaError_t launch_make_twin(const void *w, uint8_t *w8, uint8_t *ex, uint8_t *ok,
                              int32_t *accepted, int G, int N, int K, cudaStream_t stream);
+// The per-(row, 32-column) scale layout: exponents and flags [G][N][K/32].
+cudaError_t launch_make_twin_rows(const void *w, uint8_t *w8, uint8_t *ex, uint8_t *ok, int32_t *accepted,
+                                  int G, int N, int K, cudaStream_t stream);
+cudaError_t launch_dequant_rows(const uint8_t *w8, const uint8_t *ex, void *out, int G, int N, int K,
+                                cudaStream_t stream);
 cudaError_t launch_pad_k(const uint8_t *w8, const uint8_t *ex, uint8_t *w8_out, uint8_t *ex_out,
                          int G, int N, int K, int Kp, int pad_exp, cudaStream_t stream);
 cudaError_t launch_pad_x(const void *x, long long ldx, void *x_out, int M, int G, int K, int Kp,

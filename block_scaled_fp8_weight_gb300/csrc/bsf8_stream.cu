@@ -119,17 +119,23 @@ struct XBuf {
 // word straight into its MMAs.  mxa / mxb collect the largest rebuilt magnitude of rows r /
 // r+8: an e4m3 NaN code rebuilds to the pattern 0x07F0, above every finite code's 0x07E0
 // (448 * 2^-120), so the task's rows holding one are set to NaN once, at the end.
-template <int NT8, bool TWO>
+// ROWS: xb.e holds the exponent bytes of rows r (bits 0..7) and r + 8 (bits 8..15), the
+// per-(row, 32-column) scale layout; else one byte for the thread's 32 x 32 block.
+template <int NT8, bool TWO, bool ROWS>
 __device__ __forceinline__ void compute_step(const uint8_t *stage, int r, int q, const XBuf<NT8> &xb,
                                              float (&acc)[StepCfg<NT8>::ACC][NT8][4],
                                              uint32_t &mxa, uint32_t &mxb) {
     using C = StepCfg<NT8>;
-    const Scale sc = make_scale(xb.e);
-    uint32_t s1 = sc.s1, s2 = sc.s2;
+    const uint32_t ea = ROWS ? (xb.e & 0xFFu) : xb.e, eb = ROWS ? (xb.e >> 8) : xb.e;
+    uint32_t s1a, s2a = 0, s1b, s2b = 0;
     if (TWO) {  // exact for every exponent byte: restore e4m3 * 1, then scale by 2^(e-127)
-        s1 = 0x7B807B80u;
-        const uint32_t b = xb.e == 0 ? 0x0040u : (xb.e << 7);
-        s2 = b | (b << 16);
+        s1a = s1b = 0x7B807B80u;
+        const uint32_t ba = ea == 0 ? 0x0040u : (ea << 7), bb = eb == 0 ? 0x0040u : (eb << 7);
+        s2a = ba | (ba << 16);
+        s2b = bb | (bb << 16);
+    } else {
+        s1a = make_scale(ea).s1;
+        s1b = ROWS ? make_scale(eb).s1 : s1a;
     }
 #pragma unroll
     for (int v = 0; v < C::WV; ++v) {
@@ -143,13 +149,13 @@ __device__ __forceinline__ void compute_step(const uint8_t *stage, int r, int q,
             spread4(i == 0 ? b.x : i == 1 ? b.y : i == 2 ? b.z : b.w, u0, u1);
             mxa = bf16x2_max_abs(mxa, bf16x2_max_abs(t0, t1));
             mxb = bf16x2_max_abs(mxb, bf16x2_max_abs(u0, u1));
-            uint32_t alo = bf16x2_mul(t0, s1), ahi = bf16x2_mul(t1, s1);
-            uint32_t blo = bf16x2_mul(u0, s1), bhi = bf16x2_mul(u1, s1);
+            uint32_t alo = bf16x2_mul(t0, s1a), ahi = bf16x2_mul(t1, s1a);
+            uint32_t blo = bf16x2_mul(u0, s1b), bhi = bf16x2_mul(u1, s1b);
             if (TWO) {
-                alo = bf16x2_mul(alo, s2);
-                ahi = bf16x2_mul(ahi, s2);
-                blo = bf16x2_mul(blo, s2);
-                bhi = bf16x2_mul(bhi, s2);
+                alo = bf16x2_mul(alo, s2a);
+                ahi = bf16x2_mul(ahi, s2a);
+                blo = bf16x2_mul(blo, s2b);
+                bhi = bf16x2_mul(bhi, s2b);
             }
 #pragma unroll
             for (int t = 0; t < NT8; ++t) {
@@ -233,7 +239,7 @@ __device__ __forceinline__ void group_epilogue(const StreamParams &p, float (*re
     }
 }
 
-template <int NT8>
+template <int NT8, bool ROWS>
 __global__ void __launch_bounds__(kStreamThreads, NT8 <= 2 ? 2 : 1)
     stream_kernel(const __grid_constant__ StreamParams p) {
     using C = StepCfg<NT8>;
@@ -350,7 +356,8 @@ __global__ void __launch_bounds__(kStreamThreads, NT8 <= 2 ? 2 : 1)
         const int m = min(mbase + t * 8 + r, p.M - 1);
         xsrc[t] = p.x + (size_t)m * p.ldx + (size_t)g * p.K + k0 + q * C::TC;
     }
-    const size_t ebase = (size_t)g * (p.N / 32) * (p.K / 32) + (size_t)((k0 + q * C::TC) / 32);
+    // exponent bytes: one per 32 x 32 block, or (ROWS) one per weight row and 32 columns
+    const size_t ebase = (size_t)g * (ROWS ? p.N : p.N / 32) * (p.K / 32) + (size_t)((k0 + q * C::TC) / 32);
     auto load_x = [&](XBuf<NT8> &xb, int gi, int t) {
         const int slab = slab0 + gi * slab_step;
         if (active && gi < ngroups && slab < nslabs && k0 + t * C::KS + q * C::TC < k1) {
@@ -358,20 +365,26 @@ __global__ void __launch_bounds__(kStreamThreads, NT8 <= 2 ? 2 : 1)
             for (int tt = 0; tt < NT8; ++tt)
 #pragma unroll
                 for (int v = 0; v < C::XV; ++v) xb.v[tt][v] = ldg_v4(xsrc[tt] + t * C::KS + 8 * v);
-            xb.e = ldg_u8(p.ex + ebase + (size_t)(slab / 2) * (p.K / 32) + t * (C::KS / 32));
+            if (ROWS) {
+                const uint8_t *ea = p.ex + ebase + (size_t)(slab * 16 + r) * (p.K / 32) + t * (C::KS / 32);
+                xb.e = ldg_u8(ea) | (ldg_u8(ea + (size_t)8 * (p.K / 32)) << 8);
+            } else {
+                xb.e = ldg_u8(p.ex + ebase + (size_t)(slab / 2) * (p.K / 32) + t * (C::KS / 32));
+            }
         } else {
 #pragma unroll
             for (int tt = 0; tt < NT8; ++tt)
 #pragma unroll
                 for (int v = 0; v < C::XV; ++v) xb.v[tt][v] = make_uint4(0, 0, 0, 0);
-            xb.e = 127;
+            xb.e = ROWS ? (127u | (127u << 8)) : 127u;
         }
     };
     auto compute = [&](const uint8_t *st, const XBuf<NT8> &cur) {
-        if (__any_sync(0xFFFFFFFFu, cur.e > 134u))
-            compute_step<NT8, true>(st, r, q, cur, acc, mxa, mxb);
+        const uint32_t emax = ROWS ? max(cur.e & 0xFFu, cur.e >> 8) : cur.e;
+        if (__any_sync(0xFFFFFFFFu, emax > 134u))
+            compute_step<NT8, true, ROWS>(st, r, q, cur, acc, mxa, mxb);
         else
-            compute_step<NT8, false>(st, r, q, cur, acc, mxa, mxb);
+            compute_step<NT8, false, ROWS>(st, r, q, cur, acc, mxa, mxb);
     };
 
     XBuf<NT8> xa, xb;
@@ -480,7 +493,7 @@ StreamPlan plan_stream_ks(int M, int N, int K, int G, int S, bool partials, int 
 }
 
 namespace {
-template <int NT8>
+template <int NT8, bool ROWS>
 cudaError_t launch_stream_nt8(const StreamPlan &pl, const StreamParams &prm, cudaStream_t stream,
                               const Options &opt) {
     cudaLaunchConfig_t cfg = {};
@@ -493,7 +506,7 @@ cudaError_t launch_stream_nt8(const StreamPlan &pl, const StreamParams &prm, cud
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!__atomic_load_n(&configured[dev], __ATOMIC_ACQUIRE)) {
-        e = cudaFuncSetAttribute(stream_kernel<NT8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(stream_kernel<NT8, ROWS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
         if (e != cudaSuccess) return e;
         __atomic_store_n(&configured[dev], 1, __ATOMIC_RELEASE);
@@ -507,7 +520,7 @@ cudaError_t launch_stream_nt8(const StreamPlan &pl, const StreamParams &prm, cud
             int sms = 0, per_sm = 0;
             e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
             if (e != cudaSuccess) return e;
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stream_kernel<NT8>, kStreamThreads, smem);
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stream_kernel<NT8, ROWS>, kStreamThreads, smem);
             if (e != cudaSuccess) return e;
             c = std::max(1, sms * std::max(1, per_sm));
             __atomic_store_n(&cap[dev], c, __ATOMIC_RELEASE);
@@ -531,13 +544,13 @@ cudaError_t launch_stream_nt8(const StreamPlan &pl, const StreamParams &prm, cud
     }
     cfg.attrs = attrs;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, stream_kernel<NT8>, prm);
+    return cudaLaunchKernelEx(&cfg, stream_kernel<NT8, ROWS>, prm);
 }
 }  // namespace
 
 cudaError_t launch_stream(const StreamPlan &pl, const void *x, long long ldx, const uint8_t *w8,
                           const uint8_t *ex, void *y, float *partials, int M, int N, int K, int G,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, bool rows_exp) {
     const Options opt = options();
     StreamParams prm;
     prm.x = static_cast<const uint16_t *>(x);
@@ -559,11 +572,17 @@ cudaError_t launch_stream(const StreamPlan &pl, const void *x, long long ldx, co
     prm.spl = pl.spl;
     prm.cps = pl.cps;
     prm.mode = pl.mode;
+    if (rows_exp) switch (pl.nt8) {
+            case 1: return launch_stream_nt8<1, true>(pl, prm, stream, opt);
+            case 2: return launch_stream_nt8<2, true>(pl, prm, stream, opt);
+            case 3: return launch_stream_nt8<3, true>(pl, prm, stream, opt);
+            default: return launch_stream_nt8<4, true>(pl, prm, stream, opt);
+        }
     switch (pl.nt8) {
-        case 1: return launch_stream_nt8<1>(pl, prm, stream, opt);
-        case 2: return launch_stream_nt8<2>(pl, prm, stream, opt);
-        case 3: return launch_stream_nt8<3>(pl, prm, stream, opt);
-        default: return launch_stream_nt8<4>(pl, prm, stream, opt);
+        case 1: return launch_stream_nt8<1, false>(pl, prm, stream, opt);
+        case 2: return launch_stream_nt8<2, false>(pl, prm, stream, opt);
+        case 3: return launch_stream_nt8<3, false>(pl, prm, stream, opt);
+        default: return launch_stream_nt8<4, false>(pl, prm, stream, opt);
     }
 }
 

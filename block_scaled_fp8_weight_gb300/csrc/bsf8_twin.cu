@@ -162,9 +162,92 @@ cudaError_t launch_make_twin(const void *w, uint8_t *w8, uint8_t *ex, uint8_t *o
     return e;
 }
 
+// ----------------------------------------------------- make_twin, 1 x 32 blocks
+// The per-(row, 32-column) scale layout of the adapter table's draft_main_proj row: the
+// same rule as make_twin with the block narrowed to one row of 32 columns; exponents and
+// flags [G][N][K/32].  One thread a segment (64 bytes of bf16 in, 32 codes out), so a
+// warp's loads cover 2 KB of consecutive columns.
+__global__ void __launch_bounds__(256) make_twin_rows_kernel(const uint16_t *__restrict__ w,
+                                                             uint8_t *__restrict__ w8,
+                                                             uint8_t *__restrict__ ex,
+                                                             uint8_t *__restrict__ ok,
+                                                             int32_t *__restrict__ accepted,
+                                                             long long nseg) {
+    pdl_trigger();
+    pdl_wait();
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long sg = (long long)blockIdx.x * blockDim.x + threadIdx.x; sg < nseg; sg += stride) {
+        const uint16_t *src = w + sg * 32;
+        uint32_t v[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(src + 8 * i);
+            v[4 * i + 0] = u.x; v[4 * i + 1] = u.y; v[4 * i + 2] = u.z; v[4 * i + 3] = u.w;
+        }
+        uint32_t amax = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = max(amax, max(v[i] & 0x7FFFu, (v[i] >> 16) & 0x7FFFu));
+        uint4 *dst = reinterpret_cast<uint4 *>(w8 + sg * 32);
+        if (amax >= 0x7F80u) {  // Inf or NaN in the segment
+            const uint4 nanq = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+            dst[0] = nanq;
+            dst[1] = nanq;
+            ex[sg] = 0xFF;
+            if (ok) ok[sg] = 0;
+            *accepted = 0;
+            continue;
+        }
+        int E, f;
+        if (amax < 0x0080u) {  // below 2^-126: the 2^-126 floor
+            E = -126;
+            f = 0;
+        } else {
+            E = (int)(amax >> 7) - 127;
+            f = (int)(amax & 0x7Fu);
+        }
+        int e = E - 8 + (f > 0x60 ? 1 : 0);
+        e = min(127, max(-127, e));
+        const float inv = __uint_as_float((uint32_t)(127 - e) << 23);
+        const Scale sc = make_scale((uint32_t)(e + 127));
+        uint32_t codes[8];
+        bool good = true;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t p0 = v[2 * i], p1 = v[2 * i + 1];
+            const float f0 = __uint_as_float(p0 << 16) * inv;
+            const float f1 = __uint_as_float(p0 & 0xFFFF0000u) * inv;
+            const float f2 = __uint_as_float(p1 << 16) * inv;
+            const float f3 = __uint_as_float(p1 & 0xFFFF0000u) * inv;
+            const uint32_t c = (uint32_t)cvt_e4m3x2(f1, f0) | ((uint32_t)cvt_e4m3x2(f3, f2) << 16);
+            codes[i] = c;
+            uint32_t lo, hi;
+            rebuild4(c, sc, lo, hi);
+            good = good && bf16_pair_equal(lo, p0) && bf16_pair_equal(hi, p1);
+        }
+        dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+        dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+        ex[sg] = (uint8_t)(e + 127);
+        if (ok) ok[sg] = good ? 1 : 0;
+        if (!good) *accepted = 0;
+    }
+}
+
+cudaError_t launch_make_twin_rows(const void *w, uint8_t *w8, uint8_t *ex, uint8_t *ok, int32_t *accepted,
+                                  int G, int N, int K, cudaStream_t stream) {
+    cudaError_t e = launch_pdl(set_i32_kernel, 1, 1, stream, accepted, 1);
+    if (e != cudaSuccess) return e;
+    const long long nseg = (long long)G * N * (K / 32);
+    if (nseg > 0)
+        e = launch_pdl(make_twin_rows_kernel, grid_for(nseg, 256), 256, stream, static_cast<const uint16_t *>(w),
+                       w8, ex, ok, accepted, nseg);
+    return e;
+}
+
 // -------------------------------------------------------------------- dequant
 // One thread per 16 codes of a row: out = bf16(e4m3 * 2^(e-127)) via rebuild4 (the
 // same rebuild the GEMM runs in registers), NaN codes patched to NaN.
+// ROWS: one exponent byte per (row, 32 columns), [G][N][K/32]; else per 32 x 32 block.
+template <bool ROWS>
 __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict__ w8,
                                                       const uint8_t *__restrict__ ex,
                                                       uint16_t *__restrict__ out, int K,
@@ -177,7 +260,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict_
         const long long byte = c * 16;
         const long long row = byte / K;  // g * N + n
         const int k = (int)(byte - row * K);
-        const uint32_t e = ex[(size_t)(row / 32) * kb + k / 32];
+        const uint32_t e = ex[(size_t)(ROWS ? row : row / 32) * kb + k / 32];
         const Scale sc = make_scale(e);
         const uint4 q = *reinterpret_cast<const uint4 *>(w8 + byte);
         const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
@@ -197,8 +280,17 @@ cudaError_t launch_dequant(const uint8_t *w8, const uint8_t *ex, void *out, int 
                            cudaStream_t stream) {
     const long long chunks = (long long)G * N * K / 16;
     if (chunks > 0)
-        return launch_pdl(dequant_kernel, grid_for(chunks, 256), 256, stream, w8, ex, static_cast<uint16_t *>(out),
-                          K, chunks);
+        return launch_pdl(dequant_kernel<false>, grid_for(chunks, 256), 256, stream, w8, ex,
+                          static_cast<uint16_t *>(out), K, chunks);
+    return cudaSuccess;
+}
+
+cudaError_t launch_dequant_rows(const uint8_t *w8, const uint8_t *ex, void *out, int G, int N, int K,
+                                cudaStream_t stream) {
+    const long long chunks = (long long)G * N * K / 16;
+    if (chunks > 0)
+        return launch_pdl(dequant_kernel<true>, grid_for(chunks, 256), 256, stream, w8, ex,
+                          static_cast<uint16_t *>(out), K, chunks);
     return cudaSuccess;
 }
 

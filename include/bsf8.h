@@ -174,6 +174,29 @@ int bsf8_splitk_reduce(const float *partials, void *y, int S, int64_t count,
 int bsf8_splitk_reduce_f32(const float *partials, float *y, int S, int64_t count,
                            bsf8_stream_t stream);
 
+/* ------------------------------------- per-(row, 32-column) scales (1 x 32 blocks)
+ * The adapter table of "docs/tp4-adapters.md" (draft_main_proj): e4m3 codes with one
+ * power-of-two scale per (weight row, 32 columns), checked to reproduce the bf16 weight
+ * exactly, for the draft's projection of up to 16 rows.  The pages give no formula for it;
+ * these entry points take make_twin's rule with the block narrowed to 1 x 32.  Layouts as
+ * above except the exponents (and make_twin_rows' flags): exp[G][N][K/32], byte e + 127.
+ *   bsf8_make_twin_rows: as bsf8_make_twin, per 1 x 32 segment.
+ *   bsf8_dequant_rows:   as bsf8_dequant with the per-row exponents.
+ *   bsf8_gemm_rows:      as bsf8_gemm (same x, y, split rule and fixed-order sum) with the
+ *                        per-row exponents, on the cp.async streaming kernel (every M up to
+ *                        BSF8_MAX_M; meant for the pages' <= 16 rows); workspace per
+ *                        bsf8_gemm_rows_workspace_bytes (0 unless a slab needs more than
+ *                        64 column tasks).
+ * Errors as the block-scale counterparts. */
+int bsf8_make_twin_rows(const void *w, uint8_t *w8, uint8_t *exp, uint8_t *block_ok,
+                        int32_t *accepted, int G, int N, int K, bsf8_stream_t stream);
+int bsf8_dequant_rows(const uint8_t *w8, const uint8_t *exp, void *out, int G, int N, int K,
+                      bsf8_stream_t stream);
+size_t bsf8_gemm_rows_workspace_bytes(int M, int N, int K, int G, int split_k);
+int bsf8_gemm_rows(const void *x, const uint8_t *w8, const uint8_t *exp, void *y, int M,
+                   int N, int K, int G, int split_k, int64_t ldx, void *workspace,
+                   size_t workspace_bytes, bsf8_stream_t stream);
+
 /* --------------------------------------------------- GEMM without a workspace
  * The pages have no counterpart for this entry point; it serves callers that cannot
  * allocate device memory for a workspace -- e.g. a serving engine that has reserved all of
