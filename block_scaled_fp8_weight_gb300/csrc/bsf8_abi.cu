@@ -197,6 +197,24 @@ inline cudaError_t launch_call(const Call &c, const void *x, long long ldx, cons
     }
 }
 
+// The per-row-scale GEMM runs on the decode-ahead kernel where the block layout's small
+// calls do (M <= 8, its grid within two blocks an SM), else on the streaming kernel.
+struct RowsCall {
+    bool lowm;
+    StreamPlan sp;
+};
+
+inline RowsCall plan_rows(int M, int N, int K, int G, int S) {
+    RowsCall c{};
+    if (M <= 8) {
+        c.sp = plan_lowm(M, N, K, G, S, false);
+        c.lowm = (long long)c.sp.grid_x * G <= 2LL * sm_count();
+        if (c.lowm) return c;
+    }
+    c.sp = plan_stream(M, N, K, G, S, false);
+    return c;
+}
+
 }  // namespace
 
 extern "C" {
@@ -300,8 +318,8 @@ int bsf8_dequant_rows(const uint8_t *w8, const uint8_t *exp, void *out, int G, i
 
 size_t bsf8_gemm_rows_workspace_bytes(int M, int N, int K, int G, int split_k) {
     if (check_gnk(G, N, K) || M < 1 || M > BSF8_MAX_M || split_k < 0 || split_k > K / 32) return 0;
-    const int S = split_k == 0 ? auto_split(M, N, K, G) : split_k;
-    if (plan_stream(M, N, K, G, S, false).mode != kStreamPartials) return 0;
+    const int S = split_k == 0 ? (M <= 8 ? 1 : auto_split(M, N, K, G)) : split_k;
+    if (plan_rows(M, N, K, G, S).sp.mode != kStreamPartials) return 0;
     return (size_t)S * M * G * N * sizeof(float);
 }
 
@@ -309,16 +327,19 @@ int bsf8_gemm_rows(const void *x, const uint8_t *w8, const uint8_t *exp, void *y
                    int split_k, int64_t ldx, void *workspace, size_t workspace_bytes, bsf8_stream_t stream) {
     int st = check_gemm_args(x, w8, exp, y, M, N, K, G, split_k, ldx);
     if (st) return st;
-    const int S = split_k == 0 ? auto_split(M, N, K, G) : split_k;
+    const int S = split_k == 0 ? (M <= 8 ? 1 : auto_split(M, N, K, G)) : split_k;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const StreamPlan pl = plan_stream(M, N, K, G, S, false);
-    if (pl.mode != kStreamPartials)
-        return from_cuda(launch_stream(pl, x, ldx, w8, exp, y, nullptr, M, N, K, G, s, true));
+    const RowsCall c = plan_rows(M, N, K, G, S);
+    auto launch = [&](void *yy, float *P) {
+        return c.lowm ? launch_lowm(c.sp, x, ldx, w8, exp, yy, P, M, N, K, G, s, true)
+                      : launch_stream(c.sp, x, ldx, w8, exp, yy, P, M, N, K, G, s, true);
+    };
+    if (c.sp.mode != kStreamPartials) return from_cuda(launch(y, nullptr));
     const size_t need = (size_t)S * M * G * N * sizeof(float);
     if (!workspace || workspace_bytes < need) return BSF8_ERR_WORKSPACE;
     if (!aligned16(workspace)) return BSF8_ERR_ALIGN;
     float *P = static_cast<float *>(workspace);
-    st = from_cuda(launch_stream(pl, x, ldx, w8, exp, nullptr, P, M, N, K, G, s, true));
+    st = from_cuda(launch(nullptr, P));
     if (st) return st;
     return from_cuda(launch_splitk_reduce(P, y, S, (long long)M * G * N, s));
 }

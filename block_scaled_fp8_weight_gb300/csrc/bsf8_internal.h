@@ -67,7 +67,7 @@ StreamPlan plan_stream_ks(int M, int N, int K, int G, int S, bool partials, int 
 StreamPlan plan_lowm(int M, int N, int K, int G, int S, bool partials);
 cudaError_t launch_lowm(const StreamPlan &plan, const void *x, long long ldx, const uint8_t *w8,
                         const uint8_t *ex, void *y, float *partials, int M, int N, int K, int G,
-                        cudaStream_t stream);
+                        cudaStream_t stream, bool rows_exp = false);
 
 // TMA-fed kernel (bsf8_tma.cu) for up to 16 token rows per pass; 128-column steps.
 StreamPlan plan_tma(int M, int N, int K, int G, int S, bool partials);

@@ -246,9 +246,11 @@ __device__ __forceinline__ BoxOffs box_offsets(int r, int q) {
 // (row r+8, same), where col c means column 32q + c of the step.  mxa / mxb keep the
 // largest rebuilt magnitude of rows r / r+8 before scaling (an e4m3 NaN code spreads to
 // 0x07F0, above every finite code's 0x07E0).
-template <bool TWO>
+// e: the exponent byte of the thread's block; with ROWS (one exponent per weight row and 32
+// columns) e is row r's and eb row r+8's.
+template <bool TWO, bool ROWS>
 __device__ __forceinline__ void decode_box(const uint8_t *box, const BoxOffs &o, bool mine,
-                                           uint32_t e, uint32_t (&a)[32], uint32_t &mxa,
+                                           uint32_t e, uint32_t eb, uint32_t (&a)[32], uint32_t &mxa,
                                            uint32_t &mxb) {
     uint4 ra[2], rb[2];
     if (mine) {
@@ -259,14 +261,18 @@ __device__ __forceinline__ void decode_box(const uint8_t *box, const BoxOffs &o,
     } else {
         ra[0] = ra[1] = rb[0] = rb[1] = make_uint4(0, 0, 0, 0);
     }
-    uint32_t s1, s2 = 0;
+    uint32_t s1, s2 = 0, s1b, s2b = 0;
     if (TWO) {  // exact for every exponent byte: restore e4m3 * 1, then scale by 2^(e-127)
-        s1 = 0x7B807B80u;
+        s1 = s1b = 0x7B807B80u;
         const uint32_t bb = e == 0 ? 0x0040u : (e << 7);
         s2 = bb | (bb << 16);
+        const uint32_t b8 = eb == 0 ? 0x0040u : (eb << 7);
+        s2b = ROWS ? (b8 | (b8 << 16)) : s2;
     } else {    // e <= 134: one multiply by 2^(e-7)
         const uint32_t b = (e + 120u) << 7;
         s1 = b | (b << 16);
+        const uint32_t b8 = (eb + 120u) << 7;
+        s1b = ROWS ? (b8 | (b8 << 16)) : s1;
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -278,12 +284,12 @@ __device__ __forceinline__ void decode_box(const uint8_t *box, const BoxOffs &o,
         mxa = max_xorsign_abs(mxa, max_xorsign_abs(t0, t1));
         mxb = max_xorsign_abs(mxb, max_xorsign_abs(u0, u1));
         uint32_t alo = bf16x2_mul(t0, s1), ahi = bf16x2_mul(t1, s1);
-        uint32_t blo = bf16x2_mul(u0, s1), bhi = bf16x2_mul(u1, s1);
+        uint32_t blo = bf16x2_mul(u0, s1b), bhi = bf16x2_mul(u1, s1b);
         if (TWO) {
             alo = bf16x2_mul(alo, s2);
             ahi = bf16x2_mul(ahi, s2);
-            blo = bf16x2_mul(blo, s2);
-            bhi = bf16x2_mul(bhi, s2);
+            blo = bf16x2_mul(blo, s2b);
+            bhi = bf16x2_mul(bhi, s2b);
         }
         a[4 * j + 0] = alo;
         a[4 * j + 1] = blo;
@@ -355,6 +361,7 @@ __device__ __forceinline__ void partials_epilogue(const LowParams &p, float (*re
 // One barrier covers all of a warp's boxes: the copies complete in one transaction count,
 // far faster than a barrier per box.  x goes through the load/store path, not the TMA unit,
 // so the post-wait copies of all 8 warps run in parallel.
+template <bool ROWS>
 __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant__ LowParams p) {
     extern __shared__ uint8_t dyn_smem[];
     // the swizzled boxes need 1024-byte alignment
@@ -422,7 +429,26 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
             ? (uint32_t)__ldg(p.ex + (size_t)g * (p.N / 32) * (p.K / 32) +
                               (size_t)(slab / 2) * (p.K / 32) + me.k0 / 32 + lane)
             : 127u;
-    const bool two = __any_sync(0xFFFFFFFFu, ereg > 134u);
+    // ROWS: the exponents of rows r and r+8 at this thread's block of each step (byte t)
+    uint32_t era = 0x7F7F7F7Fu, erb = 0x7F7F7F7Fu;
+    if (ROWS && slab_ok) {
+        const uint8_t *e0 = p.ex + ((size_t)g * p.N + (size_t)slab * 16 + r) * (p.K / 32) + me.k0 / 32;
+        era = erb = 0;
+#pragma unroll
+        for (int t = 0; t < kMaxKt / kKS; ++t) {
+            const int blk = 4 * t + q;
+            const uint32_t ea = blk < nkb ? (uint32_t)__ldg(e0 + blk) : 127u;
+            const uint32_t eb = blk < nkb ? (uint32_t)__ldg(e0 + (size_t)8 * (p.K / 32) + blk) : 127u;
+            era |= ea << (8 * t);
+            erb |= eb << (8 * t);
+        }
+    }
+    uint32_t emax = ereg;
+    if (ROWS) {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) emax = max(emax, max((era >> (8 * t)) & 0xFFu, (erb >> (8 * t)) & 0xFFu));
+    }
+    const bool two = __any_sync(0xFFFFFFFFu, emax > 134u);
     const BoxOffs bo = box_offsets(r, q);
 
     // ---- before the wait: rebuild every step into tensor memory
@@ -439,12 +465,14 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
     for (int t = 0; t < nst; ++t) {
         const int col = me.k0 + t * kKS;
         const bool mine = !err && slab_ok && col + q * 32 < me.k1;
-        const uint32_t e = __shfl_sync(0xFFFFFFFFu, ereg, (4 * t + q) & 31);
+        const uint32_t eblk = __shfl_sync(0xFFFFFFFFu, ereg, (4 * t + q) & 31);
+        const uint32_t e = ROWS ? (era >> (8 * t)) & 0xFFu : eblk;
+        const uint32_t eb = ROWS ? (erb >> (8 * t)) & 0xFFu : eblk;
         uint32_t a[32];
         if (two)
-            decode_box<true>(region + t * kSlotBytes, bo, mine, e, a, mxa, mxb);
+            decode_box<true, ROWS>(region + t * kSlotBytes, bo, mine, e, eb, a, mxa, mxb);
         else
-            decode_box<false>(region + t * kSlotBytes, bo, mine, e, a, mxa, mxb);
+            decode_box<false, ROWS>(region + t * kSlotBytes, bo, mine, e, eb, a, mxa, mxb);
         tmem_st32(tbase + 32u * t, a);
     }
     tmem_wait_st();
@@ -660,9 +688,33 @@ StreamPlan plan_lowm(int M, int N, int K, int G, int S, bool partials) {
     return pl;
 }
 
+namespace {
+
+// Shared-memory attributes of one instantiation, set once per device.
+template <bool ROWS>
+cudaError_t configure_lowm(size_t smem) {
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!__atomic_load_n(&configured[dev], __ATOMIC_ACQUIRE)) {
+        e = cudaFuncSetAttribute(lowm_kernel<ROWS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        // two blocks an SM need the largest shared-memory carve-out
+        e = cudaFuncSetAttribute(lowm_kernel<ROWS>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        __atomic_store_n(&configured[dev], 1, __ATOMIC_RELEASE);
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
 cudaError_t launch_lowm(const StreamPlan &pl, const void *x, long long ldx, const uint8_t *w8,
                         const uint8_t *ex, void *y, float *partials, int M, int N, int K, int G,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, bool rows_exp) {
     if (M < 1 || M > 8 || pl.nt8 != 1 || pl.m_chunks != 1 || pl.kt > kMaxKt) return cudaErrorInvalidValue;
     const Options opt = options();
     LowParams prm;
@@ -693,20 +745,8 @@ cudaError_t launch_lowm(const StreamPlan &pl, const void *x, long long ldx, cons
     if (!prm.status) return cudaErrorInvalidSymbol;
 
     const size_t smem = (size_t)kSmemBytes;
-    static int configured[64] = {0};
-    int dev = 0;
-    e = cudaGetDevice(&dev);
+    e = rows_exp ? configure_lowm<true>(smem) : configure_lowm<false>(smem);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!__atomic_load_n(&configured[dev], __ATOMIC_ACQUIRE)) {
-        e = cudaFuncSetAttribute(lowm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        // two blocks an SM need the largest shared-memory carve-out
-        e = cudaFuncSetAttribute(lowm_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 (int)cudaSharedmemCarveoutMaxShared);
-        if (e != cudaSuccess) return e;
-        __atomic_store_n(&configured[dev], 1, __ATOMIC_RELEASE);
-    }
     cudaLaunchConfig_t cfg = {};
     // one group a block: the grid is the plan's (blocks beyond two an SM run in turn)
     cfg.gridDim = dim3((unsigned)pl.grid_x, (unsigned)G, 1);
@@ -729,7 +769,7 @@ cudaError_t launch_lowm(const StreamPlan &pl, const void *x, long long ldx, cons
     }
     cfg.attrs = attrs;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, lowm_kernel, prm);
+    return rows_exp ? cudaLaunchKernelEx(&cfg, lowm_kernel<true>, prm) : cudaLaunchKernelEx(&cfg, lowm_kernel<false>, prm);
 }
 
 }  // namespace bsf8

@@ -183,8 +183,10 @@ int bsf8_splitk_reduce_f32(const float *partials, float *y, int S, int64_t count
  *   bsf8_make_twin_rows: as bsf8_make_twin, per 1 x 32 segment.
  *   bsf8_dequant_rows:   as bsf8_dequant with the per-row exponents.
  *   bsf8_gemm_rows:      as bsf8_gemm (same x, y, split rule and fixed-order sum) with the
- *                        per-row exponents, on the cp.async streaming kernel (every M up to
- *                        BSF8_MAX_M; meant for the pages' <= 16 rows); workspace per
+ *                        per-row exponents, on the decode-ahead kernel for M <= 8 where
+ *                        bsf8_gemm uses it, else on the cp.async streaming kernel (every M
+ *                        up to BSF8_MAX_M; meant for the pages' <= 16 rows); split_k 0 means
+ *                        1 up to 8 rows, else the streaming kernel's choice; workspace per
  *                        bsf8_gemm_rows_workspace_bytes (0 unless a slab needs more than
  *                        64 column tasks).
  * Errors as the block-scale counterparts. */
