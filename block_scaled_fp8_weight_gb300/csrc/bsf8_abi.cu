@@ -90,13 +90,18 @@ constexpr size_t kMaxSmem = 227 * 1024;
 // 8 token rows and at most two blocks an SM.  Larger calls stream (the cp.async kernel
 // sustains more bandwidth once the rebuild can no longer run ahead).  TMA coordinates are
 // 32-bit, so the TMA kernels need G*N < 2^31.
-enum MainKernel { kKernelStream = 0, kKernelTma = 1, kKernelLowM = 2, kKernelUmma = 3, kKernelWide = 4 };
+enum MainKernel {
+    kKernelStream = 0, kKernelTma = 1, kKernelLowM = 2, kKernelUmma = 3, kKernelWide = 4, kKernelAhead = 5
+};
 
 // Above this many token rows the tensor-core kernel (tcgen05) runs: its MMAs are cheap
 // there, while the mma.sync kernels become bound by their MMA issue.  Measured on a GB300:
 // mid-row wo_a (G = 4, 1024 x 4096) at M = 64 takes 14 us against 35 us, at M = 192
 // 23 us against 92 us; at M = 16 the streaming kernel is ahead (9 us against 14 us).
 constexpr int kUmmaMinRows = 24;
+
+// Token rows the decode-ahead tensor-core kernel (bsf8_ahead.cu) serves by default from 9 up.
+constexpr int kAheadMaxRows = 32;
 
 // The split count when the caller leaves it to the library (split_k = 0).  Up to 8 token
 // rows: 1 -- the decode-ahead and streaming kernels cut a split into tasks of at most 512
@@ -134,7 +139,16 @@ inline MainKernel main_kernel(int M, int N, int K, int G, int S, bool partials) 
         case 4: if (M <= 8) return kKernelLowM; break;
         case 5: if (plan_umma(M, N, K, G, S, partials).ok) return kKernelUmma; break;
         case 6: if (plan_wide(M, N, K, G, S, partials).ok) return kKernelWide; break;
+        case 7: if (plan_ahead(M, N, K, G, S, partials).ok) return kKernelAhead; break;
         default: break;
+    }
+    if (M > 8 && M <= kAheadMaxRows) {
+        // 9..32 rows where every 128-row block of the decode-ahead tensor-core plan holds
+        // one block an SM (its cluster of <= 8 tasks a row block): wo_a (G = 2, 1024 x 4096)
+        // at M = 16 takes 5.9 us against 7.5 us streaming, at M = 32 8.9 against 9.5 us for
+        // the tensor-core kernel.
+        const AheadPlan ap = plan_ahead(M, N, K, G, S, partials);
+        if (ap.ok && (long long)ap.grid_x * G <= sm_count()) return kKernelAhead;
     }
     if (M > kUmmaMinRows) return plan_umma(M, N, K, G, S, partials).ok ? kKernelUmma : kKernelStream;
     if (M > 8) {
@@ -160,6 +174,7 @@ struct Call {
     StreamPlan sp;
     UmmaPlan up;
     WidePlan wp;
+    AheadPlan ap;
     bool partials_out;
 };
 
@@ -174,6 +189,10 @@ inline Call plan_call(int M, int N, int K, int G, int S, bool partials) {
         case kKernelWide:
             c.wp = plan_wide(M, N, K, G, S, partials);
             c.partials_out = c.wp.partials;
+            return c;
+        case kKernelAhead:
+            c.ap = plan_ahead(M, N, K, G, S, partials);
+            c.partials_out = c.ap.partials;
             return c;
         case kKernelLowM: c.sp = plan_lowm(M, N, K, G, S, partials); break;
         case kKernelTma: c.sp = plan_tma(M, N, K, G, S, partials); break;
@@ -191,21 +210,30 @@ inline cudaError_t launch_call(const Call &c, const void *x, long long ldx, cons
     switch (c.kernel) {
         case kKernelUmma: return launch_umma(c.up, x, ldx, w8, ex, y, P, M, N, K, G, s);
         case kKernelWide: return launch_wide(c.wp, x, ldx, w8, ex, y, P, M, N, K, G, s);
+        case kKernelAhead: return launch_ahead(c.ap, x, ldx, w8, ex, y, P, M, N, K, G, s);
         case kKernelLowM: return launch_lowm(c.sp, x, ldx, w8, ex, y, P, M, N, K, G, s);
         case kKernelTma: return launch_tma(c.sp, x, ldx, w8, ex, y, P, M, N, K, G, s);
         default: return launch_stream(c.sp, x, ldx, w8, ex, y, P, M, N, K, G, s);
     }
 }
 
-// The per-row-scale GEMM runs on the decode-ahead kernel where the block layout's small
-// calls do (M <= 8, its grid within two blocks an SM), else on the streaming kernel.
+// The per-row-scale GEMM runs where the block layout's calls of the same shape do: on the
+// decode-ahead kernel (M <= 8, its grid within two blocks an SM), on the decode-ahead
+// tensor-core kernel (9..32 rows, its grid within one block an SM; with
+// BSF8_OPT_GEMM_PATH 7 wherever its plan holds), else on the streaming kernel.
 struct RowsCall {
-    bool lowm;
+    bool lowm, ahead;
     StreamPlan sp;
+    AheadPlan ap;
 };
 
 inline RowsCall plan_rows(int M, int N, int K, int G, int S) {
     RowsCall c{};
+    if (options().gemm_path == 7 || (M > 8 && M <= kAheadMaxRows)) {
+        c.ap = plan_ahead(M, N, K, G, S, false);
+        c.ahead = c.ap.ok && (options().gemm_path == 7 || (long long)c.ap.grid_x * G <= sm_count());
+        if (c.ahead) return c;
+    }
     if (M <= 8) {
         c.sp = plan_lowm(M, N, K, G, S, false);
         c.lowm = (long long)c.sp.grid_x * G <= 2LL * sm_count();
@@ -319,7 +347,8 @@ int bsf8_dequant_rows(const uint8_t *w8, const uint8_t *exp, void *out, int G, i
 size_t bsf8_gemm_rows_workspace_bytes(int M, int N, int K, int G, int split_k) {
     if (check_gnk(G, N, K) || M < 1 || M > BSF8_MAX_M || split_k < 0 || split_k > K / 32) return 0;
     const int S = split_k == 0 ? (M <= 8 ? 1 : auto_split(M, N, K, G)) : split_k;
-    if (plan_rows(M, N, K, G, S).sp.mode != kStreamPartials) return 0;
+    const RowsCall c = plan_rows(M, N, K, G, S);
+    if (c.ahead || c.sp.mode != kStreamPartials) return 0;
     return (size_t)S * M * G * N * sizeof(float);
 }
 
@@ -330,6 +359,7 @@ int bsf8_gemm_rows(const void *x, const uint8_t *w8, const uint8_t *exp, void *y
     const int S = split_k == 0 ? (M <= 8 ? 1 : auto_split(M, N, K, G)) : split_k;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const RowsCall c = plan_rows(M, N, K, G, S);
+    if (c.ahead) return from_cuda(launch_ahead(c.ap, x, ldx, w8, exp, y, nullptr, M, N, K, G, s, true));
     auto launch = [&](void *yy, float *P) {
         return c.lowm ? launch_lowm(c.sp, x, ldx, w8, exp, yy, P, M, N, K, G, s, true)
                       : launch_stream(c.sp, x, ldx, w8, exp, yy, P, M, N, K, G, s, true);
@@ -421,7 +451,7 @@ int bsf8_set_option(int option, int64_t value) {
         case BSF8_OPT_WAIT_TIMEOUT_NS: g_opt_timeout_ns.store((long long)value); return BSF8_OK;
         case BSF8_OPT_DEBUG_SKIP_LOADS: g_opt_skip_loads.store(value ? 1 : 0); return BSF8_OK;
         case BSF8_OPT_GEMM_PATH:
-            if (value > 6) return BSF8_ERR_VALUE;
+            if (value > 7) return BSF8_ERR_VALUE;
             g_opt_gemm_path.store((int)value);
             return BSF8_OK;
         default: return BSF8_ERR_VALUE;

@@ -14,7 +14,7 @@ struct Options {
     unsigned long long timeout_ns;
     int skip_loads;
     int gemm_path;  // 0: by shape; 1: TMA-ring; 2: streaming; 3: TMA-fed; 4: decode-ahead;
-                    // 5: tensor-core; 6: wide-weight
+                    // 5: tensor-core; 6: wide-weight; 7: decode-ahead tensor-core
 };
 Options options();
 
@@ -104,6 +104,18 @@ WidePlan plan_wide(int M, int N, int K, int G, int S, bool partials);
 cudaError_t launch_wide(const WidePlan &plan, const void *x, long long ldx, const uint8_t *w8,
                         const uint8_t *ex, void *y, float *partials, int M, int N, int K, int G,
                         cudaStream_t stream);
+
+// Decode-ahead tensor-core kernel (bsf8_ahead.cu) for up to 32 token rows: blocks of 128
+// rows x one task (<= 512 columns of a split), a cluster per 128 rows holding all of their
+// tasks (at most 8), the rebuilt weights in tensor memory before the dependency wait.
+struct AheadPlan {
+    int S, chunk_cols, kt, tps, ntok, nacc, cluster, rows_per_rank, grid_x;
+    bool partials, ok;  // ok: the kernel can run this call (else another kernel)
+};
+AheadPlan plan_ahead(int M, int N, int K, int G, int S, bool partials);
+cudaError_t launch_ahead(const AheadPlan &plan, const void *x, long long ldx, const uint8_t *w8,
+                         const uint8_t *ex, void *y, float *partials, int M, int N, int K, int G,
+                         cudaStream_t stream, bool rows_exp = false);
 
 int auto_split(int M, int N, int K, int G);
 GemmPlan plan_gemm(int M, int N, int K, int G, int S, int mode);

@@ -183,8 +183,9 @@ int bsf8_splitk_reduce_f32(const float *partials, float *y, int S, int64_t count
  *   bsf8_make_twin_rows: as bsf8_make_twin, per 1 x 32 segment.
  *   bsf8_dequant_rows:   as bsf8_dequant with the per-row exponents.
  *   bsf8_gemm_rows:      as bsf8_gemm (same x, y, split rule and fixed-order sum) with the
- *                        per-row exponents, on the decode-ahead kernel for M <= 8 where
- *                        bsf8_gemm uses it, else on the cp.async streaming kernel (every M
+ *                        per-row exponents, on the decode-ahead kernel for M <= 8 and on the
+ *                        decode-ahead tensor-core kernel for 9..32 rows where bsf8_gemm uses
+ *                        them, else on the cp.async streaming kernel (every M
  *                        up to BSF8_MAX_M; meant for the pages' <= 16 rows); split_k 0 means
  *                        1 up to 8 rows, else the streaming kernel's choice; workspace per
  *                        bsf8_gemm_rows_workspace_bytes (0 unless a slab needs more than
@@ -257,21 +258,29 @@ enum {
     BSF8_OPT_WAIT_TIMEOUT_NS = 2,  /* bound of every in-kernel wait (default 2e9 ns)   */
     BSF8_OPT_DEBUG_SKIP_LOADS = 3, /* test only: the TMA-ring GEMM issues no weight    */
                                    /* loads, so its waits run out (BSF8_ERR_TIMEOUT)   */
-    BSF8_OPT_GEMM_PATH = 4         /* 0 (default): the kernel chosen by shape -- the    */
-                                   /* decode-ahead kernel up to 8 token rows (when its */
-                                   /* grid fits two blocks an SM), the tensor-core     */
-                                   /* kernel for 9..16 rows at split_k 1 over at least */
-                                   /* one 128-row block per SM and beyond 24 rows, the */
-                                   /* wide-weight kernel up to 8 rows at split_k 1     */
-                                   /* where the decode-ahead grid does not fit, the    */
-                                   /* cp.async streaming                               */
-                                   /* kernel otherwise; 1: the shared-memory TMA-ring  */
-                                   /* kernel (split_k <= 8); 2: the streaming kernel;  */
-                                   /* 3: the TMA-fed kernel (M <= 16); 4: the decode-  */
-                                   /* ahead kernel (M <= 8); 5: the tensor-core        */
-                                   /* (tcgen05) kernel (M <= 192); 6: the wide-weight  */
-                                   /* kernel (M <= 8; K and the split's columns        */
-                                   /* multiples of 128, at most 6144 columns a split). */
+    BSF8_OPT_GEMM_PATH = 4         /* 0 (default): the kernel chosen by shape:         */
+                                   /*  - up to 8 token rows: the decode-ahead kernel   */
+                                   /*    when its grid fits two blocks an SM, else the */
+                                   /*    wide-weight kernel at split_k 1, else the     */
+                                   /*    cp.async streaming kernel;                    */
+                                   /*  - 9..32 rows: the decode-ahead tensor-core      */
+                                   /*    kernel when its plan holds (S x tasks of at   */
+                                   /*    most 512 columns <= 8) and its grid fits one  */
+                                   /*    block an SM;                                  */
+                                   /*  - else 9..16 rows: the tensor-core kernel at    */
+                                   /*    split_k 1 over at least one 128-row block per */
+                                   /*    SM, the streaming kernel otherwise (up to 24  */
+                                   /*    rows);                                        */
+                                   /*  - beyond 24 rows: the tensor-core kernel.       */
+                                   /* Forced: 1: the shared-memory TMA-ring kernel     */
+                                   /* (split_k <= 8); 2: the streaming kernel; 3: the  */
+                                   /* TMA-fed kernel (M <= 16); 4: the decode-ahead    */
+                                   /* kernel (M <= 8); 5: the tensor-core (tcgen05)    */
+                                   /* kernel (M <= 192 a token tile); 6: the wide-     */
+                                   /* weight kernel (M <= 8; K and the split's columns */
+                                   /* multiples of 128, at most 6144 columns a split); */
+                                   /* 7: the decode-ahead tensor-core kernel (M <= 32, */
+                                   /* S x ceil(split columns / 512) <= 8).             */
                                    /* A forced kernel that does not apply to a call    */
                                    /* falls back to 0.                                 */
 };

@@ -59,12 +59,13 @@ def test_down_proj_padding_leaves_output_bitwise_unchanged(bsf8_lib):
     assert np.array_equal(y6, y7)
 
 
-@pytest.mark.parametrize("path,M", [(0, 4), (3, 12), (1, 4), (0, 40), (6, 4)])
+@pytest.mark.parametrize("path,M", [(0, 4), (3, 12), (1, 4), (0, 40), (6, 4), (7, 4), (7, 20)])
 def test_timeout_is_reported_without_hanging(bsf8_lib, path, M):
     """With the test-only option that suppresses the weight loads, the mbarrier waits of
     the decode-ahead GEMM (path 0 at M = 4), the TMA-fed GEMM (path 3), the TMA-ring GEMM
-    (path 1), the tensor-core GEMM (path 0 at M = 40) and the wide-weight GEMM (path 6)
-    run out after the shortened
+    (path 1), the tensor-core GEMM (path 0 at M = 40), the wide-weight GEMM (path 6) and
+    the decode-ahead tensor-core GEMM (path 7, 16- and 32-token tiles) run out after the
+    shortened
     bound; the kernel records BSF8_ERR_TIMEOUT, writes nothing and returns.  Normal calls
     work again afterwards."""
     w8, ex = wl.TINY.weights()
