@@ -106,9 +106,21 @@ constexpr int kAheadMaxRows = 32;
 // The split count when the caller leaves it to the library (split_k = 0).  Up to 8 token
 // rows: 1 -- the decode-ahead and streaming kernels cut a split into tasks of at most 512
 // (decode-ahead) or ~K/8 columns anyway, and more splits only add partial sums (measured:
-// down_proj 4.0 us at one split against 5.4 at four).
+// down_proj 4.0 us at one split against 5.4 at four); likewise 1 for 9..32 rows where the
+// decode-ahead tensor-core kernel takes the call in one split.
+inline int sm_count();
+
+// 9..32 rows whose one-split plan on the decode-ahead tensor-core kernel fits one block an
+// SM: that kernel cuts the split into tasks anyway, so more splits would only add partials.
+inline bool ahead_one_split(int M, int N, int K, int G) {
+    if (M <= 8 || M > kAheadMaxRows) return false;
+    const AheadPlan ap = plan_ahead(M, N, K, G, 1, false);
+    return ap.ok && (long long)ap.grid_x * G <= sm_count();
+}
+
 inline int call_auto_split(int M, int N, int K, int G) {
     if (M <= 8) return 1;
+    if (ahead_one_split(M, N, K, G)) return 1;
     if (M > kUmmaMinRows && (long long)G * N < (1LL << 31)) {
         int sms = 0;
         int dev = 0;
@@ -346,7 +358,7 @@ int bsf8_dequant_rows(const uint8_t *w8, const uint8_t *exp, void *out, int G, i
 
 size_t bsf8_gemm_rows_workspace_bytes(int M, int N, int K, int G, int split_k) {
     if (check_gnk(G, N, K) || M < 1 || M > BSF8_MAX_M || split_k < 0 || split_k > K / 32) return 0;
-    const int S = split_k == 0 ? (M <= 8 ? 1 : auto_split(M, N, K, G)) : split_k;
+    const int S = split_k == 0 ? (M <= 8 || ahead_one_split(M, N, K, G) ? 1 : auto_split(M, N, K, G)) : split_k;
     const RowsCall c = plan_rows(M, N, K, G, S);
     if (c.ahead || c.sp.mode != kStreamPartials) return 0;
     return (size_t)S * M * G * N * sizeof(float);
@@ -356,7 +368,7 @@ int bsf8_gemm_rows(const void *x, const uint8_t *w8, const uint8_t *exp, void *y
                    int split_k, int64_t ldx, void *workspace, size_t workspace_bytes, bsf8_stream_t stream) {
     int st = check_gemm_args(x, w8, exp, y, M, N, K, G, split_k, ldx);
     if (st) return st;
-    const int S = split_k == 0 ? (M <= 8 ? 1 : auto_split(M, N, K, G)) : split_k;
+    const int S = split_k == 0 ? (M <= 8 || ahead_one_split(M, N, K, G) ? 1 : auto_split(M, N, K, G)) : split_k;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const RowsCall c = plan_rows(M, N, K, G, S);
     if (c.ahead) return from_cuda(launch_ahead(c.ap, x, ldx, w8, exp, y, nullptr, M, N, K, G, s, true));

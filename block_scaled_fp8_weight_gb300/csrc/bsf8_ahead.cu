@@ -9,8 +9,9 @@
 // _wo_a_mid_kernel() with their fixed-order split-K sums.
 //
 // A block owns 128 weight rows of one group and one task: at most 512 columns inside one
-// split.  A cluster holds every task of its 128 rows (S splits x tps tasks, at most 8
-// blocks), so the split-K sum never leaves the cluster.
+// split.  A cluster holds every task of its 128 rows (S splits x tps tasks, at most 16
+// blocks; past 8 a non-portable cluster size, where the device schedules one), so the
+// split-K sum never leaves the cluster.
 //   before the wait (the weights are static):
 //     * thread 0 loads the task's codes -- up to four 128-row x 128-byte boxes, 128-byte
 //       swizzle -- on one mbarrier;
@@ -63,11 +64,13 @@ constexpr int kSmemABytes = kRowsA * kSmemColsA * 2;    // 32 KB
 constexpr int kTmemColsA = 256;                         // accumulators (64) + A ((kt - 128) / 2)
 constexpr int kAccColsA = 64;                           // 64 / ntok accumulators of ntok columns
 constexpr int kMaxTokA = 32;
-constexpr int kMaxClusterA = 8;
+constexpr int kMaxPortableClusterA = 8;
+constexpr int kMaxClusterA = 16;
 // After the rebuild the codes' room holds the x tile (<= 8 chunks x 32 x 128 bytes) and the
-// gather tiles: [C tasks][L rows][ntok] fp32 partials this block folds, C * ceil(128 / C) <= 133.
+// gather tiles: [C tasks][L rows][ntok] fp32 partials this block folds, C * ceil(128 / C) <= 140
+// for C <= 16.
 constexpr int kXTileBytesA = (kMaxKtA / 64) * kMaxTokA * 128;
-constexpr int kGatherBytesA = 133 * kMaxTokA * 4;
+constexpr int kGatherBytesA = 140 * kMaxTokA * 4;
 constexpr int kSmemBytesA = kMaxBoxesA * kBoxBytesA + kSmemABytes + 1024;
 static_assert(kXTileBytesA + kGatherBytesA <= kMaxBoxesA * kBoxBytesA, "x and gather fit the codes' room");
 static_assert(kTmemColsA >= kAccColsA + (kMaxKtA - kSmemColsA) / 2, "accumulators and A fit");
@@ -595,9 +598,43 @@ cudaError_t configure_ahead() {
         e = cudaFuncSetAttribute(ahead_kernel<ROWS>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(ahead_kernel<ROWS>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
         __atomic_store_n(&configured[dev], 1, __ATOMIC_RELEASE);
     }
     return cudaSuccess;
+}
+
+// Whether clusters of `size` blocks of this kernel can be scheduled on the current device
+// (sizes up to 8 always can; larger ones depend on the GPU's cluster limits).  Asked once
+// per device and size.
+bool cluster_fits(int size) {
+    if (size <= kMaxPortableClusterA) return true;
+    static int known[64][kMaxClusterA + 1] = {};  // 0 unknown, 1 yes, 2 no
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || size > kMaxClusterA) return false;
+    int k = __atomic_load_n(&known[dev][size], __ATOMIC_ACQUIRE);
+    if (k == 0) {
+        k = 2;
+        if (configure_ahead<false>() == cudaSuccess && configure_ahead<true>() == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)size, 1, 1);
+            cfg.blockDim = dim3(kThreadsA, 1, 1);
+            cfg.dynamicSmemBytes = kSmemBytesA;
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = (unsigned)size;
+            attr.val.clusterDim.y = 1;
+            attr.val.clusterDim.z = 1;
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, ahead_kernel<false>, &cfg) == cudaSuccess && n > 0) k = 1;
+            else (void)cudaGetLastError();
+        }
+        __atomic_store_n(&known[dev][size], k, __ATOMIC_RELEASE);
+    }
+    return k == 1;
 }
 
 }  // namespace
@@ -619,6 +656,7 @@ AheadPlan plan_ahead(int M, int N, int K, int G, int S, bool partials) {
     pl.partials = partials;
     pl.ok = pl.cluster <= kMaxClusterA && pl.kt <= kMaxKtA &&
             kAccColsA + std::max(0, pl.kt - kSmemColsA) / 2 <= kTmemColsA;
+    if (pl.ok && pl.cluster > kMaxPortableClusterA) pl.ok = cluster_fits(pl.cluster);
     return pl;
 }
 

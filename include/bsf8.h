@@ -141,9 +141,11 @@ int bsf8_gemm(const void *x, const uint8_t *w8, const uint8_t *exp, void *y,
 size_t bsf8_gemm_workspace_bytes(int M, int N, int K, int G, int split_k);
 
 /* The split count bsf8_gemm uses for split_k = 0.  Returns a value in 1 .. K/32, or a
- * negative status for invalid sizes.  For M <= 24 it depends on the sizes only (at most
- * 8); for M > 24 (the tensor-core kernel) on the current device's SM count too, and with
- * no device the M <= 24 rule applies. */
+ * negative status for invalid sizes.  1 up to 8 rows, and for 9..32 rows where the
+ * decode-ahead tensor-core kernel takes the call in one split (its one-split grid fits the
+ * device's SMs); otherwise for M <= 24 it depends on the sizes only (at most 8), for M > 24
+ * (the tensor-core kernel) on the current device's SM count too.  With no device the
+ * size-only rule applies. */
 int bsf8_gemm_auto_split(int M, int N, int K, int G);
 
 /* First pass alone: writes the fp32 partials P[S][M][G][N] (S = split_k >= 1, every
@@ -187,7 +189,8 @@ int bsf8_splitk_reduce_f32(const float *partials, float *y, int S, int64_t count
  *                        decode-ahead tensor-core kernel for 9..32 rows where bsf8_gemm uses
  *                        them, else on the cp.async streaming kernel (every M
  *                        up to BSF8_MAX_M; meant for the pages' <= 16 rows); split_k 0 means
- *                        1 up to 8 rows, else the streaming kernel's choice; workspace per
+ *                        1 up to 8 rows and where the decode-ahead tensor-core kernel takes
+ *                        the call in one split, else the streaming kernel's choice; workspace per
  *                        bsf8_gemm_rows_workspace_bytes (0 unless a slab needs more than
  *                        64 column tasks).
  * Errors as the block-scale counterparts. */

@@ -4,7 +4,7 @@ against the CPU oracle.
 A block holds 128 weight rows x at most 512 columns of one split, the first 128 columns'
 weights in shared memory and the rest in tensor memory as the MMA's A operand; a cluster
 holds all tasks of its rows (S splits x tps tasks <= 8) and folds them in split order.
-The cases cover both A sources, clusters of 1 to 8 blocks (3, 5 and 7 included), weight
+The cases cover both A sources, clusters of 1 to 16 blocks (3, 5, 7, 10, 12, 14 included), weight
 rows past N inside a 128-row block, an empty split, every code under every exponent byte,
 NaN codes, per-row exponents and the head-to-toe wo_a shape.  Outputs are held to the
 GEMM's floating-point bar; repeated calls and gemm = reduce(partials) are bitwise equal."""
@@ -23,13 +23,14 @@ AHEAD = 7
 
 def plan_holds(M, K, S):
     """The kernel's plan rule (bsf8_ahead.cu, plan_ahead): tasks of at most 512 columns,
-    S x tasks-per-split blocks in a cluster of at most 8, at most 32 token rows.  Cases
+    S x tasks-per-split blocks in a cluster of at most 16 (past 8 where the GPU schedules
+    such clusters, as a GB300 does), at most 32 token rows.  Cases
     that fail it would silently run on another kernel, so every case asserts it."""
     chunk = -(-(K // 32) // S) * 32
     tps = max(1, -(-chunk // 512))
     kt = -(-(-(-chunk // tps)) // 32) * 32
     ntok = 16 if M <= 16 else 32
-    return 1 <= M <= 32 and S * tps <= 8 and kt <= 512 and 64 + max(0, kt - 128) // 2 <= 256
+    return 1 <= M <= 32 and S * tps <= 16 and kt <= 512 and 64 + max(0, kt - 128) // 2 <= 256
 
 
 def run_ahead(x, w8, ex, S, rows=False):
@@ -87,6 +88,10 @@ def test_one_hot_every_code_and_exponent(bsf8_lib):
     (32, 2, 128, 1024, 8),   # full 32-token tile
     (4, 1, 256, 128, 4),     # tasks of 32 columns: 2 MMAs, fewer than the accumulators
     (4, 1, 256, 160, 4),     # splits of 64 columns: the last one is empty
+    (16, 1, 256, 5120, 1),   # cluster 10 (non-portable): K = 5120 in one split
+    (6, 1, 128, 6144, 1),    # cluster 12
+    (3, 2, 128, 4096, 16),   # cluster 16, tasks of 256
+    (20, 1, 256, 7168, 14),  # cluster 14, rows folded 10 a block (the last block 0)
 ])
 def test_matches_oracle(bsf8_lib, M, G, N, K, S):
     assert plan_holds(M, K, S)
@@ -143,7 +148,7 @@ def test_nan_codes_poison_their_rows(bsf8_lib):
     assert_gemm_close(y[:, :, keep], ref[:, :, keep], "nan codes")
 
 
-@pytest.mark.parametrize("M,S", [(1, 1), (6, 2), (16, 8)])
+@pytest.mark.parametrize("M,S", [(1, 1), (6, 2), (16, 8), (12, 16)])
 def test_rows_exponents(bsf8_lib, M, S):
     """One exponent per weight row and 32 columns ([G, N, K/32]) through the same kernel."""
     r = wl.rng(1301 + M)
