@@ -156,9 +156,9 @@ inline MainKernel main_kernel(int M, int N, int K, int G, int S, bool partials) 
     }
     if (M > 8 && M <= kAheadMaxRows) {
         // 9..32 rows where every 128-row block of the decode-ahead tensor-core plan holds
-        // one block an SM (its cluster of <= 8 tasks a row block): wo_a (G = 2, 1024 x 4096)
+        // one block an SM (its cluster of <= 16 tasks a row block): wo_a (G = 2, 1024 x 4096)
         // at M = 16 takes 5.9 us against 7.5 us streaming, at M = 32 8.9 against 9.5 us for
-        // the tensor-core kernel.
+        // the tensor-core kernel; gate_up (1152 x 5120) at M = 16 5.1 against 8.4.
         const AheadPlan ap = plan_ahead(M, N, K, G, S, partials);
         if (ap.ok && (long long)ap.grid_x * G <= sm_count()) return kKernelAhead;
     }

@@ -34,9 +34,10 @@
 //       fp32 partials).
 // A block takes 256 TMEM columns (accumulators + A) and ~97 KB of shared memory, so two
 // share an SM: the next call's blocks become resident and rebuild while this call
-// finishes.  After the wait a call costs the x round trip, one thread's MMA issue, the
-// accumulator read and the reduction; the mma.sync decode-ahead kernel (bsf8_lowm.cu)
-// spends 8x more MMA instructions there.
+// finishes.  After the wait a call costs the x round trip, the MMA issue (a warp per
+// accumulator), the accumulators' read and the reduction; the mma.sync decode-ahead kernel
+// (bsf8_lowm.cu) spends 8x more MMA instructions there but issues them from all 8 warps,
+// which is still faster up to 8 token rows.
 //
 // Every wait is bounded: on timeout the block records BSF8_ERR_TIMEOUT, stores nothing,
 // lets its copies land and returns.

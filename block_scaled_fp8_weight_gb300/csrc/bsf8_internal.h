@@ -107,7 +107,7 @@ cudaError_t launch_wide(const WidePlan &plan, const void *x, long long ldx, cons
 
 // Decode-ahead tensor-core kernel (bsf8_ahead.cu) for up to 32 token rows: blocks of 128
 // rows x one task (<= 512 columns of a split), a cluster per 128 rows holding all of their
-// tasks (at most 8), the rebuilt weights in tensor memory before the dependency wait.
+// tasks (at most 16), the rebuilt weights in tensor memory before the dependency wait.
 struct AheadPlan {
     int S, chunk_cols, kt, tps, ntok, nacc, cluster, rows_per_rank, grid_x;
     bool partials, ok;  // ok: the kernel can run this call (else another kernel)

@@ -121,7 +121,8 @@ int bsf8_dequant(const uint8_t *w8, const uint8_t *exp, void *out, int G, int N,
  *             slab of 16 rows needs more
  *             than 64 column tasks, e.g. split_k > 64).  No zeroing is needed; it must not
  *             be shared by calls that can overlap.
- * The splits are summed inside one thread block, across a cluster of up to 8 blocks
+ * The splits are summed inside one thread block, across a cluster of up to 8 blocks (16
+ * for the decode-ahead tensor-core kernel, where the device schedules such clusters)
  * through distributed shared memory, or by the fixed-order reduce of a second pass, always
  * in the same fixed order as bsf8_gemm_partials followed by bsf8_splitk_reduce, which give
  * the same bits.
@@ -268,8 +269,9 @@ enum {
                                    /*    cp.async streaming kernel;                    */
                                    /*  - 9..32 rows: the decode-ahead tensor-core      */
                                    /*    kernel when its plan holds (S x tasks of at   */
-                                   /*    most 512 columns <= 8) and its grid fits one  */
-                                   /*    block an SM;                                  */
+                                   /*    most 512 columns <= 16, past 8 where the      */
+                                   /*    device schedules such clusters) and its grid  */
+                                   /*    fits one block an SM;                         */
                                    /*  - else 9..16 rows: the tensor-core kernel at    */
                                    /*    split_k 1 over at least one 128-row block per */
                                    /*    SM, the streaming kernel otherwise (up to 24  */
@@ -283,7 +285,7 @@ enum {
                                    /* weight kernel (M <= 8; K and the split's columns */
                                    /* multiples of 128, at most 6144 columns a split); */
                                    /* 7: the decode-ahead tensor-core kernel (M <= 32, */
-                                   /* S x ceil(split columns / 512) <= 8).             */
+                                   /* S x ceil(split columns / 512) <= 16).            */
                                    /* A forced kernel that does not apply to a call    */
                                    /* falls back to 0.                                 */
 };
