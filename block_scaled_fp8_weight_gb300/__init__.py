@@ -22,12 +22,14 @@ __all__ = [
     "Bsf8Error", "load", "make_twin", "twin_or_none", "dequant", "gemm", "gemm_partials", "gemm_f32", "splitk_reduce_f32", "make_twin_rows", "dequant_rows", "gemm_rows",
     "splitk_reduce", "pad_k", "pad_x", "workspace_bytes", "auto_split", "device_status",
     "set_option", "get_option", "OPT_PDL", "OPT_WAIT_TIMEOUT_NS", "OPT_DEBUG_SKIP_LOADS",
-    "OPT_GEMM_PATH",
+    "OPT_GEMM_PATH", "gemm_kernel", "KERNELS",
     "MAX_M", "STATUS",
 ]
 
 MAX_M = 16384
 OPT_PDL, OPT_WAIT_TIMEOUT_NS, OPT_DEBUG_SKIP_LOADS, OPT_GEMM_PATH = 1, 2, 3, 4
+# bsf8_gemm's kernels (BSF8_KERNEL_*), the values gemm_kernel() returns and OPT_GEMM_PATH forces
+KERNELS = {2: "stream", 4: "decode_ahead", 5: "tensor_core", 6: "wide", 7: "decode_ahead_tc"}
 STATUS = {0: "OK", 1: "ERR_SHAPE", 2: "ERR_ALIGN", 3: "ERR_STRIDE", 4: "ERR_WORKSPACE",
           5: "ERR_NULL", 6: "ERR_CUDA", 7: "ERR_TIMEOUT", 8: "ERR_DEVICE", 9: "ERR_VALUE"}
 
@@ -71,6 +73,8 @@ def load(build_if_missing: bool = True):
             "bsf8_gemm": (I, [P, P, P, P, I, I, I, I, I, I64, P, SZ, P]),
             "bsf8_gemm_workspace_bytes": (SZ, [I, I, I, I, I]),
             "bsf8_gemm_auto_split": (I, [I, I, I, I]),
+            "bsf8_gemm_kernel": (I, [I, I, I, I, I]),
+            "bsf8_gemm_static_scratch": (I, [P, P, P, P, I, I, I, I, I, I64, P]),
             "bsf8_gemm_partials": (I, [P, P, P, P, I, I, I, I, I, I64, P]),
             "bsf8_make_twin_rows": (I, [P, P, P, P, P, I, I, I, P]),
             "bsf8_dequant_rows": (I, [P, P, P, I, I, I, P]),
@@ -246,6 +250,15 @@ def auto_split(M, N, K, G) -> int:
     r = load().bsf8_gemm_auto_split(M, N, K, G)
     if r < 0:
         raise Bsf8Error(-r, "bsf8_gemm_auto_split")
+    return r
+
+
+def gemm_kernel(M, N, K, G, split_k=0) -> int:
+    """The kernel bsf8_gemm runs for these sizes (a KERNELS key); raises when a kernel forced
+    through OPT_GEMM_PATH cannot run the call."""
+    r = load().bsf8_gemm_kernel(M, N, K, G, split_k)
+    if r < 0:
+        raise Bsf8Error(-r, "bsf8_gemm_kernel")
     return r
 
 

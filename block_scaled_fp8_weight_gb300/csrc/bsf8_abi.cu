@@ -82,16 +82,14 @@ inline int check_gemm_args(const void *x, const uint8_t *w8, const uint8_t *exp,
     return BSF8_OK;
 }
 
-constexpr size_t kMaxSmem = 227 * 1024;
-
-// Up to 16 token rows per pass run on the TMA-fed kernel, more on the streaming kernel.
 // Kernel for a call.  The decode-ahead kernel pays off when each of its blocks holds one
 // group of tasks, so that the group's weights are rebuilt before the dependency wait: up to
 // 8 token rows and at most two blocks an SM.  Larger calls stream (the cp.async kernel
 // sustains more bandwidth once the rebuild can no longer run ahead).  TMA coordinates are
-// 32-bit, so the TMA kernels need G*N < 2^31.
+// 32-bit, so the TMA kernels need G*N < 2^31.  The values are those of BSF8_OPT_GEMM_PATH
+// and of bsf8_gemm_kernel.
 enum MainKernel {
-    kKernelStream = 0, kKernelTma = 1, kKernelLowM = 2, kKernelUmma = 3, kKernelWide = 4, kKernelAhead = 5
+    kKernelNone = -1, kKernelStream = 2, kKernelLowM = 4, kKernelUmma = 5, kKernelWide = 6, kKernelAhead = 7
 };
 
 // Above this many token rows the tensor-core kernel (tcgen05) runs: its MMAs are cheap
@@ -103,36 +101,6 @@ constexpr int kUmmaMinRows = 24;
 // Token rows the decode-ahead tensor-core kernel (bsf8_ahead.cu) serves by default from 9 up.
 constexpr int kAheadMaxRows = 32;
 
-// The split count when the caller leaves it to the library (split_k = 0).  Up to 8 token
-// rows: 1 -- the decode-ahead and streaming kernels cut a split into tasks of at most 512
-// (decode-ahead) or ~K/8 columns anyway, and more splits only add partial sums (measured:
-// down_proj 4.0 us at one split against 5.4 at four); likewise 1 for 9..32 rows where the
-// decode-ahead tensor-core kernel takes the call in one split.
-inline int sm_count();
-
-// 9..32 rows whose one-split plan on the decode-ahead tensor-core kernel fits one block an
-// SM: that kernel cuts the split into tasks anyway, so more splits would only add partials.
-inline bool ahead_one_split(int M, int N, int K, int G) {
-    if (M <= 8 || M > kAheadMaxRows) return false;
-    const AheadPlan ap = plan_ahead(M, N, K, G, 1, false);
-    return ap.ok && (long long)ap.grid_x * G <= sm_count();
-}
-
-inline int call_auto_split(int M, int N, int K, int G) {
-    if (M <= 8) return 1;
-    if (ahead_one_split(M, N, K, G)) return 1;
-    if (M > kUmmaMinRows && (long long)G * N < (1LL << 31)) {
-        int sms = 0;
-        int dev = 0;
-        if (cudaGetDevice(&dev) == cudaSuccess &&
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0) {
-            const int S = umma_auto_split(M, N, K, G, sms);
-            if (plan_umma(M, N, K, G, S, false).ok) return S;
-        }
-    }
-    return auto_split(M, N, K, G);
-}
-
 inline int sm_count() {
     static int count[64] = {0};
     int dev = 0;
@@ -143,40 +111,71 @@ inline int sm_count() {
     return c;
 }
 
-inline MainKernel main_kernel(int M, int N, int K, int G, int S, bool partials) {
-    if ((long long)G * N >= (1LL << 31)) return kKernelStream;
-    switch (options().gemm_path) {  // a forced kernel, where it applies
+// 9..32 rows whose one-split plan on the decode-ahead tensor-core kernel fits one block an
+// SM: that kernel cuts the split into tasks anyway, so more splits would only add partials.
+inline bool ahead_one_split(int M, int N, int K, int G) {
+    if (M <= 8 || M > kAheadMaxRows) return false;
+    const AheadPlan ap = plan_ahead(M, N, K, G, 1, false);
+    return ap.ok && (long long)ap.grid_x * G <= sm_count();
+}
+
+// The split count when the caller leaves it to the library (split_k = 0).  Up to 8 token
+// rows: 1 -- the decode-ahead and streaming kernels cut a split into tasks of at most 512
+// (decode-ahead) or ~K/8 columns anyway, and more splits only add partial sums (measured:
+// down_proj 4.0 us at one split against 5.4 at four); likewise 1 for 9..32 rows where the
+// decode-ahead tensor-core kernel takes the call in one split.
+inline int call_auto_split(int M, int N, int K, int G) {
+    if (M <= 8) return 1;
+    if (ahead_one_split(M, N, K, G)) return 1;
+    if (M > kUmmaMinRows && (long long)G * N < (1LL << 31)) {
+        const int sms = sm_count();
+        if (sms > 0) {
+            const int S = umma_auto_split(M, N, K, G, sms);
+            if (plan_umma(M, N, K, G, S, false).ok) return S;
+        }
+    }
+    return auto_split(M, N, K, G);
+}
+
+// The kernel a call of these sizes runs.  It depends on the sizes, the split count and the
+// options only -- not on whether the caller wants y or the fp32 partials -- so that
+// bsf8_gemm and bsf8_gemm_partials + bsf8_splitk_reduce run the same kernel and give the
+// same bits.  A kernel forced through BSF8_OPT_GEMM_PATH that cannot run the call gives
+// kKernelNone (the entry points then return BSF8_ERR_VALUE).
+inline MainKernel main_kernel(int M, int N, int K, int G, int S) {
+    const bool tma_ok = (long long)G * N < (1LL << 31);
+    switch (options().gemm_path) {  // a forced kernel
         case 2: return kKernelStream;
-        case 3: if (M <= 16) return kKernelTma; break;
-        case 4: if (M <= 8) return kKernelLowM; break;
-        case 5: if (plan_umma(M, N, K, G, S, partials).ok) return kKernelUmma; break;
-        case 6: if (plan_wide(M, N, K, G, S, partials).ok) return kKernelWide; break;
-        case 7: if (plan_ahead(M, N, K, G, S, partials).ok) return kKernelAhead; break;
+        case 4: return M <= 8 && tma_ok && lowm_fits(plan_lowm(M, N, K, G, S, false)) ? kKernelLowM : kKernelNone;
+        case 5: return tma_ok && plan_umma(M, N, K, G, S, false).ok ? kKernelUmma : kKernelNone;
+        case 6: return tma_ok && plan_wide(M, N, K, G, S, false).ok ? kKernelWide : kKernelNone;
+        case 7: return tma_ok && plan_ahead(M, N, K, G, S, false).ok ? kKernelAhead : kKernelNone;
         default: break;
     }
+    if (!tma_ok) return kKernelStream;
     if (M > 8 && M <= kAheadMaxRows) {
         // 9..32 rows where every 128-row block of the decode-ahead tensor-core plan holds
         // one block an SM (its cluster of <= 16 tasks a row block): wo_a (G = 2, 1024 x 4096)
         // at M = 16 takes 5.9 us against 7.5 us streaming, at M = 32 8.9 against 9.5 us for
         // the tensor-core kernel; gate_up (1152 x 5120) at M = 16 5.1 against 8.4.
-        const AheadPlan ap = plan_ahead(M, N, K, G, S, partials);
+        const AheadPlan ap = plan_ahead(M, N, K, G, S, false);
         if (ap.ok && (long long)ap.grid_x * G <= sm_count()) return kKernelAhead;
     }
-    if (M > kUmmaMinRows) return plan_umma(M, N, K, G, S, partials).ok ? kKernelUmma : kKernelStream;
+    if (M > kUmmaMinRows) return plan_umma(M, N, K, G, S, false).ok ? kKernelUmma : kKernelStream;
     if (M > 8) {
         // 9..16 rows over an unsplit wide weight (a block of 128 rows for every SM, e.g. an
         // output head): the tensor-core kernel, two blocks an SM, measured 57 us against
         // 65 us for the streaming kernel at N = 32768, K = 5120.  Narrower weights stream.
         if (M <= 16 && S == 1 && (long long)G * ((N + 127) / 128) >= sm_count() &&
-            plan_umma(M, N, K, G, S, partials).ok)
+            plan_umma(M, N, K, G, S, false).ok)
             return kKernelUmma;
         return kKernelStream;
     }
-    const StreamPlan pl = plan_lowm(M, N, K, G, S, partials);
-    if ((long long)pl.grid_x * G <= 2LL * sm_count()) return kKernelLowM;
+    const StreamPlan pl = plan_lowm(M, N, K, G, S, false);
+    if (lowm_fits(pl) && (long long)pl.grid_x * G <= 2LL * sm_count()) return kKernelLowM;
     // more weight than the decode-ahead grid holds: the wide-weight kernel streams it
     // (one split: more would add the reduce pass the streaming kernel does without)
-    return S == 1 && plan_wide(M, N, K, G, S, partials).ok ? kKernelWide : kKernelStream;
+    return S == 1 && plan_wide(M, N, K, G, S, false).ok ? kKernelWide : kKernelStream;
 }
 
 // How one call runs: the kernel, its plan, and whether it writes fp32 partials (then the
@@ -192,8 +191,9 @@ struct Call {
 
 inline Call plan_call(int M, int N, int K, int G, int S, bool partials) {
     Call c{};
-    c.kernel = main_kernel(M, N, K, G, S, partials);
+    c.kernel = main_kernel(M, N, K, G, S);
     switch (c.kernel) {
+        case kKernelNone: return c;
         case kKernelUmma:
             c.up = plan_umma(M, N, K, G, S, partials);
             c.partials_out = c.up.partials;
@@ -207,10 +207,9 @@ inline Call plan_call(int M, int N, int K, int G, int S, bool partials) {
             c.partials_out = c.ap.partials;
             return c;
         case kKernelLowM: c.sp = plan_lowm(M, N, K, G, S, partials); break;
-        case kKernelTma: c.sp = plan_tma(M, N, K, G, S, partials); break;
         default: c.sp = plan_stream(M, N, K, G, S, partials); break;
     }
-    c.partials_out = c.sp.mode == kStreamPartials;
+    c.partials_out = c.sp.mode == kStreamPartials || c.sp.to_partials;
     return c;
 }
 
@@ -224,8 +223,8 @@ inline cudaError_t launch_call(const Call &c, const void *x, long long ldx, cons
         case kKernelWide: return launch_wide(c.wp, x, ldx, w8, ex, y, P, M, N, K, G, s);
         case kKernelAhead: return launch_ahead(c.ap, x, ldx, w8, ex, y, P, M, N, K, G, s);
         case kKernelLowM: return launch_lowm(c.sp, x, ldx, w8, ex, y, P, M, N, K, G, s);
-        case kKernelTma: return launch_tma(c.sp, x, ldx, w8, ex, y, P, M, N, K, G, s);
-        default: return launch_stream(c.sp, x, ldx, w8, ex, y, P, M, N, K, G, s);
+        case kKernelStream: return launch_stream(c.sp, x, ldx, w8, ex, y, P, M, N, K, G, s);
+        default: return cudaErrorInvalidValue;
     }
 }
 
@@ -248,7 +247,7 @@ inline RowsCall plan_rows(int M, int N, int K, int G, int S) {
     }
     if (M <= 8) {
         c.sp = plan_lowm(M, N, K, G, S, false);
-        c.lowm = (long long)c.sp.grid_x * G <= 2LL * sm_count();
+        c.lowm = lowm_fits(c.sp) && (long long)c.sp.grid_x * G <= 2LL * sm_count();
         if (c.lowm) return c;
     }
     c.sp = plan_stream(M, N, K, G, S, false);
@@ -308,7 +307,8 @@ int bsf8_gemm_auto_split(int M, int N, int K, int G) {
 size_t bsf8_gemm_workspace_bytes(int M, int N, int K, int G, int split_k) {
     if (check_gnk(G, N, K) || M < 1 || M > BSF8_MAX_M || split_k < 0 || split_k > K / 32) return 0;
     const int S = split_k == 0 ? call_auto_split(M, N, K, G) : split_k;
-    if (!plan_call(M, N, K, G, S, false).partials_out) return 0;
+    const Call c = plan_call(M, N, K, G, S, false);
+    if (c.kernel == kKernelNone || !c.partials_out) return 0;
     return (size_t)S * M * G * N * sizeof(float);
 }
 
@@ -319,22 +319,25 @@ int bsf8_gemm(const void *x, const uint8_t *w8, const uint8_t *exp, void *y, int
     if (st) return st;
     const int S = split_k == 0 ? call_auto_split(M, N, K, G) : split_k;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (options().gemm_path != 1 || S > kMaxClusterSplits) {
-        const Call c = plan_call(M, N, K, G, S, false);
-        if (!c.partials_out) return from_cuda(launch_call(c, x, ldx, w8, exp, y, nullptr, M, N, K, G, s));
-        const size_t need = (size_t)S * M * G * N * sizeof(float);
-        if (!workspace || workspace_bytes < need) return BSF8_ERR_WORKSPACE;
-        if (!aligned16(workspace)) return BSF8_ERR_ALIGN;
-        float *P = static_cast<float *>(workspace);
-        st = from_cuda(launch_call(c, x, ldx, w8, exp, nullptr, P, M, N, K, G, s));
-        if (st) return st;
-        return from_cuda(launch_splitk_reduce(P, y, S, (long long)M * G * N, s));
-    }
-    {  // the shared-memory TMA-ring kernel (BSF8_OPT_GEMM_PATH = 1), S <= 8
-        const GemmPlan pl = plan_gemm(M, N, K, G, S, S == 1 ? kModeDirect : kModeCluster);
-        if (pl.smem_bytes > kMaxSmem) return BSF8_ERR_SHAPE;
-        return from_cuda(launch_gemm(pl, x, ldx, w8, exp, y, nullptr, M, N, K, G, s));
-    }
+    const Call c = plan_call(M, N, K, G, S, false);
+    if (c.kernel == kKernelNone) return BSF8_ERR_VALUE;
+    if (!c.partials_out) return from_cuda(launch_call(c, x, ldx, w8, exp, y, nullptr, M, N, K, G, s));
+    const size_t need = (size_t)S * M * G * N * sizeof(float);
+    if (!workspace || workspace_bytes < need) return BSF8_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return BSF8_ERR_ALIGN;
+    float *P = static_cast<float *>(workspace);
+    st = from_cuda(launch_call(c, x, ldx, w8, exp, nullptr, P, M, N, K, G, s));
+    if (st) return st;
+    return from_cuda(launch_splitk_reduce(P, y, S, (long long)M * G * N, s));
+}
+
+int bsf8_gemm_kernel(int M, int N, int K, int G, int split_k) {
+    int st = check_gnk(G, N, K);
+    if (st) return -st;
+    if (M < 1 || M > BSF8_MAX_M || split_k < 0 || split_k > K / 32) return -BSF8_ERR_SHAPE;
+    const int S = split_k == 0 ? call_auto_split(M, N, K, G) : split_k;
+    const MainKernel k = main_kernel(M, N, K, G, S);
+    return k == kKernelNone ? -BSF8_ERR_VALUE : (int)k;
 }
 
 int bsf8_make_twin_rows(const void *w, uint8_t *w8, uint8_t *exp, uint8_t *block_ok, int32_t *accepted,
@@ -394,13 +397,9 @@ int bsf8_gemm_partials(const void *x, const uint8_t *w8, const uint8_t *exp, flo
     if (split_k < 1) return BSF8_ERR_SHAPE;
     if (!aligned16(partials)) return BSF8_ERR_ALIGN;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (options().gemm_path != 1) {
-        const Call c = plan_call(M, N, K, G, split_k, true);
-        return from_cuda(launch_call(c, x, ldx, w8, exp, nullptr, partials, M, N, K, G, s));
-    }
-    const GemmPlan pl = plan_gemm(M, N, K, G, split_k, kModePartials);
-    if (pl.smem_bytes > kMaxSmem) return BSF8_ERR_SHAPE;
-    return from_cuda(launch_gemm(pl, x, ldx, w8, exp, nullptr, partials, M, N, K, G, s));
+    const Call c = plan_call(M, N, K, G, split_k, true);
+    if (c.kernel == kKernelNone) return BSF8_ERR_VALUE;
+    return from_cuda(launch_call(c, x, ldx, w8, exp, nullptr, partials, M, N, K, G, s));
 }
 
 int bsf8_splitk_reduce(const float *partials, void *y, int S, int64_t count, bsf8_stream_t stream) {
@@ -463,7 +462,7 @@ int bsf8_set_option(int option, int64_t value) {
         case BSF8_OPT_WAIT_TIMEOUT_NS: g_opt_timeout_ns.store((long long)value); return BSF8_OK;
         case BSF8_OPT_DEBUG_SKIP_LOADS: g_opt_skip_loads.store(value ? 1 : 0); return BSF8_OK;
         case BSF8_OPT_GEMM_PATH:
-            if (value > 7) return BSF8_ERR_VALUE;
+            if (value > 7 || value == 1 || value == 3) return BSF8_ERR_VALUE;
             g_opt_gemm_path.store((int)value);
             return BSF8_OK;
         default: return BSF8_ERR_VALUE;

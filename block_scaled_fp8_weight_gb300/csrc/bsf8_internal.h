@@ -13,8 +13,8 @@ struct Options {
     int pdl;
     unsigned long long timeout_ns;
     int skip_loads;
-    int gemm_path;  // 0: by shape; 1: TMA-ring; 2: streaming; 3: TMA-fed; 4: decode-ahead;
-                    // 5: tensor-core; 6: wide-weight; 7: decode-ahead tensor-core
+    int gemm_path;  // 0: by shape; 2: streaming; 4: decode-ahead; 5: tensor-core;
+                    // 6: wide-weight; 7: decode-ahead tensor-core
 };
 Options options();
 
@@ -22,29 +22,9 @@ Options options();
 // per device); nullptr if the lookup fails.
 int *status_word();
 
-// GEMM geometry shared by the host planner and the kernels.
-constexpr int kBN = 64;           // weight rows per CTA
-constexpr int kStageK = 256;      // weight columns per pipeline stage (4 warps x 64)
-constexpr int kRowPitch = 320;    // shared-memory bytes per staged row (256 + 64 pad)
-constexpr int kStageBytes = kBN * kRowPitch;
-constexpr int kMaxStages = 4;
-constexpr int kConsumerWarps = 4;
-constexpr int kGemmThreads = (kConsumerWarps + 1) * 32;
-constexpr int kPrefetchCols = 1024;  // L2 prefetch per CTA row before the dependency wait
+// Largest cluster the streaming and decode-ahead kernels form to sum a slab's splits
+// (the portable cluster size).
 constexpr int kMaxClusterSplits = 8;
-constexpr int kTargetCtas = 2 * 152; // GB300: 152 SMs
-
-enum GemmMode { kModeDirect = 0, kModeCluster = 1, kModePartials = 2 };
-
-struct GemmPlan {
-    int S;            // splits
-    int chunk_cols;   // columns per split (multiple of 32)
-    int nt8;          // n8 tiles of tokens per CTA (1..4)
-    int m_chunks;     // ceil(M / (8 * nt8))
-    int stages;       // ring depth
-    int mode;
-    size_t smem_bytes;
-};
 
 // Weight-streaming kernel (bsf8_stream.cu): warp tasks of 16 rows x a column range.
 enum StreamMode { kStreamInCta = 0, kStreamCluster = 1, kStreamPartials = 2, kStreamGroup = 3 };
@@ -54,6 +34,8 @@ struct StreamPlan {
     int nt8, m_chunks;           // token tiles of 8 per pass, passes over the tokens
     int mode, spc, cluster, spl, cps, grid_x;
     int tpc;  // group mode (decode-ahead kernel): tasks of each slab a block holds
+    int to_partials;  // group mode (decode-ahead kernel): the fold writes each split's fp32
+                      // partial (tasks summed in order) instead of summing the splits into y
 };
 
 StreamPlan plan_stream(int M, int N, int K, int G, int S, bool partials);
@@ -63,17 +45,16 @@ StreamPlan plan_stream_ks(int M, int N, int K, int G, int S, bool partials, int 
                           int max_kt = 1 << 30);
 
 // Decode-ahead kernel (bsf8_lowm.cu) for up to 8 token rows; 128-column steps, tasks of
-// at most 1024 columns.
+// at most 512 columns.  The plan's decomposition does not depend on `partials` (a call for
+// the partials differs only in what the fold stores), so y and the partials summed by the
+// fixed-order reduce agree bit for bit.  lowm_fits: the kernel can run the plan.
 StreamPlan plan_lowm(int M, int N, int K, int G, int S, bool partials);
+bool lowm_fits(const StreamPlan &plan);
 cudaError_t launch_lowm(const StreamPlan &plan, const void *x, long long ldx, const uint8_t *w8,
                         const uint8_t *ex, void *y, float *partials, int M, int N, int K, int G,
                         cudaStream_t stream, bool rows_exp = false);
 
-// TMA-fed kernel (bsf8_tma.cu) for up to 16 token rows per pass; 128-column steps.
-StreamPlan plan_tma(int M, int N, int K, int G, int S, bool partials);
-cudaError_t launch_tma(const StreamPlan &plan, const void *x, long long ldx, const uint8_t *w8,
-                       const uint8_t *ex, void *y, float *partials, int M, int N, int K, int G,
-                       cudaStream_t stream);
+// Streaming kernel (bsf8_stream.cu).
 // rows_exp: exponents per (weight row, 32 columns), [G][N][K/32], instead of per 32 x 32 block
 cudaError_t launch_stream(const StreamPlan &plan, const void *x, long long ldx, const uint8_t *w8,
                           const uint8_t *ex, void *y, float *partials, int M, int N, int K, int G,
@@ -117,13 +98,10 @@ cudaError_t launch_ahead(const AheadPlan &plan, const void *x, long long ldx, co
                          const uint8_t *ex, void *y, float *partials, int M, int N, int K, int G,
                          cudaStream_t stream, bool rows_exp = false);
 
+// The streaming kernel's split count for split_k = 0 (bsf8_reduce.cu; sizes only).
 int auto_split(int M, int N, int K, int G);
-GemmPlan plan_gemm(int M, int N, int K, int G, int S, int mode);
 
 // Launchers return a cudaError_t.
-cudaError_t launch_gemm(const GemmPlan &plan, const void *x, long long ldx, const uint8_t *w8,
-                        const uint8_t *ex, void *y, float *partials, int M, int N, int K, int G,
-                        cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const float *P, void *y, int S, long long count,
                                  cudaStream_t stream);
 cudaError_t launch_splitk_reduce_f32(const float *P, float *y, int S, long long count, cudaStream_t stream);

@@ -63,17 +63,22 @@ constexpr int kGatherTiles = 32;   // group mode: [16 rows][8 tokens] fp32 parti
 constexpr int kSmemBytes = 84 * 1024;
 static_assert(kRingBytes + kGatherTiles * 512 + 1024 <= kSmemBytes, "slots fit the request");
 static_assert(3 * (kSmemBytes + 1024) > 228 * 1024, "at most two blocks an SM");
-static_assert(2 * (kSmemBytes + 1024 + 6 * 1024) <= 228 * 1024, "two blocks fit an SM");
+static_assert(2 * (kSmemBytes + 1024 + 8 * 1024) <= 228 * 1024, "two blocks fit an SM");
 
 struct LowParams {
     CUtensorMap wmap;  // w8 as a [G*N rows][K columns] byte matrix, box 128 x 16
+    // x as {64 columns, M rows, K/64 column chunks, G groups} (pitches ldx*2, 128, K*2
+    // bytes), box {64, 8, 2, 1}: a step's 8 x 128 tile in one copy, each 64-column chunk an
+    // 8 x 64 box with the 128-byte swizzle (rows >= M read as zeros).  Used when xtma != 0.
+    CUtensorMap xmap;
+    int xtma;
     const uint16_t *x;  // [M][ldx] bf16
     long long ldx;
     const uint8_t *ex;
     uint16_t *y;
     float *partials;
     int M, N, K, G, S;
-    int chunk_cols, kt, tps, spc, cluster, spl, cps, mode, tpc;
+    int chunk_cols, kt, tps, spc, cluster, spl, cps, mode, tpc, to_partials;
     unsigned long long timeout_ns;
     int skip_loads;
     int *status;
@@ -298,69 +303,117 @@ __device__ __forceinline__ void decode_box(const uint8_t *box, const BoxOffs &o,
     }
 }
 
-// This thread's x fragment of a step: token r, columns 32q .. 32q+31 (16 words, word i =
-// columns 2i, 2i+1), from an 8 x 128 tile stored as two 8 x 64 boxes with the 128-byte
-// swizzle.  Zero where the thread's columns are past its task.
-__device__ __forceinline__ void load_xfrag(const uint8_t *slot, int r, int q, bool mine,
-                                           uint4 (&xv)[4]) {
+// Half H of this thread's x fragment of a step: token r, columns 32q + 16H .. 32q + 16H + 15
+// (8 words, word i = columns 2i, 2i+1 of the half), from an 8 x 128 tile stored as two 8 x 64
+// boxes with the 128-byte swizzle.  Zero where the thread's columns are past its task.
+template <int H>
+__device__ __forceinline__ void load_xhalf(const uint8_t *slot, int r, int q, bool mine,
+                                           uint4 (&xv)[2]) {
     const uint8_t *row = slot + (q >> 1) * 1024 + r * 128;
 #pragma unroll
-    for (int v = 0; v < 4; ++v)
-        xv[v] = mine ? *reinterpret_cast<const uint4 *>(row + ((((q & 1) * 4 + v) ^ r) << 4))
+    for (int v = 0; v < 2; ++v)
+        xv[v] = mine ? *reinterpret_cast<const uint4 *>(row + ((((q & 1) * 4 + 2 * H + v) ^ r) << 4))
                      : make_uint4(0, 0, 0, 0);
 }
 
-// The step's 8 MMAs (m16n8k16, rows r / r+8 of the slab, tokens 0..7): MMA j multiplies
-// columns 4j..4j+3 of every thread's 32.  Two accumulators break the dependency chain.
-__device__ __forceinline__ void mma_step(const uint32_t (&a)[32], const uint4 (&xv)[4],
-                                         float (&acc)[2][4]) {
+// MMAs j0 .. j0+3 of a step (m16n8k16, rows r / r+8 of the slab, tokens 0..7): MMA j
+// multiplies columns 4j..4j+3 of every thread's 32 into accumulator j % 4.  An mma.sync on
+// this GPU takes ~190 cycles to complete against an SM rate of one every ~4.5 cycles, so the
+// MMAs of a warp are spread over 4 independent accumulation chains (32 an SM).
+template <int J0>
+__device__ __forceinline__ void mma_half(const uint32_t (&a)[32], const uint4 (&xv)[2],
+                                         float (&acc)[4][4]) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const uint4 &x = xv[j / 2];
-        mma_bf16_16816(acc[j & 1], a[4 * j], a[4 * j + 1], a[4 * j + 2], a[4 * j + 3],
+    for (int j = J0; j < J0 + 4; ++j) {
+        const uint4 &x = xv[(j - J0) / 2];
+        mma_bf16_16816(acc[j & 3], a[4 * j], a[4 * j + 1], a[4 * j + 2], a[4 * j + 3],
                        (j & 1) ? x.z : x.x, (j & 1) ? x.w : x.y);
     }
+}
+
+// 16 TMEM columns of this thread's lane -> registers.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
 }
 
 __device__ __forceinline__ void st_cluster_v2f32(uint32_t addr, float a, float b) {
     asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }
 
+// Parameters the block reads after the dependency wait, staged in shared memory before it.
+// Kernel parameters read right after griddepcontrol.wait are slow to arrive (a measured
+// ~0.5 us a call over a handful of reads on the decode-ahead tensor-core kernel), while
+// shared memory answers at once.
+struct PostParams {
+    const uint16_t *x;
+    uint16_t *y;
+    float *partials;
+    long long ldx;
+    unsigned long long timeout_ns;
+    int *status;
+    int M, N, K, G, S, tps, tpc, cluster, mode, cps, spl, skip_loads, xtma, to_partials;
+};
+
 // Partials mode: red[w] holds warp w's task partial [16 rows][8 tokens]; the block stores
 // its splits' fp32 partials (tasks of a split summed in task order).  Stores are skipped
 // when the block met an error.
-__device__ __forceinline__ void partials_epilogue(const LowParams &p, float (*red)[16][8],
+__device__ __forceinline__ void partials_epilogue(const PostParams &q, float (*red)[16][8],
                                                   const volatile int *err, int g) {
-    const int mrows = min(8, p.M);
+    const int mrows = min(8, q.M);
     __syncthreads();
     if (*err) return;
-    const int slab = blockIdx.x / p.cps;
+    const int slab = blockIdx.x / q.cps;
     const int per_split = 16 * mrows;
-    for (int i = threadIdx.x; i < p.spl * per_split; i += kThreads) {
+    for (int i = threadIdx.x; i < q.spl * per_split; i += kThreads) {
         const int ls = i / per_split, rem = i - ls * per_split;
         const int m = rem / 16, row = rem - m * 16;
-        const int ss = (blockIdx.x % p.cps) * p.spl + ls;
-        if (ss >= p.S) continue;
-        float ps = red[ls * p.tps][row][m];
-        for (int uu = 1; uu < p.tps; ++uu) ps = ps + red[ls * p.tps + uu][row][m];
-        p.partials[(((size_t)ss * p.M + m) * p.G + g) * p.N + slab * 16 + row] = ps;
+        const int ss = (blockIdx.x % q.cps) * q.spl + ls;
+        if (ss >= q.S) continue;
+        float ps = red[ls * q.tps][row][m];
+        for (int uu = 1; uu < q.tps; ++uu) ps = ps + red[ls * q.tps + uu][row][m];
+        q.partials[(((size_t)ss * q.M + m) * q.G + g) * q.N + slab * 16 + row] = ps;
     }
+}
+
+// 4-D tensor copy global -> this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_4d(void *dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                       int c3, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Keeps v in a register as an opaque value, so that the compiler cannot recompute it from
+// kernel parameters after the dependency wait.
+__device__ __forceinline__ int opaque(int v) {
+    asm volatile("mov.b32 %0, %0;" : "+r"(v));
+    return v;
 }
 
 }  // namespace
 
 // One block: 8 warps.  Warp w owns an 8 KB region of shared memory (4 slots of 2 KB) and
-// one mbarrier.  Its task has nst <= 4 steps of 128 columns.
-//   before the wait: lane 0 arms the barrier with the task's weight bytes and issues one TMA
+// two mbarriers (weights, x).  Its task has nst <= 4 steps of 128 columns.
+//   before the wait: lane 0 arms the weight barrier with the task's bytes and issues one TMA
 //     box (16 rows x 128 columns, 128-byte swizzle) per step into slot t; the warp waits,
-//     rebuilds each box into its 32 fragment registers and parks them in tensor memory;
-//   after the wait: every lane copies its share of the task's x tiles (8 token rows x 128
-//     columns a step, 16 bytes a copy) into the same slots with cp.async, in the layout of
-//     a 128-byte-swizzled box; then, step by step, the fragments come back from tensor
-//     memory (tcgen05.ld) and meet x in the MMAs.
-// One barrier covers all of a warp's boxes: the copies complete in one transaction count,
-// far faster than a barrier per box.  x goes through the load/store path, not the TMA unit,
-// so the post-wait copies of all 8 warps run in parallel.
+//     rebuilds each box into its 32 fragment registers and parks steps 1.. in tensor memory
+//     (step 0 stays in registers);
+//   after the wait: the task's x tile (8 token rows x the task's columns) arrives in the
+//     same slots -- one TMA box a task when the columns allow it, else 16-byte cp.async
+//     copies -- in the layout of 128-byte-swizzled 8 x 64 boxes; step by step the warp
+//     multiplies, reading the next step's fragments back from tensor memory (tcgen05.ld)
+//     while the current step's MMAs run.
+// One barrier covers all of a warp's weight boxes: the copies complete in one transaction
+// count, far faster than a barrier per box.
 template <bool ROWS>
 __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant__ LowParams p) {
     extern __shared__ uint8_t dyn_smem[];
@@ -369,8 +422,12 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
     float *const gather = reinterpret_cast<float *>(ring + kRingBytes);  // group mode tiles
     __shared__ __align__(16) float red[kWarps][16][8];
     __shared__ __align__(8) uint64_t wbar[kWarps];
+    __shared__ __align__(8) uint64_t xbar[kWarps][kPre];  // x: one barrier a step
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
+    __shared__ PostParams sp;
+    __shared__ long long s_fold_y[kThreads];  // y element this thread folds (-1: none)
+    __shared__ int s_fold_t[kThreads];        // its first partial tile (float index)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -390,10 +447,39 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
 
     if (lane == 0) {
         mbar_init(&wbar[warp], 1);
+#pragma unroll
+        for (int t = 0; t < kPre; ++t) mbar_init(&xbar[warp][t], 1);
         fence_mbar_init();
     }
     if (threadIdx.x == 0) s_err = 0;
-    if (threadIdx.x == 32) prefetch_tensormap(&p.wmap);
+    if (threadIdx.x == 32) {
+        prefetch_tensormap(&p.wmap);
+        if (p.xtma) prefetch_tensormap(&p.xmap);
+    }
+    if (threadIdx.x == 64) {
+        PostParams t;
+        t.x = p.x;
+        t.y = p.y;
+        t.partials = p.partials;
+        t.ldx = p.ldx;
+        t.timeout_ns = p.timeout_ns;
+        t.status = p.status;
+        t.M = p.M;
+        t.N = p.N;
+        t.K = p.K;
+        t.G = p.G;
+        t.S = p.S;
+        t.tps = p.tps;
+        t.tpc = p.tpc;
+        t.cluster = p.cluster;
+        t.mode = p.mode;
+        t.cps = p.cps;
+        t.spl = p.spl;
+        t.skip_loads = p.skip_loads;
+        t.xtma = p.xtma;
+        t.to_partials = p.to_partials;
+        sp = t;
+    }
     if (warp == 0) tmem_alloc(&s_tmem, kTmemCols);
     tc_fence_before();
     __syncthreads();
@@ -417,8 +503,8 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
     }
     // The task's x rows, pulled into L2 while the previous kernel runs.  They may still
     // change before the wait; a prefetch only moves lines into L2, where the producer's
-    // writes land as well, and x is read after the wait from L2 (cp.async.cg), so the
-    // copies see the producer's values.  Where x is already in L2 this costs nothing.
+    // writes land as well, and x is read after the wait from L2 (TMA, or cp.async.cg), so
+    // the copies see the producer's values.  Where x is already in L2 this costs nothing.
     if (xj == 0 && lane < p.M && lane < 8 && me.k1 > me.k0)
         prefetch_l2(p.x + (size_t)lane * p.ldx + (size_t)g * p.K + me.k0,
                     (uint32_t)((me.k1 - me.k0) * 2));
@@ -451,7 +537,8 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
     const bool two = __any_sync(0xFFFFFFFFu, emax > 134u);
     const BoxOffs bo = box_offsets(r, q);
 
-    // ---- before the wait: rebuild every step into tensor memory
+    // ---- before the wait: rebuild every step; steps 1.. into tensor memory, step 0 into
+    //      registers (the first MMAs after the wait need no tensor-memory round trip)
     int err = 0;
     uint32_t mxa = 0, mxb = 0;
     {
@@ -462,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
             if (lane == 0) report_timeout(p.status);
         }
     }
-    for (int t = 0; t < nst; ++t) {
+    for (int t = 1; t < nst; ++t) {
         const int col = me.k0 + t * kKS;
         const bool mine = !err && slab_ok && col + q * 32 < me.k1;
         const uint32_t eblk = __shfl_sync(0xFFFFFFFFu, ereg, (4 * t + q) & 31);
@@ -475,22 +562,89 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
             decode_box<false, ROWS>(region + t * kSlotBytes, bo, mine, e, eb, a, mxa, mxb);
         tmem_st32(tbase + 32u * t, a);
     }
+    uint32_t cur[32];
+    {
+        const bool mine = !err && slab_ok && me.k0 + q * 32 < me.k1;
+        const uint32_t eblk = __shfl_sync(0xFFFFFFFFu, ereg, q);
+        const uint32_t e = ROWS ? era & 0xFFu : eblk;
+        const uint32_t eb = ROWS ? erb & 0xFFu : eblk;
+        if (two)
+            decode_box<true, ROWS>(region, bo, mine, e, eb, cur, mxa, mxb);
+        else
+            decode_box<false, ROWS>(region, bo, mine, e, eb, cur, mxa, mxb);
+    }
     tmem_wait_st();
+
+    // ---- everything after the wait that depends only on the weights and the plan, done
+    //      now: rows with an e4m3 NaN code, where this warp's partial tile goes, and which
+    //      output this thread folds
+    uint32_t fa = nan_code_seen(mxa) ? 1u : 0u, fb = nan_code_seen(mxb) ? 1u : 0u;
+    fa |= __shfl_xor_sync(0xFFFFFFFFu, fa, 1);
+    fa |= __shfl_xor_sync(0xFFFFFFFFu, fa, 2);
+    fb |= __shfl_xor_sync(0xFFFFFFFFu, fb, 1);
+    fb |= __shfl_xor_sync(0xFFFFFFFFu, fb, 2);
+    const int C = p.cluster, spc = kWarps / p.tpc, tslab = p.S * p.tps;
+    const int rank = blockIdx.x % C;
+    // group mode: the partial tile of this warp's task sits at tile index li * tslab + tau of
+    // block rr of the cluster (slab sl of the block group's spc reduced by rank sl % C)
+    uint32_t tile_addr = 0;
+    {
+        const int sl = warp / p.tpc;
+        const int rr = sl % C, li = sl / C;
+        const int tau = rank * p.tpc + warp % p.tpc;
+        float *tile = gather + (size_t)(li * tslab + tau) * 128 + r * 8 + 2 * q;
+        tile_addr = C == 1 ? smem_u32(tile) : map_to_rank(tile, (uint32_t)rr);
+    }
+    // fold: output i of this block (i = thread, thread + 256, ...) is token m, row `row` of
+    // local slab lj; fold_n outputs in all
+    const int mrows = min(8, p.M), per_slab = 16 * mrows;
+    const int nmine = (spc - rank + C - 1) / C;  // slabs rank, rank + C, ...
+    const int fold_n = p.mode == kStreamPartials ? 0 : nmine * per_slab;
+    long long fold_y = -1;   // y element of this thread's first output
+    int fold_t = 0;          // its first tile, as a float index into gather
+    if ((int)threadIdx.x < fold_n && fold_n > 0) {
+        const int i = threadIdx.x;
+        const int lj = i / per_slab, rem = i - lj * per_slab;
+        const int m = rem / 16, row = rem - m * 16;
+        const int sb = (blockIdx.x / C) * spc + lj * C + rank;
+        if (sb < nslabs) {
+            fold_y = ((long long)m * p.G + g) * p.N + sb * 16 + row;
+            fold_t = lj * tslab * 128 + row * 8 + m;
+        }
+    }
+    s_fold_y[threadIdx.x] = fold_y;  // read back after the wait (kept out of registers)
+    s_fold_t[threadIdx.x] = fold_t;
+    // held in registers as they are (not recomputed from kernel parameters after the wait)
+    const int k0 = opaque(me.k0), k1 = opaque(me.k1);
+    const int boxed_steps = opaque(slab_ok ? nbox : 0);
+    const int nsteps = opaque(nst);
+    const int active = opaque(me.active ? 1 : 0);
+    tile_addr = (uint32_t)opaque((int)tile_addr);
     __syncthreads();  // every warp's weight boxes are rebuilt: the regions may take x
+    // the regions were read through the generic proxy; x lands through the async proxy
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 
     // ---- the dependency wait: x (and y) belong to the kernels before this one
     pdl_wait();
+    const PostParams &prm = sp;  // read from shared memory where used
 
-    // ---- x tiles of the task's steps (16-byte copies, rows >= M as zeros), in the layout of
-    //      a 128-byte-swizzled 8 x 64 box pair per step
-    {
-        const long long gk = (long long)p.G * p.K;
-        const bool task_ok = me.k1 > me.k0;
-        for (int c = xj * 32 + lane; c < nst * 128; c += xn * 32) {
+    // ---- x tiles of the task's steps, in the layout of a 128-byte-swizzled 8 x 64 box pair
+    //      per step (rows >= M as zeros)
+    const bool task_ok = k1 > k0;
+    if (prm.xtma) {
+        // one 2 KB box a step, each on its own barrier, issued by lanes 0.. of the first
+        // warp of the task's column range: the step's MMAs start as soon as it lands
+        if (xj == 0 && lane < nsteps && task_ok) {
+            mbar_arrive_expect_tx(&xbar[warp][lane], (uint32_t)kSlotBytes);
+            tma_4d(region + lane * kSlotBytes, &p.xmap, 0, 0, k0 / 64 + 2 * lane, g, &xbar[warp][lane]);
+        }
+    } else {
+        const long long gk = (long long)prm.G * prm.K;
+        for (int c = xj * 32 + lane; c < nsteps * 128; c += xn * 32) {
             const int t = c >> 7, row = (c >> 4) & 7, unit = c & 15;
-            const int col = me.k0 + t * kKS + unit * 8;  // first of the copy's 8 columns
-            const bool in = task_ok && row < p.M && (long long)g * p.K + col < gk;
-            const uint16_t *src = p.x + (in ? (size_t)row * p.ldx + (size_t)g * p.K + col : 0);
+            const int col = k0 + t * kKS + unit * 8;  // first of the copy's 8 columns
+            const bool in = task_ok && row < prm.M && (long long)g * prm.K + col < gk;
+            const uint16_t *src = prm.x + (in ? (size_t)row * prm.ldx + (size_t)g * prm.K + col : 0);
             cp_async_16_zfill(xregion + t * kSlotBytes + (unit >> 3) * 1024 + row * 128 +
                                   (((unit & 7) ^ row) << 4),
                               src, in ? 16u : 0u);
@@ -499,95 +653,144 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
         __syncthreads();
     }
 
-    // ---- MMAs: fragments back from tensor memory, x from the slots
-    float acc[2][4];
+    // ---- MMAs, in half steps (4 MMAs, 16 fragment registers each).  Step t's fragments are
+    //      in cur; the next half's arrive from tensor memory into nh while the current
+    //      half's MMAs run, and are moved into cur once those MMAs have been issued (the
+    //      asynchronous load never writes a register an MMA in flight may still read).
+    float acc[4][4];
 #pragma unroll
-    for (int a = 0; a < 2; ++a)
+    for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[a][c] = 0.0f;
-    for (int t = 0; t < nst; ++t) {
-        uint32_t a[32];
-        tmem_ld32(tbase + 32u * t, a);
-        const int col = me.k0 + t * kKS;
-        const bool boxed = slab_ok && col < me.k1;
-        const bool mine = boxed && col + q * 32 < me.k1;
-        uint4 xv[4];
-        load_xfrag(xregion + t * kSlotBytes, r, q, mine, xv);
-        tmem_wait_ld();
-        if (!err && boxed) mma_step(a, xv, acc);
+#pragma unroll
+    for (int t = 0; t < kPre; ++t) {
+        if (t < nsteps) {
+            const bool more = t + 1 < nsteps;
+            if (prm.xtma && task_ok) {
+                const bool ok = err || mbar_wait_bounded(&xbar[xl][t], 0u, prm.timeout_ns);
+                if (__any_sync(0xFFFFFFFFu, !ok)) {
+                    if (lane == 0) report_timeout(prm.status);
+                    err = 1;
+                    *(volatile int *)&s_err = 1;
+                }
+            }
+            const int col = k0 + t * kKS;
+            const bool mine = t < boxed_steps && col + q * 32 < k1;
+            const bool run = !err && t < boxed_steps;
+            uint4 xv[2];
+            load_xhalf<0>(xregion + t * kSlotBytes, r, q, mine, xv);
+            uint32_t nh[16];
+            if (more) tmem_ld16(tbase + 32u * (t + 1), nh);       // next step, first half
+            if (run) mma_half<0>(cur, xv, acc);
+            load_xhalf<1>(xregion + t * kSlotBytes, r, q, mine, xv);
+            if (more) {
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) cur[i] = nh[i];
+                tmem_ld16(tbase + 32u * (t + 1) + 16u, nh);        // next step, second half
+            }
+            if (run) mma_half<4>(cur, xv, acc);
+            if (more) {
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) cur[16 + i] = nh[i];
+            }
+        }
     }
 
     // ---- the fixed-order reduction and store
     {
-        uint32_t fa = nan_code_seen(mxa) ? 1u : 0u, fb = nan_code_seen(mxb) ? 1u : 0u;
-        fa |= __shfl_xor_sync(0xFFFFFFFFu, fa, 1);
-        fa |= __shfl_xor_sync(0xFFFFFFFFu, fa, 2);
-        fb |= __shfl_xor_sync(0xFFFFFFFFu, fb, 1);
-        fb |= __shfl_xor_sync(0xFFFFFFFFu, fb, 2);
         const float qnan = __uint_as_float(0x7FC00000u);
         float v[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            v[c] = acc[0][c] + acc[1][c];
+            v[c] = (acc[0][c] + acc[1][c]) + (acc[2][c] + acc[3][c]);
             if ((c < 2 && fa) || (c >= 2 && fb)) v[c] = qnan;
         }
-        if (p.mode == kStreamPartials) {
+        if (prm.mode == kStreamPartials) {
             *reinterpret_cast<float2 *>(&red[warp][r][2 * q]) = make_float2(v[0], v[1]);
             *reinterpret_cast<float2 *>(&red[warp][r + 8][2 * q]) = make_float2(v[2], v[3]);
-            partials_epilogue(p, red, &s_err, g);
+            partials_epilogue(prm, red, &s_err, g);
         } else {
-            // Group mode: every warp pushes its partial tile to the block of the cluster that
-            // reduces its slab (slab sl of the cluster's spc goes to rank sl % C, local tile
-            // index sl / C), then each block folds its slabs' tiles in the fixed order.
-            const int C = p.cluster, spc = kWarps / p.tpc, tslab = p.S * p.tps;
-            const int rank = blockIdx.x % C;
-            const int sl = warp / p.tpc;
-            const int rr = sl % C, li = sl / C;
-            const int tau = rank * p.tpc + warp % p.tpc;
-            if (me.active) {
-                float *tile = gather + (size_t)(li * tslab + tau) * 128;
-                float *d0 = tile + r * 8 + 2 * q, *d1 = tile + (r + 8) * 8 + 2 * q;
-                if (C == 1) {
-                    *reinterpret_cast<float2 *>(d0) = make_float2(v[0], v[1]);
-                    *reinterpret_cast<float2 *>(d1) = make_float2(v[2], v[3]);
+            // Group mode: every warp puts its partial tile in the block that reduces its
+            // slab (this block when C = 1, else over DSMEM), then each block folds its
+            // slabs' tiles in the fixed order.
+            if (active) {
+                if (prm.cluster == 1) {
+                    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(tile_addr), "f"(v[0]), "f"(v[1]) : "memory");
+                    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(tile_addr + 8 * 8 * 4), "f"(v[2]), "f"(v[3])
+                                 : "memory");
                     if (err) s_err = 1;
                 } else {
-                    st_cluster_v2f32(map_to_rank(d0, (uint32_t)rr), v[0], v[1]);
-                    st_cluster_v2f32(map_to_rank(d1, (uint32_t)rr), v[2], v[3]);
+                    st_cluster_v2f32(tile_addr, v[0], v[1]);
+                    st_cluster_v2f32(tile_addr + 8 * 8 * 4, v[2], v[3]);
                     if (err && lane == 0) {  // the reducer must not store a sum with garbage in it
-                        const uint32_t ea = map_to_rank((const void *)&s_err, (uint32_t)rr);
+                        const int sl = warp / prm.tpc;
+                        const uint32_t ea = map_to_rank((const void *)&s_err, (uint32_t)(sl % prm.cluster));
                         asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(ea), "r"(1u) : "memory");
                     }
                 }
             }
-            if (C > 1)
+            if (prm.cluster > 1)
                 cluster_sync();
             else
                 __syncthreads();
             if (!s_err) {
-                const int nslabs = p.N / 16, mrows = min(8, p.M), per_slab = 16 * mrows;
-                const int nmine = (spc - rank + C - 1) / C;  // slabs rank, rank + C, ...
-                for (int i = threadIdx.x; i < nmine * per_slab; i += kThreads) {
-                    const int lj = i / per_slab, rem = i - lj * per_slab;
-                    const int m = rem / 16, row = rem - m * 16;
-                    const int slab = (blockIdx.x / C) * spc + lj * C + rank;
-                    if (slab >= nslabs) continue;
-                    const float *tiles = gather + (size_t)lj * tslab * 128 + row * 8 + m;
+                const int S = prm.S, tps = prm.tps;
+                // partials: split ss of output (m, g, n) at P[ss][m][g][n], i.e. y's index
+                // plus ss * M * G * N
+                const long long mgn = (long long)prm.M * prm.G * prm.N;
+                const long long fy = s_fold_y[threadIdx.x];
+                if (fy >= 0) {
+                    const float *tiles = gather + s_fold_t[threadIdx.x];
                     float y = 0.0f;
-                    for (int ss = 0; ss < p.S; ++ss) {
-                        float ps = tiles[(ss * p.tps) * 128];
-                        for (int uu = 1; uu < p.tps; ++uu) ps = ps + tiles[(ss * p.tps + uu) * 128];
-                        y = ss == 0 ? ps : y + ps;
+                    if (prm.to_partials) {
+                        for (int ss = 0; ss < S; ++ss) {
+                            float ps = tiles[(ss * tps) * 128];
+                            for (int uu = 1; uu < tps; ++uu) ps = ps + tiles[(ss * tps + uu) * 128];
+                            prm.partials[fy + ss * mgn] = ps;
+                        }
+                    } else {
+#pragma unroll 8
+                        for (int ss = 0; ss < S; ++ss) {
+                            float ps = tiles[(ss * tps) * 128];
+                            for (int uu = 1; uu < tps; ++uu) ps = ps + tiles[(ss * tps + uu) * 128];
+                            y = ss == 0 ? ps : y + ps;
+                        }
+                        prm.y[fy] = f32_to_bf16_rn(y);
                     }
-                    p.y[((size_t)m * p.G + g) * p.N + slab * 16 + row] = f32_to_bf16_rn(y);
+                }
+                // outputs past the first 256 of the block (blocks of several slabs)
+                const int nsl = prm.N / 16, C2 = prm.cluster, spc2 = kWarps / prm.tpc;
+                const int mr = min(8, prm.M), ps_ = 16 * mr, ts = S * tps;
+                for (int i = threadIdx.x + kThreads; i < fold_n; i += kThreads) {
+                    const int lj = i / ps_, rem = i - lj * ps_;
+                    const int m = rem / 16, row = rem - m * 16;
+                    const int sb = (blockIdx.x / C2) * spc2 + lj * C2 + (blockIdx.x % C2);
+                    if (sb >= nsl) continue;
+                    const float *tiles = gather + (size_t)lj * ts * 128 + row * 8 + m;
+                    const long long yi = ((long long)m * prm.G + g) * prm.N + sb * 16 + row;
+                    float y = 0.0f;
+                    for (int ss = 0; ss < S; ++ss) {
+                        float ps = tiles[(ss * tps) * 128];
+                        for (int uu = 1; uu < tps; ++uu) ps = ps + tiles[(ss * tps + uu) * 128];
+                        if (prm.to_partials)
+                            prm.partials[yi + ss * mgn] = ps;
+                        else
+                            y = ss == 0 ? ps : y + ps;
+                    }
+                    if (!prm.to_partials) prm.y[yi] = f32_to_bf16_rn(y);
                 }
             }
         }
     }
 
-    // After an error, let the weight boxes this warp issued land before the block exits.
-    if (err && lane == 0 && nbox > 0 && !p.skip_loads)
-        (void)mbar_wait_bounded(&wbar[warp], 0u, p.timeout_ns);
+    // After an error, let the copies this warp issued land before the block exits.
+    if (err) {
+        if (lane == 0 && nbox > 0 && !prm.skip_loads) (void)mbar_wait_bounded(&wbar[warp], 0u, prm.timeout_ns);
+        if (prm.xtma && xj == 0 && task_ok && lane < nsteps)
+            (void)mbar_wait_bounded(&xbar[warp][lane], 0u, prm.timeout_ns);
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -658,20 +861,67 @@ cudaError_t weight_map(const uint8_t *w8, long long rows, int K, CUtensorMap *ou
     return cudaSuccess;
 }
 
+// Tensor maps of recently used activations: x[M][ldx] bf16 as {64 columns, M rows, K/64
+// chunks, G groups}, box {64, 8, 2, 1}, 128-byte swizzle (the 8 x 128 tile of one step).
+// Needs K % 64 == 0.  Returns cudaErrorNotSupported where the driver declines the map.
+struct XKey {
+    const void *ptr;
+    long long ldx;
+    int M, K, G;
+};
+
+cudaError_t x_map(const void *x, int M, int K, int G, long long ldx, CUtensorMap *out) {
+    static std::mutex mu;
+    static XKey keys[64];
+    static CUtensorMap maps[64];
+    static int used = 0, next = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (keys[i].ptr == x && keys[i].ldx == ldx && keys[i].M == M && keys[i].K == K && keys[i].G == G) {
+            *out = maps[i];
+            return cudaSuccess;
+        }
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return cudaErrorNotSupported;
+    CUtensorMap m;
+    const cuuint64_t dims[4] = {64u, (cuuint64_t)M, (cuuint64_t)(K / 64), (cuuint64_t)G};
+    const cuuint64_t strides[3] = {(cuuint64_t)ldx * 2u, 128u, (cuuint64_t)K * 2u};
+    const cuuint32_t box[4] = {64u, 8u, (cuuint32_t)(kKS / 64), 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    const CUresult res = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(x), dims, strides,
+                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (res != CUDA_SUCCESS) return cudaErrorNotSupported;
+    keys[next] = XKey{x, ldx, M, K, G};
+    maps[next] = m;
+    next = (next + 1) % 64;
+    if (used < 64) ++used;
+    *out = m;
+    return cudaSuccess;
+}
+
 }  // namespace
 
 StreamPlan plan_lowm(int M, int N, int K, int G, int S, bool partials) {
-    StreamPlan pl = plan_stream_ks(M, N, K, G, S, partials, kKS, 1, kMaxKt);
+    // the same decomposition whether the caller wants y or the partials
+    StreamPlan pl = plan_stream_ks(M, N, K, G, S, false, kKS, 1, kMaxKt);
     if (pl.mode == kStreamPartials) {
         pl.tpc = kWarps;
         return pl;
     }
     // Group mode.  A block holds tpc tasks of each of 8 / tpc slabs (the slabs' warps share
     // the tasks' x tiles) and a cluster of ceil(tslab / tpc) blocks holds all of the slabs'
-    // tasks.  Fewer tasks a block means less x to fetch after the wait per block, but a
-    // larger cluster; kLowTasksPerBlock is the balance, raised until the cluster fits 8.
+    // tasks.  Where a slab has at most 8 tasks a block holds all of them (a cluster of one):
+    // the splits are then summed in the block behind one __syncthreads, with no DSMEM push
+    // and no cluster barrier after the wait.  Otherwise fewer tasks a block means less x to
+    // fetch after the wait per block, but a larger cluster; kLowTasksPerBlock is the
+    // balance, raised until the cluster fits 8.
     const int tslab = S * pl.tps;
     int tpc = kLowTasksPerBlock;
+    if (tslab <= kWarps) {
+        tpc = 1;
+        while (tpc < tslab) tpc *= 2;
+    }
     while (tpc < kWarps && (tslab + tpc - 1) / tpc > kMaxClusterSplits) tpc *= 2;
     while (tpc > 1 && tpc / 2 >= tslab) tpc /= 2;  // no more than the slab has
     const int spc = kWarps / tpc, cluster = (tslab + tpc - 1) / tpc;
@@ -685,7 +935,15 @@ StreamPlan plan_lowm(int M, int N, int K, int G, int S, bool partials) {
     pl.cluster = cluster;
     pl.mode = kStreamGroup;
     pl.grid_x = (N / 16 + pl.spc - 1) / pl.spc * pl.cluster;
+    pl.to_partials = partials ? 1 : 0;
     return pl;
+}
+
+// Partials mode sums a split's tasks inside one block of 8 warps; group mode clusters of
+// at most 8 (the portable size) blocks.
+bool lowm_fits(const StreamPlan &pl) {
+    if (pl.mode == kStreamPartials) return pl.tps <= kWarps;
+    return pl.mode == kStreamGroup && pl.cluster <= kMaxClusterSplits;
 }
 
 namespace {
@@ -715,11 +973,23 @@ cudaError_t configure_lowm(size_t smem) {
 cudaError_t launch_lowm(const StreamPlan &pl, const void *x, long long ldx, const uint8_t *w8,
                         const uint8_t *ex, void *y, float *partials, int M, int N, int K, int G,
                         cudaStream_t stream, bool rows_exp) {
-    if (M < 1 || M > 8 || pl.nt8 != 1 || pl.m_chunks != 1 || pl.kt > kMaxKt) return cudaErrorInvalidValue;
+    if (M < 1 || M > 8 || pl.nt8 != 1 || pl.m_chunks != 1 || pl.kt > kMaxKt || !lowm_fits(pl))
+        return cudaErrorInvalidValue;
+    if ((pl.mode == kStreamPartials || pl.to_partials) ? partials == nullptr : y == nullptr)
+        return cudaErrorInvalidValue;
     const Options opt = options();
     LowParams prm;
     cudaError_t e = weight_map(w8, (long long)G * N, K, &prm.wmap);
     if (e != cudaSuccess) return e;
+    // x by one TMA box a task where every task starts on a 64-column chunk of its group
+    prm.xtma = 0;
+    if (K % 64 == 0 && pl.chunk_cols % 64 == 0 && pl.kt % 64 == 0) {
+        e = x_map(x, M, K, G, ldx, &prm.xmap);
+        if (e == cudaSuccess)
+            prm.xtma = 1;
+        else if (e != cudaErrorNotSupported)
+            return e;
+    }
     prm.x = static_cast<const uint16_t *>(x);
     prm.ldx = ldx;
     prm.ex = ex;
@@ -739,6 +1009,7 @@ cudaError_t launch_lowm(const StreamPlan &pl, const void *x, long long ldx, cons
     prm.cps = pl.cps;
     prm.mode = pl.mode;
     prm.tpc = pl.tpc;
+    prm.to_partials = pl.to_partials;
     prm.timeout_ns = opt.timeout_ns;
     prm.skip_loads = opt.skip_loads;
     prm.status = status_word();

@@ -5,11 +5,14 @@
 // the GPU's memory up front for its own arena (weights, KV cache) has no allocation left to
 // give, and a plugin or callback running inside such an engine may not call the allocator
 // at all.  This entry point needs nothing from them but the inputs and the output: it runs
-// the two-pass split-K GEMM (the fp32 partials pass, then the fixed-order reduce) with the
-// partials in a buffer compiled into the library -- a file-scope device array that every
-// GPU which loads the library holds until the process exits.
+// the two passes of the split-K GEMM -- bsf8_gemm_partials, then bsf8_splitk_reduce -- with
+// the partials in a buffer compiled into the library, a file-scope device array that every
+// GPU which loads the library holds until the process exits.  Those two passes run the
+// kernel bsf8_gemm runs for the same sizes and split count and sum the splits in the same
+// fixed order, so the result is bsf8_gemm's, bit for bit.
 #include "bsf8.h"
-#include "bsf8_internal.h"
+
+#include <cuda_runtime.h>
 
 #include <cstdint>
 
@@ -42,8 +45,6 @@ cudaError_t static_scratch_address(float **out) {
     return cudaSuccess;
 }
 
-inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 inline int status_of(cudaError_t e) {
     if (e == cudaSuccess) return BSF8_OK;
     if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
@@ -56,27 +57,25 @@ inline int status_of(cudaError_t e) {
 extern "C" int bsf8_gemm_static_scratch(const void *x, const uint8_t *w8, const uint8_t *exp,
                                         void *y, int M, int N, int K, int G, int split_k,
                                         int64_t ldx, bsf8_stream_t stream) {
-    // Argument rules of bsf8_gemm.
+    // Argument rules of bsf8_gemm (bsf8_gemm_partials checks the rest).
     if (!x || !w8 || !exp || !y) return BSF8_ERR_NULL;
     if (G < 1 || N < 32 || K < 32 || (N % 32) != 0 || (K % 32) != 0) return BSF8_ERR_SHAPE;
     if ((long long)G * N * (long long)K > (1LL << 46)) return BSF8_ERR_SHAPE;
     if (M < 1 || M > BSF8_MAX_M) return BSF8_ERR_SHAPE;
     if (split_k < 0 || split_k > K / 32) return BSF8_ERR_SHAPE;
-    if (ldx < (int64_t)G * K) return BSF8_ERR_STRIDE;
-    if (!aligned16(x) || (ldx % 8) != 0 || !aligned16(w8)) return BSF8_ERR_ALIGN;
 
-    const int S = split_k == 0 ? bsf8::auto_split(M, N, K, G) : split_k;
+    // the split count bsf8_gemm uses
+    const int S = split_k == 0 ? bsf8_gemm_auto_split(M, N, K, G) : split_k;
+    if (S < 1) return -S;
     // The partials P[S][M][G][N] must fit the compiled-in buffer.
     if ((size_t)S * M * G * N > kScratchFloats) return BSF8_ERR_WORKSPACE;
 
     float *P = nullptr;
-    cudaError_t e = static_scratch_address(&P);
+    const cudaError_t e = static_scratch_address(&P);
     if (e != cudaSuccess) return status_of(e);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // Every split writes all of its partials (an empty split writes +0) before the reduce
     // reads them, so nothing in the buffer needs clearing between calls.
-    const bsf8::StreamPlan pl = bsf8::plan_stream(M, N, K, G, S, true);
-    e = bsf8::launch_stream(pl, x, ldx, w8, exp, nullptr, P, M, N, K, G, s);
-    if (e != cudaSuccess) return status_of(e);
-    return status_of(bsf8::launch_splitk_reduce(P, y, S, (long long)M * G * N, s));
+    const int st = bsf8_gemm_partials(x, w8, exp, P, M, N, K, G, S, ldx, stream);
+    if (st != BSF8_OK) return st;
+    return bsf8_splitk_reduce(P, y, S, (int64_t)M * G * N, stream);
 }

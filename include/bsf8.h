@@ -11,8 +11,10 @@
  *
  * Conventions for every entry point:
  *   - Pointers are DEVICE pointers owned by the caller, except where a parameter says
- *     "host".  The library never allocates and keeps no hidden scratch: every buffer a
- *     call touches is named in its argument list.
+ *     "host".  The library never allocates, and every buffer a call touches is named in its
+ *     argument list -- with one exception: bsf8_gemm_static_scratch keeps its partials in a
+ *     buffer compiled into the library (BSF8_STATIC_SCRATCH_BYTES, 8 MiB on every GPU that
+ *     loads it), which calls that can overlap on the GPU must not use at the same time.
  *   - bf16 tensors are passed as void* holding IEEE bfloat16 bit patterns.
  *   - Row-major layouts:  w8[G][N][K] (uint8 e4m3fn codes),  exp[G][N/32][K/32]
  *     (uint8, byte = e + 127),  x[M][ldx] (bf16; group g uses columns [g*K, (g+1)*K)),
@@ -124,8 +126,8 @@ int bsf8_dequant(const uint8_t *w8, const uint8_t *exp, void *out, int G, int N,
  * The splits are summed inside one thread block, across a cluster of up to 8 blocks (16
  * for the decode-ahead tensor-core kernel, where the device schedules such clusters)
  * through distributed shared memory, or by the fixed-order reduce of a second pass, always
- * in the same fixed order as bsf8_gemm_partials followed by bsf8_splitk_reduce, which give
- * the same bits.
+ * in the same fixed order as bsf8_gemm_partials followed by bsf8_splitk_reduce, which run
+ * the same kernel (bsf8_gemm_kernel) and give the same bits.
  * The twin is treated as a static parameter: with programmatic dependent launch
  * (BSF8_OPT_PDL) the kernel starts reading w8 and exp while the kernel before it on the
  * stream may still run, if that kernel allows it (the library's kernels that write a
@@ -133,7 +135,8 @@ int bsf8_dequant(const uint8_t *w8, const uint8_t *exp, void *out, int G, int N,
  * trigger its dependents early).  x is read and y written only after that kernel ends
  * (before, x's rows may be prefetched into L2, which reads nothing into the call).
  * Errors: BSF8_ERR_NULL, BSF8_ERR_SHAPE, BSF8_ERR_ALIGN, BSF8_ERR_STRIDE,
- *         BSF8_ERR_WORKSPACE, BSF8_ERR_CUDA. */
+ *         BSF8_ERR_WORKSPACE, BSF8_ERR_CUDA; BSF8_ERR_VALUE when BSF8_OPT_GEMM_PATH forces a
+ *         kernel that cannot run the call. */
 int bsf8_gemm(const void *x, const uint8_t *w8, const uint8_t *exp, void *y,
               int M, int N, int K, int G, int split_k, int64_t ldx,
               void *workspace, size_t workspace_bytes, bsf8_stream_t stream);
@@ -149,8 +152,28 @@ size_t bsf8_gemm_workspace_bytes(int M, int N, int K, int G, int split_k);
  * size-only rule applies. */
 int bsf8_gemm_auto_split(int M, int N, int K, int G);
 
+/* Kernels of bsf8_gemm, as bsf8_gemm_kernel reports them and BSF8_OPT_GEMM_PATH forces them. */
+enum {
+    BSF8_KERNEL_STREAM = 2,          /* cp.async weight streaming, mma.sync (any M)          */
+    BSF8_KERNEL_DECODE_AHEAD = 4,    /* weights rebuilt into tensor memory before the        */
+                                     /* dependency wait, mma.sync (M <= 8)                   */
+    BSF8_KERNEL_TENSOR_CORE = 5,     /* tcgen05 MMAs on 128-row blocks (any M, token tiles   */
+                                     /* of 192)                                              */
+    BSF8_KERNEL_WIDE = 6,            /* wide weights, codes widened to f16 (M <= 8)          */
+    BSF8_KERNEL_DECODE_AHEAD_TC = 7  /* weights rebuilt into tensor memory as the tcgen05 A  */
+                                     /* operand before the dependency wait (M <= 32)         */
+};
+
+/* The kernel bsf8_gemm -- and bsf8_gemm_partials, bsf8_gemm_static_scratch -- runs for these
+ * sizes and split count (0 = the library's choice) under the current options and device: a
+ * BSF8_KERNEL_* value.  Negative: -BSF8_ERR_SHAPE for invalid sizes, -BSF8_ERR_VALUE when
+ * BSF8_OPT_GEMM_PATH forces a kernel that cannot run the call.  The choice never depends on
+ * whether the caller asks for y or for the fp32 partials. */
+int bsf8_gemm_kernel(int M, int N, int K, int G, int split_k);
+
 /* First pass alone: writes the fp32 partials P[S][M][G][N] (S = split_k >= 1, every
- * split written, empty splits as +0).  Same arguments as bsf8_gemm.
+ * split written, empty splits as +0) with the kernel bsf8_gemm runs for the same sizes and
+ * split count.  Same arguments as bsf8_gemm.
  *   partials device, out, fp32 [S][M][G][N], 16-byte aligned
  * Errors: as bsf8_gemm. */
 int bsf8_gemm_partials(const void *x, const uint8_t *w8, const uint8_t *exp,
@@ -208,9 +231,9 @@ int bsf8_gemm_rows(const void *x, const uint8_t *w8, const uint8_t *exp, void *y
  * The pages have no counterpart for this entry point; it serves callers that cannot
  * allocate device memory for a workspace -- e.g. a serving engine that has reserved all of
  * the GPU's memory for its own arena, or a plugin running inside one that may not call
- * the allocator.  It computes exactly what bsf8_gemm computes (same arguments, same
- * fixed-order split-K sum) as two passes -- the fp32 partials, then the fixed-order
- * reduce -- with the partials held in a buffer compiled into the library:
+ * the allocator.  It runs bsf8_gemm_partials and then bsf8_splitk_reduce with the split
+ * count bsf8_gemm uses (split_k 0: bsf8_gemm_auto_split), so its result equals bsf8_gemm's
+ * bit for bit, with the partials held in a buffer compiled into the library:
  *   - the buffer is BSF8_STATIC_SCRATCH_BYTES (8 MiB) of device memory that every GPU
  *     which loads the library holds until the process exits;
  *   - a call whose partials S*M*G*N*4 bytes (S = the split count used) exceed it returns
@@ -222,7 +245,7 @@ int bsf8_gemm_rows(const void *x, const uint8_t *w8, const uint8_t *exp, void *y
  *     the caller;
  *   - the first call on a device looks up the buffer's device address (a host call,
  *     cudaGetSymbolAddress), so make that first call before any stream capture.
- * Errors: as bsf8_gemm (BSF8_ERR_WORKSPACE as described). */
+ * Errors: as bsf8_gemm (BSF8_ERR_WORKSPACE as described: a call at exactly the limit runs). */
 #define BSF8_STATIC_SCRATCH_BYTES (8u * 1024u * 1024u)
 
 int bsf8_gemm_static_scratch(const void *x, const uint8_t *w8, const uint8_t *exp, void *y,
@@ -260,8 +283,11 @@ int bsf8_device_status(int *status, bsf8_stream_t stream);
 enum {
     BSF8_OPT_PDL = 1,              /* 1 (default): programmatic dependent launch on    */
     BSF8_OPT_WAIT_TIMEOUT_NS = 2,  /* bound of every in-kernel wait (default 2e9 ns)   */
-    BSF8_OPT_DEBUG_SKIP_LOADS = 3, /* test only: the TMA-ring GEMM issues no weight    */
-                                   /* loads, so its waits run out (BSF8_ERR_TIMEOUT)   */
+    BSF8_OPT_DEBUG_SKIP_LOADS = 3, /* test only: the GEMM kernels that wait on         */
+                                   /* mbarriers (decode-ahead, decode-ahead tensor-    */
+                                   /* core, tensor-core, wide-weight) issue no weight  */
+                                   /* loads, so their bounded waits run out and the    */
+                                   /* call ends with BSF8_ERR_TIMEOUT in the status    */
     BSF8_OPT_GEMM_PATH = 4         /* 0 (default): the kernel chosen by shape:         */
                                    /*  - up to 8 token rows: the decode-ahead kernel   */
                                    /*    when its grid fits two blocks an SM, else the */
@@ -277,17 +303,14 @@ enum {
                                    /*    SM, the streaming kernel otherwise (up to 24  */
                                    /*    rows);                                        */
                                    /*  - beyond 24 rows: the tensor-core kernel.       */
-                                   /* Forced: 1: the shared-memory TMA-ring kernel     */
-                                   /* (split_k <= 8); 2: the streaming kernel; 3: the  */
-                                   /* TMA-fed kernel (M <= 16); 4: the decode-ahead    */
-                                   /* kernel (M <= 8); 5: the tensor-core (tcgen05)    */
-                                   /* kernel (M <= 192 a token tile); 6: the wide-     */
-                                   /* weight kernel (M <= 8; K and the split's columns */
-                                   /* multiples of 128, at most 6144 columns a split); */
-                                   /* 7: the decode-ahead tensor-core kernel (M <= 32, */
-                                   /* S x ceil(split columns / 512) <= 16).            */
-                                   /* A forced kernel that does not apply to a call    */
-                                   /* falls back to 0.                                 */
+                                   /* Else a BSF8_KERNEL_* value forces that kernel:   */
+                                   /* 2 streaming (any call); 4 decode-ahead (M <= 8); */
+                                   /* 5 tensor-core; 6 wide-weight (M <= 8; K and the  */
+                                   /* split's columns multiples of 128, at most 6144   */
+                                   /* columns a split); 7 decode-ahead tensor-core     */
+                                   /* (M <= 32, S x ceil(split columns / 512) <= 16).  */
+                                   /* A call the forced kernel cannot run returns      */
+                                   /* BSF8_ERR_VALUE (see bsf8_gemm_kernel).           */
 };
 /* Errors: BSF8_ERR_VALUE for an unknown option or a negative value. */
 int bsf8_set_option(int option, int64_t value);

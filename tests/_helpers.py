@@ -48,13 +48,15 @@ def bf16_ord(b):
 
 def gemm_error(y_bits, ref_bits):
     """(max |y - ref| / rms(ref) over outputs that differ by more than one rounding step,
-    fraction within 1 bf16 ulp, nan mismatches).
+    fraction within 1 bf16 ulp, nan mismatches, literal max |y - ref| / rms(ref) over every
+    output).
 
     Two fp32 sums of the same products in different orders can round to adjacent bf16
     values (the pages report such one-ulp differences as due to the accumulation order
-    alone), and one ulp of an output above ~2.6 rms exceeds 1e-2 rms: those single
-    rounding flips are held to the within-1-ulp fraction, every other difference to the
-    1e-2 rms bound."""
+    alone), and one ulp of an output above ~2.6 rms exceeds 1e-2 rms: under the modified
+    tolerance those single rounding flips are held to the within-1-ulp fraction and every
+    other difference to the 1e-2 rms bound.  The literal figure applies the bound to every
+    output, flips included."""
     y = oracle.bf16_bits_to_f32(y_bits).astype(np.float64)
     r = oracle.bf16_bits_to_f32(ref_bits).astype(np.float64)
     nan_mismatch = int(np.count_nonzero(np.isnan(y) != np.isnan(r)))
@@ -63,13 +65,19 @@ def gemm_error(y_bits, ref_bits):
     dord = np.abs(bf16_ord(y_bits) - bf16_ord(ref_bits))
     far = ok & (dord > 1)
     max_rel = float(np.max(np.abs(y[far] - r[far])) / rms) if far.any() and rms > 0 else 0.0
+    literal = float(np.max(np.abs(y[ok] - r[ok])) / rms) if ok.any() and rms > 0 else 0.0
     within = float(np.mean(dord[ok] <= 1)) if ok.any() else 1.0
-    return max_rel, within, nan_mismatch
+    return max_rel, within, nan_mismatch, literal
 
 
-def assert_gemm_close(y_bits, ref_bits, what=""):
-    max_rel, within, nan_mismatch = gemm_error(y_bits, ref_bits)
+def assert_gemm_close(y_bits, ref_bits, what="", literal=False):
+    """The modified tolerance (single bf16 rounding flips excluded from the max bound, at
+    least 99.9% of outputs within one ulp); with literal=True also the bound itself,
+    max |y - ref| <= 1e-2 rms(ref) over every output."""
+    max_rel, within, nan_mismatch, lit = gemm_error(y_bits, ref_bits)
     assert nan_mismatch == 0, f"{what}: NaN pattern differs"
     assert max_rel <= REL_MAX, f"{what}: max|dy|/rms = {max_rel:.3g}"
     assert within >= ULP_FRACTION, f"{what}: only {within:.5f} within 1 ulp"
+    if literal:
+        assert lit <= REL_MAX, f"{what}: literal max|dy|/rms over all outputs = {lit:.3g}"
     return max_rel, within

@@ -143,6 +143,35 @@ def test_workspace_and_auto_split(lib):
         assert 1 <= s <= 8
 
 
+def test_gemm_kernel_query_validation(lib):
+    """bsf8_gemm_kernel: invalid sizes give -BSF8_ERR_SHAPE; a forced kernel that cannot run
+    the call gives -BSF8_ERR_VALUE (host logic only); the kernels removed from the library
+    (1, 3) and unknown values cannot be forced."""
+    q = lib.bsf8_gemm_kernel
+    assert q(0, 1024, 4096, 2, 8) == -SHAPE
+    assert q(6, 1000, 4096, 2, 8) == -SHAPE
+    assert q(6, 1024, 4096, 2, 129) == -SHAPE
+    try:
+        assert lib.bsf8_set_option(4, 4) == OK           # decode-ahead: up to 8 rows
+        assert q(12, 1024, 4096, 2, 8) == -VALUE
+        assert q(6, 1024, 4096, 2, 8) == 4
+        assert lib.bsf8_set_option(4, 6) == OK           # wide-weight: 128-column splits
+        assert q(6, 5120, 576, 1, 1) == -VALUE
+        assert lib.bsf8_set_option(4, 2) == OK           # streaming: any call
+        assert q(100, 1024, 4096, 2, 3) == 2
+        for bad in (1, 3, 8):
+            assert lib.bsf8_set_option(4, bad) == VALUE
+    finally:
+        lib.bsf8_set_option(4, 0)
+    # a refused forced kernel is refused by the GEMM entry points too, before any CUDA call
+    try:
+        assert lib.bsf8_set_option(4, 4) == OK
+        assert _gemm(lib, M=12) == VALUE
+        assert lib.bsf8_gemm_partials(A, B, C, D, 12, 1024, 4096, 2, 8, 8192, None) == VALUE
+    finally:
+        lib.bsf8_set_option(4, 0)
+
+
 def test_options_roundtrip(lib):
     assert lib.bsf8_get_option(1) == 1
     assert lib.bsf8_set_option(1, 0) == OK and lib.bsf8_get_option(1) == 0

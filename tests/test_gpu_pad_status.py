@@ -59,15 +59,14 @@ def test_down_proj_padding_leaves_output_bitwise_unchanged(bsf8_lib):
     assert np.array_equal(y6, y7)
 
 
-@pytest.mark.parametrize("path,M", [(0, 4), (3, 12), (1, 4), (0, 40), (6, 4), (7, 4), (7, 20)])
-def test_timeout_is_reported_without_hanging(bsf8_lib, path, M):
+@pytest.mark.parametrize("path,M,kernel", [(0, 4, 4), (0, 40, 5), (6, 4, 6), (7, 4, 7), (7, 20, 7)])
+def test_timeout_is_reported_without_hanging(bsf8_lib, path, M, kernel):
     """With the test-only option that suppresses the weight loads, the mbarrier waits of
-    the decode-ahead GEMM (path 0 at M = 4), the TMA-fed GEMM (path 3), the TMA-ring GEMM
-    (path 1), the tensor-core GEMM (path 0 at M = 40), the wide-weight GEMM (path 6) and
-    the decode-ahead tensor-core GEMM (path 7, 16- and 32-token tiles) run out after the
-    shortened
-    bound; the kernel records BSF8_ERR_TIMEOUT, writes nothing and returns.  Normal calls
-    work again afterwards."""
+    the decode-ahead GEMM (path 0 at M = 4), the tensor-core GEMM (path 0 at M = 40), the
+    wide-weight GEMM (path 6) and the decode-ahead tensor-core GEMM (path 7, 16- and
+    32-token tiles) run out after the shortened bound; the kernel records
+    BSF8_ERR_TIMEOUT, writes nothing and returns.  Normal calls work again afterwards.
+    The library confirms which kernel each case runs."""
     w8, ex = wl.TINY.weights()
     x = wl.TINY.x(M=M)
     w8_d, ex_d, x_d = to_dev_u8(w8), to_dev_u8(ex), to_dev_bf16(x)
@@ -79,6 +78,7 @@ def test_timeout_is_reported_without_hanging(bsf8_lib, path, M):
         bsf8.set_option(bsf8.OPT_WAIT_TIMEOUT_NS, 2_000_000)     # 2 ms
         bsf8.set_option(bsf8.OPT_DEBUG_SKIP_LOADS, 1)
         for S in (1, 4):
+            assert bsf8.gemm_kernel(M, 256, 512, 1, S) == kernel
             bsf8.gemm(x_d, w8_d, ex_d, split_k=S, out=y)
             assert bsf8.device_status() == 7
             assert torch.all(y == 7.0)                            # nothing written

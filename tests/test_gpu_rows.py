@@ -69,7 +69,7 @@ def test_gemm_rows_matches_oracle(bsf8_lib, M, S):
 def test_gemm_rows_one_hot_and_repeated_block_exponents(bsf8_lib):
     """One-hot x over all codes x exponents (one exponent per row): bit-exact.  And with a
     block twin's exponents repeated over rows the per-row GEMM gives the block GEMM's bits
-    on the same (streaming) kernel."""
+    on the same kernel (the decode-ahead kernel at 6 rows)."""
     M, N, K = 8, 256 * 32, 32
     w8 = (np.arange(N * K) % 256).astype(np.uint8).reshape(1, N, K)
     ex = (np.arange(N) % 256).astype(np.uint8).reshape(1, N, 1)
@@ -82,8 +82,9 @@ def test_gemm_rows_one_hot_and_repeated_block_exponents(bsf8_lib):
     bw8, bex = wk.weights()
     x = wk.x(M=6)
     x_d, w8_d = to_dev_bf16(x), to_dev_u8(bw8)
-    bsf8.set_option(bsf8.OPT_GEMM_PATH, 2)  # the block GEMM on the streaming kernel too
+    bsf8.set_option(bsf8.OPT_GEMM_PATH, 4)  # the block GEMM on the decode-ahead kernel too
     try:
+        assert bsf8.gemm_kernel(6, wk.N, wk.K, wk.G, 8) == 4
         yb = bf16_bits(bsf8.gemm(x_d, w8_d, to_dev_u8(bex), split_k=8))
     finally:
         bsf8.set_option(bsf8.OPT_GEMM_PATH, 0)

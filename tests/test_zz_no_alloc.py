@@ -2,9 +2,12 @@
 
 Callers such as a serving engine that has reserved all GPU memory for its own arena (or a
 plugin running inside one) have no workspace to give; this entry point keeps its split-K
-partials in a buffer compiled into the library instead.  The test calls it through the C
-ABI, twice in a row on different inputs, and checks each result against bsf8_gemm within
-the GEMM tolerance of the other tests.  The file is named so that pytest collects it last.
+partials in a buffer compiled into the library instead.  The tests call it through the C
+ABI, several calls in a row on different inputs, and check each result against the CPU
+oracle within the GEMM tolerance of the other tests, and bit for bit against bsf8_gemm
+(which runs the same kernel and sums the splits in the same order); the automatic split
+(split_k = 0) is covered, and so are partials of exactly the buffer's size and just past
+it.  The file is named so that pytest collects it last.
 """
 import ctypes
 
@@ -13,13 +16,14 @@ import pytest
 import torch
 
 import block_scaled_fp8_weight_gb300 as bsf8
+import oracle
 from block_scaled_fp8_weight_gb300 import workloads as wl
 from _helpers import assert_gemm_close, bf16_bits, to_dev_bf16, to_dev_u8
 
 pytestmark = pytest.mark.gpu
 
 STATIC_SCRATCH_BYTES = 8 * 1024 * 1024
-ERR_WORKSPACE = 4
+OK, ERR_WORKSPACE = 0, 4
 
 
 def _entry(lib):
@@ -37,22 +41,56 @@ def _call(fn, x_d, w8_d, ex_d, y_d, M, N, K, G, S):
               M, N, K, G, S, x_d.stride(0), stream)
 
 
-def test_static_scratch_gemm_matches_bsf8_gemm_on_two_calls(bsf8_lib):
+def test_static_scratch_gemm_matches_oracle_and_bsf8_gemm(bsf8_lib):
     fn = _entry(bsf8_lib)
-    cases = [(wl.WO_A, 6, 8), (wl.DOWN_PROJ, 6, 4)]
-    for wk, M, S in cases:                       # two calls in a row, different inputs
+    cases = [(wl.WO_A, 6, 8), (wl.DOWN_PROJ, 6, 4), (wl.WO_A, 6, 0), (wl.DOWN_PROJ, 6, 0),
+             (wl.TINY, 4, 4)]
+    for wk, M, S in cases:                       # calls in a row, different inputs
         w8, ex = wk.weights()
         x = wk.x(M=M)
         w8_d, ex_d, x_d = to_dev_u8(w8), to_dev_u8(ex), to_dev_bf16(x)
-        assert S * M * wk.G * wk.N * 4 <= STATIC_SCRATCH_BYTES
+        S_used = S or bsf8.auto_split(M, wk.N, wk.K, wk.G)
+        assert S_used * M * wk.G * wk.N * 4 <= STATIC_SCRATCH_BYTES
         y_d = torch.empty((M, wk.G, wk.N), dtype=torch.bfloat16, device="cuda")
-        assert _call(fn, x_d, w8_d, ex_d, y_d, M, wk.N, wk.K, wk.G, S) == 0
+        assert _call(fn, x_d, w8_d, ex_d, y_d, M, wk.N, wk.K, wk.G, S) == OK
         ref = bf16_bits(bsf8.gemm(x_d, w8_d, ex_d, split_k=S))
         assert bsf8.device_status() == 0
-        assert_gemm_close(bf16_bits(y_d), ref, f"{wk.name} S={S}")
+        got = bf16_bits(y_d)
+        assert np.array_equal(got, ref), f"{wk.name} S={S}"
+        assert_gemm_close(got, oracle.gemm(x, w8, ex), f"{wk.name} S={S}")
 
 
-def test_static_scratch_rejects_partials_beyond_its_size(bsf8_lib):
+def test_static_scratch_at_and_past_its_size(bsf8_lib):
+    """Partials of exactly 8 MiB run (S = 8, M = 128, G = 1, N = 2048: 8*128*2048*4 bytes);
+    one more token row is refused with BSF8_ERR_WORKSPACE and writes nothing."""
+    fn = _entry(bsf8_lib)
+    G, N, K, S = 1, 2048, 4096, 8
+    r = wl.rng(8 << 20)
+    w8 = wl.codes(r, (G, N, K))
+    ex = wl.exponents(r, (G, N // 32, K // 32), 115, 127)
+    w8_d, ex_d = to_dev_u8(w8), to_dev_u8(ex)
+    M = 128
+    assert S * M * G * N * 4 == STATIC_SCRATCH_BYTES
+    x = wl.activations(r, M, G * K)
+    x_d = to_dev_bf16(x)
+    y_d = torch.empty((M, G, N), dtype=torch.bfloat16, device="cuda")
+    assert _call(fn, x_d, w8_d, ex_d, y_d, M, N, K, G, S) == OK
+    ref = bf16_bits(bsf8.gemm(x_d, w8_d, ex_d, split_k=S))
+    assert bsf8.device_status() == 0
+    got = bf16_bits(y_d)
+    assert np.array_equal(got, ref)
+    rows = [0, 64, M - 1]
+    assert_gemm_close(got[rows], oracle.gemm(x[rows], w8, ex), "8 MiB of partials")
+
+    M1 = M + 1
+    x1_d = to_dev_bf16(wl.activations(r, M1, G * K))
+    y1_d = torch.full((M1, G, N), 3.0, dtype=torch.bfloat16, device="cuda")
+    assert _call(fn, x1_d, w8_d, ex_d, y1_d, M1, N, K, G, S) == ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert torch.all(y1_d == 3.0)
+
+
+def test_static_scratch_rejects_partials_far_beyond_its_size(bsf8_lib):
     fn = _entry(bsf8_lib)
     wk = wl.MID                                   # G=4, N=1024, K=4096
     M, S = 192, 8                                 # 8*192*4*1024*4 B = 25 MiB > 8 MiB
