@@ -11,7 +11,13 @@ is no model checkpoint here).
 Prints ONE JSON line on rank 0.  `value` is the weight-stream bandwidth (e4m3 codes +
 exponent bytes per call / time per call) summed over all ranks; `e2e` is the same metric
 measured through the public Python API with the activations copied from pinned host
-memory and the outputs copied back inside the timed region.
+memory and the outputs copied back inside the timed region.  `configs` times every other
+config of the hot path (make_twin, dequant, pad-K, the GEMM at the tiny, wo_a, down_proj,
+mid-row and gate_up/head sweep shapes, per-row scales, fp32 output, prefill-sized rows),
+each over enough weight copies to stream at least twice the L2, as us/call (median over
+graph replays, p10/p90), weight GB/s, fraction of the measured HBM peak, the kernel that
+ran and the split it used.  The SM clock is sampled inside the timed region (each SM's
+cycle counter against the global timer) as well as by nvidia-smi.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl bsf8|reference]
 
@@ -24,6 +30,7 @@ exchange step, so no collective runs on the data path; only the timing is combin
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -67,6 +74,8 @@ def parse_args(argv=None):
     p.add_argument("--suite", action="store_true",
                    help="time every hot-path row (make_twin, dequant, pad-K, the GEMM at every "
                         "config) and print one JSON line per row instead of the headline line")
+    p.add_argument("--no-configs", action="store_true",
+                   help="leave the per-config map out of the headline line")
     return p.parse_args(argv)
 
 
@@ -158,7 +167,7 @@ def recorded_traffic():
 
 
 class ClockSampler:
-    """Samples nvidia-smi SM clocks and throttle reasons every 100 ms in the background."""
+    """Samples nvidia-smi SM clocks and throttle reasons every ~50 ms in the background."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -185,7 +194,7 @@ class ClockSampler:
                 self.samples.append((time.time(), float(f[1]), float(f[2]), reasons))
             except Exception:
                 pass
-            self._stop.wait(0.1)
+            self._stop.wait(0.05)
 
     def start(self):
         self._thr = threading.Thread(target=self._poll, daemon=True)
@@ -228,62 +237,102 @@ def config_dict(wk, pdl=True):
     }
 
 
-def cpu_oracle_baseline(wk, seconds: float):
-    """The oracle, as it stands, on one host core: whole wo_a layer calls at M=6."""
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_slices(wk, x, w8, ex, parts: int):
+    """The layer's weight rows cut into `parts` contiguous slices of whole 32-row blocks
+    (each output keeps its own index-order sum, so the slices give the layer's bits)."""
+    import numpy as np
+    nb = wk.N // 32
+    bounds = [round(i * nb / parts) * 32 for i in range(parts + 1)]
+    return [(np.ascontiguousarray(w8[:, a:b]), np.ascontiguousarray(ex[:, a // 32:b // 32]))
+            for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
+
+
+def oracle_layer_time(x, slices, threads: int, seconds: float):
+    """Seconds per whole-layer call of the oracle with the slices run on `threads` threads
+    (the oracle's C function runs without the interpreter lock)."""
+    import concurrent.futures as cf
     import oracle
+    run = lambda sl: oracle.gemm(x, sl[0], sl[1])
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(run, slices))                       # load + first touch
+        calls, t0 = 0, time.perf_counter()
+        while True:
+            list(ex.map(run, slices))
+            calls += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                return el / calls
+
+
+def cpu_oracle_baseline(wk, seconds: float):
+    """The oracle, as it stands, on the host cores: whole wo_a layer calls at M=6, on one
+    thread and on one thread per core (the layer's rows split across them), each the
+    median of 3 runs."""
     w8, ex = wk.weights(copy=0)
     x = wk.x(copy=0)
-    oracle.gemm(x, w8, ex)                       # load + first touch
-    calls, t0 = 0, time.perf_counter()
-    while True:
-        oracle.gemm(x, w8, ex)
-        calls += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    return {"value": wk.weight_bytes * calls / el / 1e9, "unit": "GB/s", "cores": 1,
-            "kind": "oracle", "us_per_call": el / calls * 1e6,
-            "sample": f"{calls} whole wo_a layer calls (G=2, N=1024, K=4096, M=6), "
-                      f"{el:.1f} s on one host core"}
+    cores = host_cores()
+    one = oracle_slices(wk, x, w8, ex, 1)
+    many = oracle_slices(wk, x, w8, ex, 4 * cores)
+    per = max(0.5, seconds / 6.0)
+    t1 = statistics.median(oracle_layer_time(x, one, 1, per) for _ in range(3))
+    tn = statistics.median(oracle_layer_time(x, many, cores, per) for _ in range(3))
+    return {"value": wk.weight_bytes / tn / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "us_per_call": tn * 1e6,
+            "one_thread": {"value": wk.weight_bytes / t1 / 1e9, "us_per_call": t1 * 1e6},
+            "sample": f"whole wo_a layer calls (G=2, N=1024, K=4096, M=6), median of 3 runs of "
+                      f"~{per:.1f} s: one thread per host core ({cores} cores, the layer's weight rows "
+                      f"split into {len(many)} slices), and one thread"}
 
 
 def run_reference(args, world, rank):
-    """The CPU oracle as the reference arm: each step is a bounded slice of one layer
-    call (a contiguous range of weight rows), timed on one host core."""
+    """The CPU oracle as the reference arm, on all host cores: each step is a bounded slice
+    of one layer call (a contiguous range of weight rows, split across one thread per core)."""
     if rank != 0:
         return None
     import oracle
     wk = workload()
     w8, ex = wk.weights(copy=0)
     x = wk.x(copy=0)
+    cores = host_cores()
     budget = 90.0
     probe_rows = 32
     t0 = time.perf_counter()
     oracle.gemm(x, w8[:, :probe_rows], ex[:, :probe_rows // 32])
     t_probe = max(time.perf_counter() - t0, 1e-6)
     per_step = budget / max(1, args.steps + args.warmup)
-    rows = int(min(wk.N, max(probe_rows, (per_step / t_probe) * probe_rows)) // 32 * 32)
+    rows = int(min(wk.N, max(probe_rows, (per_step / t_probe) * probe_rows * cores)) // 32 * 32)
     rows = max(32, rows)
-    ws, es = w8[:, :rows], ex[:, :rows // 32]
-    for _ in range(args.warmup):
-        oracle.gemm(x, ws, es)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle.gemm(x, ws, es)
-    el = time.perf_counter() - t0
+    sub = dataclasses.replace(wk, N=rows)
+    slices = oracle_slices(sub, x, w8[:, :rows], ex[:, :rows // 32], min(rows // 32, 4 * cores))
+    import concurrent.futures as cf
+    run = lambda sl: oracle.gemm(x, sl[0], sl[1])
+    with cf.ThreadPoolExecutor(max_workers=cores) as pool:
+        for _ in range(args.warmup):
+            list(pool.map(run, slices))
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            list(pool.map(run, slices))
+        el = time.perf_counter() - t0
     bytes_step = wk.G * rows * wk.K + wk.G * (rows // 32) * (wk.K // 32)
     value = bytes_step * args.steps / el / 1e9
     sample = (f"each step: rows [0, {rows}) of both groups of one wo_a layer (M=6), "
-              f"{rows / wk.N:.4f} of a layer call, one host core")
+              f"{rows / wk.N:.4f} of a layer call, on {cores} host cores (one thread per core)")
     cfg = config_dict(wk, pdl=False)
-    cfg["launch"] = "CPU oracle (plain C, binary32 index-order sum), single thread"
+    cfg["launch"] = "CPU oracle (plain C, binary32 index-order sum), one thread per host core"
     return {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": cfg, "impl": "reference",
         "us_per_call": el / args.steps * 1e6 * wk.N / rows,
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -299,13 +348,17 @@ def build_layers(wk, device, copies=LAYERS):
     return layers
 
 
-def time_graph(layers, wk, steps, warmup, pdl, stream, sampler=None):
+def time_graph(layers, wk, steps, warmup, pdl, stream, per_step=False, clock_probe=None):
     """Captures the 43 calls of one step in a CUDA graph; replays `warmup` untimed then
-    `steps` timed steps; returns (seconds, wall t0, wall t1)."""
+    `steps` timed steps between one pair of CUDA events; returns (seconds, wall t0, wall t1,
+    per-step seconds or None).  per_step adds an event between steps (same stream, nothing
+    else changes); clock_probe (an int64 [nsm, 2] tensor pair) samples every SM's cycle
+    counter right before and right after the timed region."""
     import torch
     import block_scaled_fp8_weight_gb300 as bsf8
     bsf8.set_option(bsf8.OPT_PDL, 1 if pdl else 0)
     outs = [torch.empty((wk.M, wk.G, wk.N), dtype=torch.bfloat16, device=stream.device) for _ in layers]
+    steps_s = None
     try:
         with torch.cuda.stream(stream):
             for (w8, ex, x), y in zip(layers, outs):          # eager warm call (module load)
@@ -318,18 +371,39 @@ def time_graph(layers, wk, steps, warmup, pdl, stream, sampler=None):
             for _ in range(warmup):
                 g.replay()
             stream.synchronize()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1 if per_step else 2)]
             w0 = time.time()
-            e0.record(stream)
-            for _ in range(steps):
+            if clock_probe is not None:
+                bsf8.sm_clock_sample(clock_probe[0], stream=stream)
+            ev[0].record(stream)
+            for i in range(steps):
                 g.replay()
-            e1.record(stream)
+                if per_step:
+                    ev[i + 1].record(stream)
+            ev[-1].record(stream)
+            if clock_probe is not None:
+                bsf8.sm_clock_sample(clock_probe[1], stream=stream)
             stream.synchronize()
             w1 = time.time()
+            if per_step:
+                steps_s = [ev[i].elapsed_time(ev[i + 1]) / 1e3 for i in range(steps)]
     finally:
         bsf8.set_option(bsf8.OPT_PDL, 1)
-    return e0.elapsed_time(e1) / 1e3, w0, w1
+    return ev[0].elapsed_time(ev[-1]) / 1e3, w0, w1, steps_s
+
+
+def region_clock(probe):
+    """Median over SMs of each SM's average clock (MHz) between the two samples."""
+    a = probe[0].cpu().numpy().astype("float64")
+    b = probe[1].cpu().numpy().astype("float64")
+    ok = (a[:, 0] > 0) & (b[:, 0] > a[:, 0])
+    if not ok.any():
+        return None
+    mhz = (b[ok, 1] - a[ok, 1]) / (b[ok, 0] - a[ok, 0]) * 1e3
+    return {"sm_mhz_median": float(statistics.median(mhz)), "sm_mhz_min": float(mhz.min()),
+            "sm_mhz_max": float(mhz.max()), "sms": int(ok.sum()),
+            "how": "each SM's cycle counter against the global ns timer, sampled by a one-warp "
+                   "block per SM right before and right after the timed region (bsf8_sm_clock_sample)"}
 
 
 def time_eager(layers, wk, steps, stream):
@@ -433,17 +507,29 @@ def profile_load_time(which, calls, device):
     return 0
 
 
-def run_suite(device, peak):
-    """Every hot-path row timed on the GPU: each call of a row in a CUDA graph over enough
-    distinct seeded copies that the inputs exceed the L2 (PDL on), reported as us/call and
-    as bytes moved per call (the row's algorithmic bytes) over time, against the HBM peak."""
+L2_BYTES = 129e6   # GB300 L2; weight copies are cycled so that each config streams >= 2x this
+
+
+def copies_for(nbytes: int, least: int = 43, most: int = 2048) -> int:
+    """Distinct input copies a config cycles through: at least 43 (one per layer, as on the
+    pages) and enough that a pass streams at least twice the L2."""
+    return int(max(least, min(most, -(-int(2 * L2_BYTES) // max(1, int(nbytes))))))
+
+
+def configs_map(device, peak, verbose=False):
+    """Every config of the hot path timed on the GPU: each row's calls in a CUDA graph of a
+    dependent chain (PDL on) over enough distinct seeded copies that a pass streams at
+    least twice the L2, replayed `reps` times with an event pair per replay; us/call is the
+    median over replays (p10/p90 beside it).  GB/s counts the weight stream (codes +
+    exponent bytes) for the GEMM rows and all bytes moved for make_twin, dequant and pad-K."""
     import ctypes
     import torch
     import block_scaled_fp8_weight_gb300 as bsf8
     from block_scaled_fp8_weight_gb300 import workloads as wl
     lib = bsf8.load()
     stream = torch.cuda.Stream(device=device)
-    out = []
+    out = {}
+    t_start = time.time()
 
     def graph_time(calls, reps):
         with torch.cuda.stream(stream):
@@ -457,67 +543,66 @@ def run_suite(device, peak):
             for _ in range(3):
                 g.replay()
             stream.synchronize()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(reps):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+            ev[0].record(stream)
+            for i in range(reps):
                 g.replay()
-            e1.record(stream)
+                ev[i + 1].record(stream)
             stream.synchronize()
         if bsf8.device_status() != 0:
             raise RuntimeError("a kernel reported a timeout")
-        return e0.elapsed_time(e1) * 1e-3 / (reps * len(calls))
+        per = sorted(ev[i].elapsed_time(ev[i + 1]) * 1e-3 / len(calls) for i in range(reps))
+        q = lambda f: per[min(len(per) - 1, int(f * len(per)))]
+        return q(0.5), q(0.1), q(0.9)
 
-    def emit(row, config, t, nbytes, weight_bytes=None):
-        line = {"row": row, "config": config, "us_per_call": t * 1e6,
-                "GBps": nbytes / t / 1e9, "frac_of_hbm_peak": nbytes / t / 1e9 / peak,
-                "bytes_per_call": nbytes}
-        if weight_bytes is not None:
-            line["weight_stream_GBps"] = weight_bytes / t / 1e9
-            line["weight_frac"] = weight_bytes / t / 1e9 / peak
-        out.append(line)
-        print(json.dumps(line), flush=True)
+    def emit(row, t, nbytes, copies, **extra):
+        t50, t10, t90 = t
+        e = {"us": round(t50 * 1e6, 3), "us_p10": round(t10 * 1e6, 3), "us_p90": round(t90 * 1e6, 3),
+             "GBps": round(nbytes / t50 / 1e9, 1), "frac": round(nbytes / t50 / 1e9 / peak, 4),
+             "copies": copies}
+        e.update(extra)
+        out[row] = e
+        if verbose:
+            print(json.dumps({"row": row, **e}), flush=True)
 
     sp = lambda: ctypes.c_void_p(stream.cuda_stream)
     ptr = lambda t: ctypes.c_void_p(t.data_ptr())
-    # make_twin and dequant on the wo_a shape, 43 copies (cold)
+    reps_for = lambda per_call_s, ncalls: int(min(200, max(5, 0.03 / max(1e-7, per_call_s * ncalls))))
+
+    # a1 make_twin and a2' dequant on the wo_a shape; a7 pad-K on down_proj
     wk = wl.WO_A
     G, N, K = wk.G, wk.N, wk.K
-    twins = [wk.weights(copy=c) for c in range(LAYERS)]
+    n = copies_for(3 * G * N * K)
+    twins = [wk.weights(copy=c) for c in range(n)]
     w8s = [torch.from_numpy(a).to(device) for a, _ in twins]
     exs = [torch.from_numpy(b).to(device) for _, b in twins]
     wbf = [bsf8.dequant(a, b) for a, b in zip(w8s, exs)]
     o8 = [torch.empty_like(a) for a in w8s]
     oe = [torch.empty_like(b) for b in exs]
     ok = [torch.empty_like(b) for b in exs]
-    acc = torch.empty((LAYERS,), dtype=torch.int32, device=device)
+    acc = torch.empty((n,), dtype=torch.int32, device=device)
     calls = [lambda i=i: lib.bsf8_make_twin(ptr(wbf[i]), ptr(o8[i]), ptr(oe[i]), ptr(ok[i]),
                                             ctypes.c_void_p(acc.data_ptr() + 4 * i), G, N, K, sp())
-             for i in range(LAYERS)]
-    t = graph_time(calls, 20)
-    emit("a1 make_twin", f"G={G} N={N} K={K} bf16 -> twin, {LAYERS} copies", t,
-         2 * G * N * K + G * N * K + 2 * G * (N // 32) * (K // 32))
-    outs = [torch.empty((G, N, K), dtype=torch.bfloat16, device=device) for _ in range(LAYERS)]
+             for i in range(n)]
+    emit("a1 make_twin wo_a", graph_time(calls, 10), 3 * G * N * K + 2 * G * (N // 32) * (K // 32), n)
+    outs = [torch.empty((G, N, K), dtype=torch.bfloat16, device=device) for _ in range(n)]
     calls = [lambda i=i: lib.bsf8_dequant(ptr(w8s[i]), ptr(exs[i]), ptr(outs[i]), G, N, K, sp())
-             for i in range(LAYERS)]
-    t = graph_time(calls, 20)
-    emit("a2' dequant", f"G={G} N={N} K={K} twin -> bf16, {LAYERS} copies", t,
-         G * N * K + G * (N // 32) * (K // 32) + 2 * G * N * K)
-    del wbf, o8, oe, ok, outs
-    # pad-K on the down_proj twin (576 -> 640), 43 copies
+             for i in range(n)]
+    emit("a2' dequant wo_a", graph_time(calls, 10), 3 * G * N * K + G * (N // 32) * (K // 32), n)
+    del wbf, o8, oe, ok, outs, w8s, exs, twins
     dk = wl.DOWN_PROJ
-    dt = [dk.weights(copy=c) for c in range(LAYERS)]
+    Kp = 640
+    n = copies_for(dk.N * (dk.K + Kp))
+    dt = [dk.weights(copy=c) for c in range(n)]
     dw = [torch.from_numpy(a).to(device) for a, _ in dt]
     de = [torch.from_numpy(b).to(device) for _, b in dt]
-    Kp = 640
-    pw = [torch.empty((1, dk.N, Kp), dtype=torch.uint8, device=device) for _ in range(LAYERS)]
-    pe = [torch.empty((1, dk.N // 32, Kp // 32), dtype=torch.uint8, device=device) for _ in range(LAYERS)]
+    pw = [torch.empty((1, dk.N, Kp), dtype=torch.uint8, device=device) for _ in range(n)]
+    pe = [torch.empty((1, dk.N // 32, Kp // 32), dtype=torch.uint8, device=device) for _ in range(n)]
     calls = [lambda i=i: lib.bsf8_pad_k(ptr(dw[i]), ptr(de[i]), ptr(pw[i]), ptr(pe[i]), 1, dk.N, dk.K,
-                                        Kp, 127, sp()) for i in range(LAYERS)]
-    t = graph_time(calls, 50)
-    emit("a7 pad_k", f"N={dk.N} K={dk.K} -> {Kp}, {LAYERS} copies", t,
-         dk.N * dk.K + dk.N * Kp + (dk.N // 32) * (dk.K // 32 + Kp // 32))
-    del w8s, exs, twins
+                                        Kp, 127, sp()) for i in range(n)]
+    emit("a7 pad_k down_proj 576->640", graph_time(calls, 20),
+         dk.N * dk.K + dk.N * Kp + (dk.N // 32) * (dk.K // 32 + Kp // 32), n)
+    del dt, dw, de, pw, pe
 
     cache = {}
 
@@ -525,11 +610,13 @@ def run_suite(device, peak):
         key = (wk.name, wk.K, copies)
         if key not in cache:
             cache.clear()
+            torch.cuda.empty_cache()
             cache[key] = [tuple(torch.from_numpy(a).to(device) for a in wk.weights(copy=c))
                           for c in range(copies)]
         return cache[key]
 
-    def gemm_row(name, wk, M, S, copies):
+    def gemm_time(wk, M, S, copies=None):
+        copies = copies or copies_for(wk.weight_bytes)
         layers = []
         for c, (w8, ex) in enumerate(weights_of(wk, copies)):
             x = wk.x(copy=c, M=M)
@@ -539,60 +626,65 @@ def run_suite(device, peak):
         wss = [torch.empty(max(16, need), dtype=torch.uint8, device=device) for _ in layers] if need else [None] * copies
         calls = [lambda l=l, y=y, w=w: bsf8.gemm(l[2], l[0], l[1], split_k=S, out=y, workspace=w)
                  for l, y, w in zip(layers, ys, wss)]
-        t = graph_time(calls, min(200, max(3, int(2e-3 / max(1e-6, wk.weight_bytes / 4e12)))))
-        xy = M * wk.G * wk.K * 2 + M * wk.G * wk.N * 2
-        emit(name, f"G={wk.G} N={wk.N} K={wk.K} M={M} split_k={S or 'auto'}, {copies} copies", t,
-             wk.weight_bytes + xy, wk.weight_bytes)
+        t = graph_time(calls, reps_for(wk.weight_bytes / 2e12, copies))
+        S_used = S or bsf8.auto_split(M, wk.N, wk.K, wk.G)
+        kern = bsf8.KERNELS[bsf8.gemm_kernel(M, wk.N, wk.K, wk.G, S)]
+        return t, {"M": M, "S": S_used, "kernel": kern, "launches_per_call": 2 if need else 1}, copies
 
-    gemm_row("a3-a6 gemm tiny", wl.TINY, 4, 1, LAYERS)
-    gemm_row("a3-a6 gemm tiny", wl.TINY, 4, 4, LAYERS)
-    for M in (2, 4, 6, 8):
-        gemm_row("a3-a6 gemm wo_a", wl.WO_A, M, 8, LAYERS)
-    gemm_row("a3-a6 gemm down_proj K=576", wl.DOWN_PROJ, 6, 0, LAYERS)
-    import dataclasses
-    gemm_row("a3-a6 gemm down_proj K=640", dataclasses.replace(wl.DOWN_PROJ, K=640), 6, 0, LAYERS)
-    for M in (9, 16, 32, 64, 96, 128, 192):
-        for S in (1, 2, 4, 8):
-            gemm_row("a3-a6 gemm mid", wl.MID, M, S, LAYERS)
-    for M in (1, 2, 6, 16, 64, 128):
-        gemm_row("a3-a6 gemm gate_up", wl.GATE_UP, M, 0, LAYERS)
-    for M in (1, 2, 6, 16, 64, 128):
-        gemm_row("a3-a6 gemm head", wl.HEAD, M, 0, 3)
+    def gemm_row(row, wk, M, S, copies=None):
+        t, info, copies = gemm_time(wk, M, S, copies)
+        emit(row, t, wk.weight_bytes, copies, **info)
 
-    # per-(row, 32-column) scales (the draft main_proj's layout): twin, dequant and GEMM at
-    # its shape (1280 output rows, K = 5120), 43 copies
+    gemm_row("C1 tiny M=4 S=1", wl.TINY, 4, 1)
+    gemm_row("C1 tiny M=4 S=4", wl.TINY, 4, 4)
+    for M in wl.WO_A_ROWS:
+        gemm_row(f"C2 wo_a M={M} S=8", wl.WO_A, M, 8)
+    gemm_row("C3 down_proj K=576 M=6", wl.DOWN_PROJ, 6, 0)
+    gemm_row("C3 down_proj K=640 M=6", dataclasses.replace(wl.DOWN_PROJ, K=640), 6, 0)
+    for M in wl.MID_ROWS:                      # each split of the sweep, the best reported
+        per_s = {}
+        for S in wl.MID_SPLITS:
+            per_s[S] = gemm_time(wl.MID, M, S)
+        best = min(per_s, key=lambda S: per_s[S][0][0])
+        t, info, copies = per_s[best]
+        emit(f"C4 mid M={M}", t, wl.MID.weight_bytes, copies, **info,
+             us_by_split={str(S): round(v[0][0] * 1e6, 3) for S, v in per_s.items()},
+             kernel_by_split={str(S): v[1]["kernel"] for S, v in per_s.items()})
+    for M in wl.SWEEP_ROWS:
+        gemm_row(f"C5 gate_up N=1152 K=5120 M={M}", wl.GATE_UP, M, 0)
+    for M in wl.SWEEP_ROWS:
+        gemm_row(f"C5 head N=32768 K=5120 M={M}", wl.HEAD, M, 0, copies=3)
+
+    # f3: per-(row, 32-column) scales at the draft main_proj shape (1280 x 5120)
     N1, K1 = 1280, 5120
+    n = copies_for(N1 * K1 + N1 * K1 // 32, least=40)
     rng = wl.rng(90)
-    rw8 = [torch.from_numpy(wl.codes(rng, (1, N1, K1))).to(device) for _ in range(LAYERS)]
-    rex = [torch.from_numpy(wl.exponents(rng, (1, N1, K1 // 32), 110, 130)).to(device) for _ in range(LAYERS)]
+    rw8 = [torch.from_numpy(wl.codes(rng, (1, N1, K1))).to(device) for _ in range(n)]
+    rex = [torch.from_numpy(wl.exponents(rng, (1, N1, K1 // 32), 110, 130)).to(device) for _ in range(n)]
     rbf = [bsf8.dequant_rows(a, b) for a, b in zip(rw8, rex)]
     o8 = [torch.empty_like(a) for a in rw8]
     oe = [torch.empty_like(b) for b in rex]
-    ok = [torch.empty_like(b) for b in rex]
-    acc = torch.empty((LAYERS,), dtype=torch.int32, device=device)
-    calls = [lambda i=i: lib.bsf8_make_twin_rows(ptr(rbf[i]), ptr(o8[i]), ptr(oe[i]), ptr(ok[i]),
+    okr = [torch.empty_like(b) for b in rex]
+    acc = torch.empty((n,), dtype=torch.int32, device=device)
+    calls = [lambda i=i: lib.bsf8_make_twin_rows(ptr(rbf[i]), ptr(o8[i]), ptr(oe[i]), ptr(okr[i]),
                                                  ctypes.c_void_p(acc.data_ptr() + 4 * i), 1, N1, K1, sp())
-             for i in range(LAYERS)]
-    t = graph_time(calls, 50)
-    emit("f3 rows make_twin", f"N={N1} K={K1} bf16 -> twin, {LAYERS} copies", t, N1 * K1 * 3 + 2 * N1 * K1 // 32)
+             for i in range(n)]
+    emit("f3 rows make_twin 1280x5120", graph_time(calls, 20), N1 * K1 * 3 + 2 * N1 * K1 // 32, n)
     calls = [lambda i=i: lib.bsf8_dequant_rows(ptr(rw8[i]), ptr(rex[i]), ptr(rbf[i]), 1, N1, K1, sp())
-             for i in range(LAYERS)]
-    t = graph_time(calls, 50)
-    emit("f3 rows dequant", f"N={N1} K={K1} twin -> bf16, {LAYERS} copies", t, N1 * K1 * 3 + N1 * K1 // 32)
+             for i in range(n)]
+    emit("f3 rows dequant 1280x5120", graph_time(calls, 20), N1 * K1 * 3 + N1 * K1 // 32, n)
     wbytes = N1 * K1 + N1 * K1 // 32
     for M in (1, 6, 16):
         xs = [torch.from_numpy(wl.activations(rng, M, K1).view("int16")).view(torch.bfloat16).to(device)
-              for _ in range(LAYERS)]
-        ys = [torch.empty((M, 1, N1), dtype=torch.bfloat16, device=device) for _ in range(LAYERS)]
-        calls = [lambda i=i: bsf8.gemm_rows(xs[i], rw8[i], rex[i], out=ys[i]) for i in range(LAYERS)]
-        t = graph_time(calls, 100)
-        emit("f3 rows gemm", f"N={N1} K={K1} M={M} split_k=auto, {LAYERS} copies", t,
-             wbytes + M * K1 * 2 + M * N1 * 2, wbytes)
+              for _ in range(n)]
+        ys = [torch.empty((M, 1, N1), dtype=torch.bfloat16, device=device) for _ in range(n)]
+        calls = [lambda i=i: bsf8.gemm_rows(xs[i], rw8[i], rex[i], out=ys[i]) for i in range(n)]
+        emit(f"f3 rows gemm 1280x5120 M={M}", graph_time(calls, 50), wbytes, n, M=M)
         del xs, ys
-    del rw8, rex, rbf, o8, oe, ok
+    del rw8, rex, rbf, o8, oe, okr
 
-    # fp32 output (the draft head's fp32 logits): partials of the kernel the shape selects,
-    # summed over the splits in fp32
+    # f2: fp32 output on the head-like weight (partials of the kernel the shape selects,
+    # summed over the splits in fp32)
     for M in (6, 64, 128):
         wk = wl.HEAD
         layers = []
@@ -605,17 +697,13 @@ def run_suite(device, peak):
         calls = [lambda l=l, P=P, y=y: (bsf8.gemm_partials(l[2], l[0], l[1], S, out=P),
                                         bsf8.splitk_reduce_f32(P, out=y) if S > 1 else None)
                  for l, P, y in zip(layers, Ps, ys)]
-        t = graph_time(calls, 20)
-        xy = M * wk.G * wk.K * 2 + M * wk.G * wk.N * 4
-        emit("f2 gemm fp32 out", f"G={wk.G} N={wk.N} K={wk.K} M={M} split_k={S}, 3 copies", t,
-             wk.weight_bytes + xy, wk.weight_bytes)
+        emit(f"f2 fp32 out head M={M}", graph_time(calls, 10), wk.weight_bytes, 3, M=M, S=S,
+             kernel=bsf8.KERNELS[bsf8.gemm_kernel(M, wk.N, wk.K, wk.G, S)])
         del layers, Ps, ys
 
-    # Past 192 rows (prefill-sized calls, the pages' drop mode served from the twin): bound by
-    # the tensor cores, so reported against the measured dense bf16 peak too.  The calls of a
-    # row share one workspace: they run one after another on the stream.
+    # f1: past 192 rows (prefill-sized calls from the twin), also against the bf16 peak
     bf16_peak = measured_bf16_tflops()
-    for wk, M, copies in ((wl.MID, 1024, 8), (wl.MID, 4096, 4), (wl.HEAD, 512, 2), (wl.HEAD, 2048, 2)):
+    for wk, M, copies in ((wl.MID, 1024, 16), (wl.MID, 4096, 4), (wl.HEAD, 512, 2), (wl.HEAD, 2048, 2)):
         layers = []
         for c, (w8, ex) in enumerate(weights_of(wk, copies)):
             x = wk.x(copy=c, M=M)
@@ -626,15 +714,15 @@ def run_suite(device, peak):
         calls = [lambda l=l, y=y: bsf8.gemm(l[2], l[0], l[1], split_k=0, out=y, workspace=ws)
                  for l, y in zip(layers, ys)]
         t = graph_time(calls, 5)
-        flops = 2.0 * M * wk.G * wk.N * wk.K
-        xy = M * wk.G * wk.K * 2 + M * wk.G * wk.N * 2
-        emit("f1 gemm large-M", f"G={wk.G} N={wk.N} K={wk.K} M={M} split_k=auto, {copies} copies", t,
-             wk.weight_bytes + xy, wk.weight_bytes)
-        out[-1]["TFLOPs"] = flops / t / 1e12
-        out[-1]["frac_of_bf16_peak"] = flops / t / 1e12 / bf16_peak
-        print(json.dumps({"row": "f1 gemm large-M", "M": M, "TFLOPs": out[-1]["TFLOPs"],
-                          "frac_of_bf16_peak": out[-1]["frac_of_bf16_peak"]}), flush=True)
+        tf = 2.0 * M * wk.G * wk.N * wk.K / t[0] / 1e12
+        emit(f"f1 large-M {'mid G=4 1024x4096' if wk is wl.MID else 'head 32768x5120'} M={M}", t,
+             wk.weight_bytes, copies, M=M, S=bsf8.auto_split(M, wk.N, wk.K, wk.G),
+             kernel=bsf8.KERNELS[bsf8.gemm_kernel(M, wk.N, wk.K, wk.G, 0)],
+             TFLOPs=round(tf, 1), frac_bf16=round(tf / bf16_peak, 4))
         del layers, ys, ws
+    cache.clear()
+    torch.cuda.empty_cache()
+    out["_seconds"] = round(time.time() - t_start, 1)
     return out
 
 
@@ -659,7 +747,7 @@ def main(argv=None):
     bsf8_build.build()
     bsf8.load()
     if args.suite:
-        run_suite(device, measured_peaks()[0])
+        configs_map(device, measured_peaks()[0], verbose=True)
         return 0
     wk = workload()
     if args.profile_calls and args.workload in ("make_twin", "dequant", "pad_k"):
@@ -687,23 +775,29 @@ def main(argv=None):
     # launch on its own (L2 flushed before each) for the launch duration in isolation.
     t_eager = time_eager(layers, wk, max(1, args.steps // 20), stream)
     t_iso = time_isolated(layers, wk, 20, stream)
-    t_nopdl, _, _ = time_graph(layers, wk, max(1, args.steps // 4), max(3, args.warmup), False, stream)
+    t_nopdl, _, _, _ = time_graph(layers, wk, max(1, args.steps // 4), max(3, args.warmup), False, stream)
 
+    nsm = torch.cuda.get_device_properties(device).multi_processor_count
+    probe = [torch.zeros((nsm, 2), dtype=torch.int64, device=device) for _ in range(2)]
     sampler = ClockSampler(local)
     sampler.start()
     barrier(dist, device)
     torch.cuda.synchronize(device)
-    elapsed, w0, w1 = time_graph(layers, wk, args.steps, max(3, args.warmup), True, stream)
+    elapsed, w0, w1, steps_s = time_graph(layers, wk, args.steps, max(3, args.warmup), True, stream,
+                                          per_step=True, clock_probe=probe)
     torch.cuda.synchronize(device)
     barrier(dist, device)
     time.sleep(0.25)
     sampler.stop()
     clocks = sampler.summary(w0, w1)
+    clocks["in_region"] = region_clock(probe)
 
     calls = LAYERS * args.steps
     t_job, bytes_job = aggregate(dist, elapsed, float(wk.weight_bytes) * calls, device)
     value = bytes_job / t_job / 1e9
     us_call = elapsed / calls * 1e6
+    per_call = sorted(t / LAYERS * 1e6 for t in steps_s)
+    q = lambda f: per_call[min(len(per_call) - 1, int(f * len(per_call)))]
 
     e2e_steps = max(1, min(args.e2e_steps, args.steps))
     t_e2e, h2d, d2h = time_e2e(layers, wk, e2e_steps, stream)
@@ -712,13 +806,16 @@ def main(argv=None):
     peak, peak_kind = measured_peaks()
     achieved = wk.algorithmic_bytes / (elapsed / calls) / 1e9
     traffic = recorded_traffic()
+    import block_scaled_fp8_weight_gb300 as bsf8
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_job / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_dict(wk), "us_per_call": us_call,
+        "us_per_call_by_step": {"median": q(0.5), "p10": q(0.1), "p90": q(0.9), "steps": len(per_call)},
         "frac_of_peak": {"measured": value / world / peak, "nominal_7900": value / world / 7900.0},
         "gpu_launches": calls,
+        "kernel": bsf8.KERNELS[bsf8.gemm_kernel(wk.M, wk.N, wk.K, wk.G, wk.split_k)],
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": KERNEL_NAME,
@@ -737,6 +834,8 @@ def main(argv=None):
             "eager_us_per_call": t_eager / (LAYERS * max(1, args.steps // 20)) * 1e6,
         },
     }
+    if rank == 0 and world == 1 and not args.no_configs:
+        line["configs"] = configs_map(device, peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_baseline(wk, args.cpu_seconds)
     if rank == 0:

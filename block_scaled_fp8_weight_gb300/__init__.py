@@ -22,7 +22,7 @@ __all__ = [
     "Bsf8Error", "load", "make_twin", "twin_or_none", "dequant", "gemm", "gemm_partials", "gemm_f32", "splitk_reduce_f32", "make_twin_rows", "dequant_rows", "gemm_rows",
     "splitk_reduce", "pad_k", "pad_x", "workspace_bytes", "auto_split", "device_status",
     "set_option", "get_option", "OPT_PDL", "OPT_WAIT_TIMEOUT_NS", "OPT_DEBUG_SKIP_LOADS",
-    "OPT_GEMM_PATH", "gemm_kernel", "KERNELS",
+    "OPT_GEMM_PATH", "gemm_kernel", "KERNELS", "sm_clock_sample",
     "MAX_M", "STATUS",
 ]
 
@@ -74,6 +74,7 @@ def load(build_if_missing: bool = True):
             "bsf8_gemm_workspace_bytes": (SZ, [I, I, I, I, I]),
             "bsf8_gemm_auto_split": (I, [I, I, I, I]),
             "bsf8_gemm_kernel": (I, [I, I, I, I, I]),
+            "bsf8_sm_clock_sample": (I, [P, I, P]),
             "bsf8_gemm_static_scratch": (I, [P, P, P, P, I, I, I, I, I, I64, P]),
             "bsf8_gemm_partials": (I, [P, P, P, P, I, I, I, I, I, I64, P]),
             "bsf8_make_twin_rows": (I, [P, P, P, P, P, I, I, I, P]),
@@ -374,6 +375,19 @@ def device_status(stream=None) -> int:
     _check(lib.bsf8_device_status(ctypes.byref(st), ctypes.c_void_p(s.cuda_stream)),
            "bsf8_device_status")
     return st.value
+
+
+def sm_clock_sample(out, stream=None):
+    """Diagnostic: per-SM (global ns timer, cycle counter) into out, an int64 CUDA tensor
+    [nsm, 2] (see bsf8_sm_clock_sample)."""
+    torch = _torch()
+    lib = load()
+    if out.dim() != 2 or out.shape[1] != 2:
+        raise ValueError("out must be [nsm, 2]")
+    s = torch.cuda.current_stream(out.device) if stream is None else stream
+    _check(lib.bsf8_sm_clock_sample(_dev(out, torch.int64, "out"), out.shape[0],
+                                    ctypes.c_void_p(s.cuda_stream)), "bsf8_sm_clock_sample")
+    return out
 
 
 def set_option(option: int, value: int):

@@ -272,6 +272,15 @@ int bsf8_pad_k(const uint8_t *w8, const uint8_t *exp, uint8_t *w8_out, uint8_t *
 int bsf8_pad_x(const void *x, int64_t ldx, void *x_out, int M, int G, int K, int Kp,
                bsf8_stream_t stream);
 
+/* ------------------------------------------------------------------ diagnostics
+ * Not part of the method: a measurement aid.  Launches 2*nsm one-warp blocks on `stream`;
+ * the block on SM i writes out[2i] = the global nanosecond timer and out[2i+1] = SM i's
+ * cycle counter (slots of SMs no block reached keep their contents).  Two samples around
+ * a timed region give each SM's average clock over it.
+ *   out  device, uint64 [nsm][2];  nsm  1 .. 4096 (the device's SM count)
+ * Errors: BSF8_ERR_NULL, BSF8_ERR_SHAPE, BSF8_ERR_CUDA, BSF8_ERR_DEVICE. */
+int bsf8_sm_clock_sample(uint64_t *out, int nsm, bsf8_stream_t stream);
+
 /* --------------------------------------------------------------- status, options
  * Synchronises `stream`, then reads into *status (host) and clears the device status
  * word of the current device: BSF8_OK, or BSF8_ERR_TIMEOUT if a kernel gave up a

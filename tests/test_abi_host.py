@@ -172,6 +172,13 @@ def test_gemm_kernel_query_validation(lib):
         lib.bsf8_set_option(4, 0)
 
 
+def test_sm_clock_sample_validation(lib):
+    """The measurement aid rejects a NULL buffer and SM counts out of range before any launch."""
+    assert lib.bsf8_sm_clock_sample(0, 152, None) == NULL
+    assert lib.bsf8_sm_clock_sample(A, 0, None) == SHAPE
+    assert lib.bsf8_sm_clock_sample(A, 4097, None) == SHAPE
+
+
 def test_options_roundtrip(lib):
     assert lib.bsf8_get_option(1) == 1
     assert lib.bsf8_set_option(1, 0) == OK and lib.bsf8_get_option(1) == 0
