@@ -406,6 +406,49 @@ def region_clock(probe):
                    "block per SM right before and right after the timed region (bsf8_sm_clock_sample)"}
 
 
+def time_broken_chain(layers, wk, steps, stream, mode, sleep_cycles=20000):
+    """Each layer's GEMM after a kernel that is not this library's (a spin of sleep_cycles
+    standing in for a collective or another op; it does not let the GEMM start early), in a
+    CUDA graph of the 43 layers.  mode "sleep": the spins alone; "plain": spin + GEMM;
+    "prefetch": spin + GEMM with bsf8_prefetch_l2 of the layer's twin on a side stream,
+    issued as the spin starts.  Returns seconds per layer."""
+    import torch
+    import block_scaled_fp8_weight_gb300 as bsf8
+    outs = [torch.empty((wk.M, wk.G, wk.N), dtype=torch.bfloat16, device=stream.device) for _ in layers]
+    side = torch.cuda.Stream(device=stream.device)
+
+    def step():
+        for (w8, ex, x), y in zip(layers, outs):
+            if mode == "prefetch":
+                ev = torch.cuda.Event()
+                ev.record(stream)
+                side.wait_event(ev)
+                bsf8.prefetch_l2(w8, ex, stream=side)
+            torch.cuda._sleep(sleep_cycles)
+            if mode != "sleep":
+                bsf8.gemm(x, w8, ex, split_k=wk.split_k, out=y)
+        if mode == "prefetch":
+            stream.wait_stream(side)
+
+    with torch.cuda.stream(stream):
+        step()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step()
+        for _ in range(3):
+            g.replay()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+        stream.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / (steps * len(layers))
+
+
 def time_eager(layers, wk, steps, stream):
     import torch
     import block_scaled_fp8_weight_gb300 as bsf8
@@ -776,6 +819,8 @@ def main(argv=None):
     t_eager = time_eager(layers, wk, max(1, args.steps // 20), stream)
     t_iso = time_isolated(layers, wk, 20, stream)
     t_nopdl, _, _, _ = time_graph(layers, wk, max(1, args.steps // 4), max(3, args.warmup), False, stream)
+    broken = {m: time_broken_chain(layers, wk, max(2, args.steps // 4), stream, m) * 1e6
+              for m in ("sleep", "plain", "prefetch")}
 
     nsm = torch.cuda.get_device_properties(device).multi_processor_count
     probe = [torch.zeros((nsm, 2), dtype=torch.int64, device=device) for _ in range(2)]
@@ -832,6 +877,13 @@ def main(argv=None):
         "variants": {
             "graph_no_pdl_us_per_call": t_nopdl / (LAYERS * max(1, args.steps // 4)) * 1e6,
             "eager_us_per_call": t_eager / (LAYERS * max(1, args.steps // 20)) * 1e6,
+            "chain_broken_by_a_foreign_kernel": {
+                "what": "each layer's GEMM after a ~10 us spin kernel that is not this library's "
+                        "(it does not let the GEMM start early); us per layer",
+                "spin_alone_us": broken["sleep"], "spin_then_gemm_us": broken["plain"],
+                "spin_then_gemm_with_l2_prefetch_us": broken["prefetch"],
+                "gemm_us_without_prefetch": broken["plain"] - broken["sleep"],
+                "gemm_us_with_prefetch": broken["prefetch"] - broken["sleep"]},
         },
     }
     if rank == 0 and world == 1 and not args.no_configs:

@@ -22,7 +22,7 @@ __all__ = [
     "Bsf8Error", "load", "make_twin", "twin_or_none", "dequant", "gemm", "gemm_partials", "gemm_f32", "splitk_reduce_f32", "make_twin_rows", "dequant_rows", "gemm_rows",
     "splitk_reduce", "pad_k", "pad_x", "workspace_bytes", "auto_split", "device_status",
     "set_option", "get_option", "OPT_PDL", "OPT_WAIT_TIMEOUT_NS", "OPT_DEBUG_SKIP_LOADS",
-    "OPT_GEMM_PATH", "gemm_kernel", "KERNELS", "sm_clock_sample",
+    "OPT_GEMM_PATH", "gemm_kernel", "KERNELS", "sm_clock_sample", "prefetch_l2",
     "MAX_M", "STATUS",
 ]
 
@@ -75,6 +75,7 @@ def load(build_if_missing: bool = True):
             "bsf8_gemm_auto_split": (I, [I, I, I, I]),
             "bsf8_gemm_kernel": (I, [I, I, I, I, I]),
             "bsf8_sm_clock_sample": (I, [P, I, P]),
+            "bsf8_prefetch_l2": (I, [P, P, I, I, I, P]),
             "bsf8_gemm_static_scratch": (I, [P, P, P, P, I, I, I, I, I, I64, P]),
             "bsf8_gemm_partials": (I, [P, P, P, P, I, I, I, I, I, I64, P]),
             "bsf8_make_twin_rows": (I, [P, P, P, P, P, I, I, I, P]),
@@ -335,6 +336,21 @@ def gemm_f32(x, w8, ex, split_k: int = 0):
     S = split_k or auto_split(M, N, K, G)
     P = gemm_partials(x, w8, ex, S)
     return P[0] if S == 1 else splitk_reduce_f32(P)
+
+
+# ----------------------------------------------------------------------- L2 prefetch
+
+def prefetch_l2(w8, ex, stream=None):
+    """Pull the twin (w8 [G,N,K], ex [G,N/32,K/32]) into L2 on `stream` (default: the
+    current stream); a hint that changes no result."""
+    torch = _torch()
+    lib = load()
+    _contig(w8, "w8")
+    _contig(ex, "exp")
+    G, N, K = w8.shape
+    s = torch.cuda.current_stream(w8.device) if stream is None else stream
+    _check(lib.bsf8_prefetch_l2(_dev(w8, torch.uint8, "w8"), _dev(ex, torch.uint8, "exp"), G, N, K,
+                                ctypes.c_void_p(s.cuda_stream)), "bsf8_prefetch_l2")
 
 
 # ----------------------------------------------------------------------- pad-K

@@ -252,6 +252,18 @@ int bsf8_gemm_static_scratch(const void *x, const uint8_t *w8, const uint8_t *ex
                              int M, int N, int K, int G, int split_k, int64_t ldx,
                              bsf8_stream_t stream);
 
+/* --------------------------------------------------------------- L2 prefetch
+ * "docs/tp4-adapters.md", adapter table, l2_prefetch row: pull a twin -- the codes
+ * w8[G][N][K] and the exponents exp[G][N/32][K/32] -- into L2 ahead of the GEMM that reads
+ * it, typically on a side stream while other work runs (collectives, kernels that do not
+ * let the GEMM start early).  A hint: it reads nothing into the program and writes
+ * nothing, so results are the same with or without it; the lines may be evicted again
+ * before the GEMM runs if other traffic passes through L2 meanwhile.
+ *   w8, exp  device, 16-byte aligned (exp's last partial 16 bytes are not prefetched)
+ * Errors: BSF8_ERR_NULL, BSF8_ERR_SHAPE, BSF8_ERR_ALIGN, BSF8_ERR_CUDA. */
+int bsf8_prefetch_l2(const uint8_t *w8, const uint8_t *exp, int G, int N, int K,
+                     bsf8_stream_t stream);
+
 /* ------------------------------------------------------------------------- pad-K
  * "shared_pad_k.py", _pad_weight(): the twin [G][N][K] becomes [G][N][Kp] with code 0
  * (+0) in the new columns and its exponents [G][N/32][K/32] become [G][N/32][Kp/32]

@@ -172,6 +172,16 @@ def test_gemm_kernel_query_validation(lib):
         lib.bsf8_set_option(4, 0)
 
 
+def test_prefetch_l2_validation(lib):
+    pf = lib.bsf8_prefetch_l2
+    assert pf(0, B, 2, 1024, 4096, None) == NULL
+    assert pf(A, 0, 2, 1024, 4096, None) == NULL
+    assert pf(A, B, 2, 1000, 4096, None) == SHAPE
+    assert pf(A, B, 0, 1024, 4096, None) == SHAPE
+    assert pf(A + 8, B, 2, 1024, 4096, None) == ALIGN
+    assert pf(A, B + 1, 2, 1024, 4096, None) == ALIGN
+
+
 def test_sm_clock_sample_validation(lib):
     """The measurement aid rejects a NULL buffer and SM counts out of range before any launch."""
     assert lib.bsf8_sm_clock_sample(0, 152, None) == NULL
