@@ -71,6 +71,8 @@ def parse_args(argv=None):
                    default="wo_a", help="profiling mode only: which workload to run (a GEMM shape, "
                                         "or make_twin / dequant on the wo_a shape, pad_k on down_proj)")
     p.add_argument("--m", type=int, default=None, help="profiling mode only: token rows")
+    p.add_argument("--copies", type=int, default=None,
+                   help="profiling mode only: distinct weight copies cycled (default 43, 3 for head)")
     p.add_argument("--suite", action="store_true",
                    help="time every hot-path row (make_twin, dequant, pad-K, the GEMM at every "
                         "config) and print one JSON line per row instead of the headline line")
@@ -804,7 +806,10 @@ def main(argv=None):
         wk = dataclasses.replace(wk, split_k=args.split_k)
     if args.m is not None:
         wk = dataclasses.replace(wk, M=args.m)
-    layers = build_layers(wk, device, copies=LAYERS if wk.copies > 1 else 3)
+    copies = LAYERS if wk.copies > 1 else 3
+    if args.profile_calls and args.copies:
+        copies = args.copies
+    layers = build_layers(wk, device, copies=copies)
     stream = torch.cuda.Stream(device=device)
     if args.profile_calls:
         with torch.cuda.stream(stream):
