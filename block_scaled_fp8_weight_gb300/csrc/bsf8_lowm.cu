@@ -67,11 +67,6 @@ static_assert(2 * (kSmemBytes + 1024 + 8 * 1024) <= 228 * 1024, "two blocks fit 
 
 struct LowParams {
     CUtensorMap wmap;  // w8 as a [G*N rows][K columns] byte matrix, box 128 x 16
-    // x as {64 columns, M rows, K/64 column chunks, G groups} (pitches ldx*2, 128, K*2
-    // bytes), box {64, 8, 2, 1}: a step's 8 x 128 tile in one copy, each 64-column chunk an
-    // 8 x 64 box with the 128-byte swizzle (rows >= M read as zeros).  Used when xtma != 0.
-    CUtensorMap xmap;
-    int xtma;
     const uint16_t *x;  // [M][ldx] bf16
     long long ldx;
     const uint8_t *ex;
@@ -103,19 +98,6 @@ __device__ __forceinline__ void tma_2d_hint(void *dst, const CUtensorMap *map, i
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-// 16-byte global -> shared copy through the load/store path (cp.async); src_bytes < 16
-// zero-fills the rest (0: nothing is read).
-__device__ __forceinline__ void cp_async_16_zfill(void *dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
-}
-
-// Waits until this thread's cp.async copies have landed.
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
@@ -233,114 +215,99 @@ __device__ __forceinline__ Task task_of(const LowParams &p, int w) {
 // Byte offsets of this thread's 16-byte units in a 16 x 128 weight box written with the
 // 128-byte swizzle (unit u of row r sits at unit u ^ (r % 8)): row r units 2q, 2q+1 and
 // row r+8 units 2q, 2q+1.
-struct BoxOffs {
-    int a0, a1, b0, b1;
-};
-
-__device__ __forceinline__ BoxOffs box_offsets(int r, int q) {
-    BoxOffs o;
-    o.a0 = r * 128 + (((2 * q) ^ (r & 7)) << 4);
-    o.a1 = r * 128 + (((2 * q + 1) ^ (r & 7)) << 4);
-    o.b0 = o.a0 + 8 * 128;
-    o.b1 = o.a1 + 8 * 128;
-    return o;
+// Byte offset, in a 16 x 128 weight box written with the 128-byte swizzle (unit u of row r
+// sits at unit u ^ (r % 8)), of row r's 8 codes at columns 32v + 8q .. 32v + 8q + 7.
+__device__ __forceinline__ int piece_offset(int r, int q, int v) {
+    return r * 128 + (((2 * v + (q >> 1)) ^ (r & 7)) << 4) + 8 * (q & 1);
 }
 
+// The column order inside a step.  Thread q of an MMA quad owns the step's columns
+// 32v + 8q .. 32v + 8q + 7 for v = 0..3 -- one 8-column piece of each 32-column exponent
+// block -- so that the quad's four threads read a token row's x in whole 64-byte runs.
+// MMA j = 2v + h takes the piece's columns 4h .. 4h+3 as its k = {2q, 2q+1, 2q+8, 2q+9}
+// (the same permutation on both operands leaves every product and every sum unchanged).
+//
 // Rebuilds this thread's share of one weight box into the A fragments of the step's 8
-// MMAs: a[4j..4j+3] = (row r, cols 4j..4j+1), (row r+8, same), (row r, cols 4j+2..4j+3),
-// (row r+8, same), where col c means column 32q + c of the step.  mxa / mxb keep the
-// largest rebuilt magnitude of rows r / r+8 before scaling (an e4m3 NaN code spreads to
-// 0x07F0, above every finite code's 0x07E0).
-// e: the exponent byte of the thread's block; with ROWS (one exponent per weight row and 32
-// columns) e is row r's and eb row r+8's.
+// MMAs: a[4j..4j+3] = (row r, piece columns 4h, 4h+1), (row r+8, same), (row r, 4h+2,
+// 4h+3), (row r+8, same).  mxa / mxb keep the largest rebuilt magnitude of rows r / r+8
+// before scaling (an e4m3 NaN code spreads to 0x07F0, above every finite code's 0x07E0).
+// e[v]: the exponent byte of block v of the step; with ROWS (one exponent per weight row
+// and 32 columns) e[v] is row r's and eb[v] row r+8's.  mine: bit v set where block v of
+// the step lies inside the task.
 template <bool TWO, bool ROWS>
-__device__ __forceinline__ void decode_box(const uint8_t *box, const BoxOffs &o, bool mine,
-                                           uint32_t e, uint32_t eb, uint32_t (&a)[32], uint32_t &mxa,
-                                           uint32_t &mxb) {
-    uint4 ra[2], rb[2];
-    if (mine) {
-        ra[0] = *reinterpret_cast<const uint4 *>(box + o.a0);
-        ra[1] = *reinterpret_cast<const uint4 *>(box + o.a1);
-        rb[0] = *reinterpret_cast<const uint4 *>(box + o.b0);
-        rb[1] = *reinterpret_cast<const uint4 *>(box + o.b1);
-    } else {
-        ra[0] = ra[1] = rb[0] = rb[1] = make_uint4(0, 0, 0, 0);
+__device__ __forceinline__ void decode_box(const uint8_t *box, int r, int q, uint32_t mine,
+                                           const uint32_t (&e)[4], const uint32_t (&eb)[4],
+                                           uint32_t (&a)[32], uint32_t &mxa, uint32_t &mxb) {
+    uint2 pa[4], pb[4];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        if ((mine >> v) & 1u) {
+            pa[v] = *reinterpret_cast<const uint2 *>(box + piece_offset(r, q, v));
+            pb[v] = *reinterpret_cast<const uint2 *>(box + piece_offset(r + 8, q, v));
+        } else {
+            pa[v] = pb[v] = make_uint2(0, 0);
+        }
     }
-    uint32_t s1, s2 = 0, s1b, s2b = 0;
-    if (TWO) {  // exact for every exponent byte: restore e4m3 * 1, then scale by 2^(e-127)
-        s1 = s1b = 0x7B807B80u;
-        const uint32_t bb = e == 0 ? 0x0040u : (e << 7);
-        s2 = bb | (bb << 16);
-        const uint32_t b8 = eb == 0 ? 0x0040u : (eb << 7);
-        s2b = ROWS ? (b8 | (b8 << 16)) : s2;
-    } else {    // e <= 134: one multiply by 2^(e-7)
-        const uint32_t b = (e + 120u) << 7;
-        s1 = b | (b << 16);
-        const uint32_t b8 = (eb + 120u) << 7;
-        s1b = ROWS ? (b8 | (b8 << 16)) : s1;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        uint32_t s1, s2 = 0, s1b, s2b = 0;
+        if (TWO) {  // exact for every exponent byte: restore e4m3 * 1, then scale by 2^(e-127)
+            s1 = s1b = 0x7B807B80u;
+            const uint32_t bb = e[v] == 0 ? 0x0040u : (e[v] << 7);
+            s2 = bb | (bb << 16);
+            const uint32_t b8 = eb[v] == 0 ? 0x0040u : (eb[v] << 7);
+            s2b = ROWS ? (b8 | (b8 << 16)) : s2;
+        } else {    // e <= 134: one multiply by 2^(e-7)
+            const uint32_t b = (e[v] + 120u) << 7;
+            s1 = b | (b << 16);
+            const uint32_t b8 = (eb[v] + 120u) << 7;
+            s1b = ROWS ? (b8 | (b8 << 16)) : s1;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int j = 2 * v + h;
+            uint32_t t0, t1, u0, u1;
+            spread_codes(h ? pa[v].y : pa[v].x, t0, t1);
+            spread_codes(h ? pb[v].y : pb[v].x, u0, u1);
+            mxa = max_xorsign_abs(mxa, max_xorsign_abs(t0, t1));
+            mxb = max_xorsign_abs(mxb, max_xorsign_abs(u0, u1));
+            uint32_t alo = bf16x2_mul(t0, s1), ahi = bf16x2_mul(t1, s1);
+            uint32_t blo = bf16x2_mul(u0, s1b), bhi = bf16x2_mul(u1, s1b);
+            if (TWO) {
+                alo = bf16x2_mul(alo, s2);
+                ahi = bf16x2_mul(ahi, s2);
+                blo = bf16x2_mul(blo, s2b);
+                bhi = bf16x2_mul(bhi, s2b);
+            }
+            a[4 * j + 0] = alo;
+            a[4 * j + 1] = blo;
+            a[4 * j + 2] = ahi;
+            a[4 * j + 3] = bhi;
+        }
     }
+}
+
+// The step's 8 MMAs (m16n8k16, rows r / r+8 of the slab, tokens 0..7) in the column order
+// above: MMA j = 2v + h multiplies piece v's columns 4h .. 4h+3; xv[v] holds token r's 8
+// columns of piece v.  Two accumulators break the dependency chain.
+__device__ __forceinline__ void mma_step(const uint32_t (&a)[32], const uint4 (&xv)[4],
+                                         float (&acc)[2][4]) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        const uint4 &av = ra[j / 4], &bv = rb[j / 4];
-        const int i = j % 4;
-        uint32_t t0, t1, u0, u1;
-        spread_codes(i == 0 ? av.x : i == 1 ? av.y : i == 2 ? av.z : av.w, t0, t1);
-        spread_codes(i == 0 ? bv.x : i == 1 ? bv.y : i == 2 ? bv.z : bv.w, u0, u1);
-        mxa = max_xorsign_abs(mxa, max_xorsign_abs(t0, t1));
-        mxb = max_xorsign_abs(mxb, max_xorsign_abs(u0, u1));
-        uint32_t alo = bf16x2_mul(t0, s1), ahi = bf16x2_mul(t1, s1);
-        uint32_t blo = bf16x2_mul(u0, s1b), bhi = bf16x2_mul(u1, s1b);
-        if (TWO) {
-            alo = bf16x2_mul(alo, s2);
-            ahi = bf16x2_mul(ahi, s2);
-            blo = bf16x2_mul(blo, s2b);
-            bhi = bf16x2_mul(bhi, s2b);
-        }
-        a[4 * j + 0] = alo;
-        a[4 * j + 1] = blo;
-        a[4 * j + 2] = ahi;
-        a[4 * j + 3] = bhi;
-    }
-}
-
-// Half H of this thread's x fragment of a step: token r, columns 32q + 16H .. 32q + 16H + 15
-// (8 words, word i = columns 2i, 2i+1 of the half), from an 8 x 128 tile stored as two 8 x 64
-// boxes with the 128-byte swizzle.  Zero where the thread's columns are past its task.
-template <int H>
-__device__ __forceinline__ void load_xhalf(const uint8_t *slot, int r, int q, bool mine,
-                                           uint4 (&xv)[2]) {
-    const uint8_t *row = slot + (q >> 1) * 1024 + r * 128;
-#pragma unroll
-    for (int v = 0; v < 2; ++v)
-        xv[v] = mine ? *reinterpret_cast<const uint4 *>(row + ((((q & 1) * 4 + 2 * H + v) ^ r) << 4))
-                     : make_uint4(0, 0, 0, 0);
-}
-
-// MMAs j0 .. j0+3 of a step (m16n8k16, rows r / r+8 of the slab, tokens 0..7): MMA j
-// multiplies columns 4j..4j+3 of every thread's 32 into accumulator j % 4.  An mma.sync on
-// this GPU takes ~190 cycles to complete against an SM rate of one every ~4.5 cycles, so the
-// MMAs of a warp are spread over 4 independent accumulation chains (32 an SM).
-template <int J0>
-__device__ __forceinline__ void mma_half(const uint32_t (&a)[32], const uint4 (&xv)[2],
-                                         float (&acc)[4][4]) {
-#pragma unroll
-    for (int j = J0; j < J0 + 4; ++j) {
-        const uint4 &x = xv[(j - J0) / 2];
-        mma_bf16_16816(acc[j & 3], a[4 * j], a[4 * j + 1], a[4 * j + 2], a[4 * j + 3],
+        const uint4 &x = xv[j / 2];
+        mma_bf16_16816(acc[j & 1], a[4 * j], a[4 * j + 1], a[4 * j + 2], a[4 * j + 3],
                        (j & 1) ? x.z : x.x, (j & 1) ? x.w : x.y);
     }
 }
 
-// 16 TMEM columns of this thread's lane -> registers.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-        "%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
+// 16 bytes of global memory, cached in L2 only (x is written by the kernel before this one;
+// after the dependency wait L2 holds its values, while this SM's L1 might not).
+__device__ __forceinline__ uint4 ld_cg_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
 }
 
 __device__ __forceinline__ void st_cluster_v2f32(uint32_t addr, float a, float b) {
@@ -358,7 +325,7 @@ struct PostParams {
     long long ldx;
     unsigned long long timeout_ns;
     int *status;
-    int M, N, K, G, S, tps, tpc, cluster, mode, cps, spl, skip_loads, xtma, to_partials;
+    int M, N, K, G, S, tps, tpc, cluster, mode, cps, spl, skip_loads, to_partials;
 };
 
 // Partials mode: red[w] holds warp w's task partial [16 rows][8 tokens]; the block stores
@@ -382,16 +349,6 @@ __device__ __forceinline__ void partials_epilogue(const PostParams &q, float (*r
     }
 }
 
-// 4-D tensor copy global -> this CTA's shared memory, completing on `bar`.
-__device__ __forceinline__ void tma_4d(void *dst, const CUtensorMap *map, int c0, int c1, int c2,
-                                       int c3, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
-        : "memory");
-}
-
 // Keeps v in a register as an opaque value, so that the compiler cannot recompute it from
 // kernel parameters after the dependency wait.
 __device__ __forceinline__ int opaque(int v) {
@@ -402,16 +359,15 @@ __device__ __forceinline__ int opaque(int v) {
 }  // namespace
 
 // One block: 8 warps.  Warp w owns an 8 KB region of shared memory (4 slots of 2 KB) and
-// two mbarriers (weights, x).  Its task has nst <= 4 steps of 128 columns.
-//   before the wait: lane 0 arms the weight barrier with the task's bytes and issues one TMA
-//     box (16 rows x 128 columns, 128-byte swizzle) per step into slot t; the warp waits,
-//     rebuilds each box into its 32 fragment registers and parks steps 1.. in tensor memory
-//     (step 0 stays in registers);
-//   after the wait: the task's x tile (8 token rows x the task's columns) arrives in the
-//     same slots -- one TMA box a task when the columns allow it, else 16-byte cp.async
-//     copies -- in the layout of 128-byte-swizzled 8 x 64 boxes; step by step the warp
-//     multiplies, reading the next step's fragments back from tensor memory (tcgen05.ld)
-//     while the current step's MMAs run.
+// one mbarrier.  Its task has nst <= 4 steps of 128 columns.
+//   before the wait: lane 0 arms the barrier with the task's weight bytes and issues one
+//     TMA box (16 rows x 128 columns, 128-byte swizzle) per step into slot t; the warp
+//     waits, rebuilds each box into its 32 fragment registers and parks steps 1.. in tensor
+//     memory (step 0 stays in registers);
+//   after the wait: every thread loads its token row's x for all of the task's steps
+//     straight into registers (16-byte loads through L2; a quad's four threads read 64
+//     contiguous bytes of a row, see the column order above), then step by step the warp
+//     brings the fragments back from tensor memory (tcgen05.ld) and runs the MMAs.
 // One barrier covers all of a warp's weight boxes: the copies complete in one transaction
 // count, far faster than a barrier per box.
 template <bool ROWS>
@@ -422,7 +378,6 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
     float *const gather = reinterpret_cast<float *>(ring + kRingBytes);  // group mode tiles
     __shared__ __align__(16) float red[kWarps][16][8];
     __shared__ __align__(8) uint64_t wbar[kWarps];
-    __shared__ __align__(8) uint64_t xbar[kWarps][kPre];  // x: one barrier a step
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
     __shared__ PostParams sp;
@@ -437,25 +392,16 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
     const int nst = p.kt / kKS;  // steps of a task (<= kPre)
     const Task me = task_of(p, warp);
     uint8_t *const region = ring + warp * kRegionBytes;
-    // warps that share a task (column range) share its x tiles, kept in the region of the
-    // first of them (warp w % tpc); each copies a part
-    const int xl = warp % p.tpc, xj = warp / p.tpc, xn = kWarps / p.tpc;
-    uint8_t *const xregion = ring + xl * kRegionBytes;
     // every block holds exactly one group (the grid is the plan's, not capped)
     const int slab = me.slab0;
     const bool slab_ok = me.active && me.ngroups > 0 && slab < nslabs;
 
     if (lane == 0) {
         mbar_init(&wbar[warp], 1);
-#pragma unroll
-        for (int t = 0; t < kPre; ++t) mbar_init(&xbar[warp][t], 1);
         fence_mbar_init();
     }
     if (threadIdx.x == 0) s_err = 0;
-    if (threadIdx.x == 32) {
-        prefetch_tensormap(&p.wmap);
-        if (p.xtma) prefetch_tensormap(&p.xmap);
-    }
+    if (threadIdx.x == 32) prefetch_tensormap(&p.wmap);
     if (threadIdx.x == 64) {
         PostParams t;
         t.x = p.x;
@@ -476,7 +422,6 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
         t.cps = p.cps;
         t.spl = p.spl;
         t.skip_loads = p.skip_loads;
-        t.xtma = p.xtma;
         t.to_partials = p.to_partials;
         sp = t;
     }
@@ -503,9 +448,9 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
     }
     // The task's x rows, pulled into L2 while the previous kernel runs.  They may still
     // change before the wait; a prefetch only moves lines into L2, where the producer's
-    // writes land as well, and x is read after the wait from L2 (TMA, or cp.async.cg), so
-    // the copies see the producer's values.  Where x is already in L2 this costs nothing.
-    if (xj == 0 && lane < p.M && lane < 8 && me.k1 > me.k0)
+    // writes land as well, and x is read after the wait through L2 only (ld.global.cg),
+    // so the loads see the producer's values.  Where x is already in L2 this costs nothing.
+    if (lane < p.M && lane < 8 && me.k1 > me.k0 && warp < p.tpc)
         prefetch_l2(p.x + (size_t)lane * p.ldx + (size_t)g * p.K + me.k0,
                     (uint32_t)((me.k1 - me.k0) * 2));
     // exponent bytes of the task: lane l holds block k0/32 + l of the slab's row block
@@ -515,27 +460,13 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
             ? (uint32_t)__ldg(p.ex + (size_t)g * (p.N / 32) * (p.K / 32) +
                               (size_t)(slab / 2) * (p.K / 32) + me.k0 / 32 + lane)
             : 127u;
-    // ROWS: the exponents of rows r and r+8 at this thread's block of each step (byte t)
-    uint32_t era = 0x7F7F7F7Fu, erb = 0x7F7F7F7Fu;
-    if (ROWS && slab_ok) {
-        const uint8_t *e0 = p.ex + ((size_t)g * p.N + (size_t)slab * 16 + r) * (p.K / 32) + me.k0 / 32;
-        era = erb = 0;
-#pragma unroll
-        for (int t = 0; t < kMaxKt / kKS; ++t) {
-            const int blk = 4 * t + q;
-            const uint32_t ea = blk < nkb ? (uint32_t)__ldg(e0 + blk) : 127u;
-            const uint32_t eb = blk < nkb ? (uint32_t)__ldg(e0 + (size_t)8 * (p.K / 32) + blk) : 127u;
-            era |= ea << (8 * t);
-            erb |= eb << (8 * t);
-        }
-    }
+    // ROWS: the exponents of rows r and r+8 from their rows of exponents (block k0/32 + i)
+    const uint8_t *er0 = p.ex + ((size_t)g * p.N + (size_t)slab * 16 + r) * (p.K / 32) + me.k0 / 32;
+    const uint8_t *er8 = er0 + (size_t)8 * (p.K / 32);
     uint32_t emax = ereg;
-    if (ROWS) {
-#pragma unroll
-        for (int t = 0; t < 4; ++t) emax = max(emax, max((era >> (8 * t)) & 0xFFu, (erb >> (8 * t)) & 0xFFu));
-    }
+    if (ROWS && slab_ok)
+        for (int i = 0; i < nkb; ++i) emax = max(emax, max((uint32_t)__ldg(er0 + i), (uint32_t)__ldg(er8 + i)));
     const bool two = __any_sync(0xFFFFFFFFu, emax > 134u);
-    const BoxOffs bo = box_offsets(r, q);
 
     // ---- before the wait: rebuild every step; steps 1.. into tensor memory, step 0 into
     //      registers (the first MMAs after the wait need no tensor-memory round trip)
@@ -549,29 +480,36 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
             if (lane == 0) report_timeout(p.status);
         }
     }
+    auto step_exps = [&](int t, uint32_t (&e)[4], uint32_t (&eb)[4], uint32_t &mine) {
+        mine = 0;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const int blk = 4 * t + v;  // block of the task
+            const bool in = !err && slab_ok && blk < nkb;
+            mine |= in ? 1u << v : 0u;
+            const uint32_t eblk = __shfl_sync(0xFFFFFFFFu, ereg, blk & 31);
+            e[v] = ROWS ? (in ? (uint32_t)__ldg(er0 + blk) : 127u) : eblk;
+            eb[v] = ROWS ? (in ? (uint32_t)__ldg(er8 + blk) : 127u) : eblk;
+        }
+    };
     for (int t = 1; t < nst; ++t) {
-        const int col = me.k0 + t * kKS;
-        const bool mine = !err && slab_ok && col + q * 32 < me.k1;
-        const uint32_t eblk = __shfl_sync(0xFFFFFFFFu, ereg, (4 * t + q) & 31);
-        const uint32_t e = ROWS ? (era >> (8 * t)) & 0xFFu : eblk;
-        const uint32_t eb = ROWS ? (erb >> (8 * t)) & 0xFFu : eblk;
+        uint32_t e[4], eb[4], mine;
+        step_exps(t, e, eb, mine);
         uint32_t a[32];
         if (two)
-            decode_box<true, ROWS>(region + t * kSlotBytes, bo, mine, e, eb, a, mxa, mxb);
+            decode_box<true, ROWS>(region + t * kSlotBytes, r, q, mine, e, eb, a, mxa, mxb);
         else
-            decode_box<false, ROWS>(region + t * kSlotBytes, bo, mine, e, eb, a, mxa, mxb);
+            decode_box<false, ROWS>(region + t * kSlotBytes, r, q, mine, e, eb, a, mxa, mxb);
         tmem_st32(tbase + 32u * t, a);
     }
     uint32_t cur[32];
     {
-        const bool mine = !err && slab_ok && me.k0 + q * 32 < me.k1;
-        const uint32_t eblk = __shfl_sync(0xFFFFFFFFu, ereg, q);
-        const uint32_t e = ROWS ? era & 0xFFu : eblk;
-        const uint32_t eb = ROWS ? erb & 0xFFu : eblk;
+        uint32_t e[4], eb[4], mine;
+        step_exps(0, e, eb, mine);
         if (two)
-            decode_box<true, ROWS>(region, bo, mine, e, eb, cur, mxa, mxb);
+            decode_box<true, ROWS>(region, r, q, mine, e, eb, cur, mxa, mxb);
         else
-            decode_box<false, ROWS>(region, bo, mine, e, eb, cur, mxa, mxb);
+            decode_box<false, ROWS>(region, r, q, mine, e, eb, cur, mxa, mxb);
     }
     tmem_wait_st();
 
@@ -620,81 +558,41 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
     const int nsteps = opaque(nst);
     const int active = opaque(me.active ? 1 : 0);
     tile_addr = (uint32_t)opaque((int)tile_addr);
-    __syncthreads();  // every warp's weight boxes are rebuilt: the regions may take x
-    // the regions were read through the generic proxy; x lands through the async proxy
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();  // the staged parameters are visible to every thread
 
     // ---- the dependency wait: x (and y) belong to the kernels before this one
     pdl_wait();
     const PostParams &prm = sp;  // read from shared memory where used
 
-    // ---- x tiles of the task's steps, in the layout of a 128-byte-swizzled 8 x 64 box pair
-    //      per step (rows >= M as zeros)
-    const bool task_ok = k1 > k0;
-    if (prm.xtma) {
-        // one 2 KB box a step, each on its own barrier, issued by lanes 0.. of the first
-        // warp of the task's column range: the step's MMAs start as soon as it lands
-        if (xj == 0 && lane < nsteps && task_ok) {
-            mbar_arrive_expect_tx(&xbar[warp][lane], (uint32_t)kSlotBytes);
-            tma_4d(region + lane * kSlotBytes, &p.xmap, 0, 0, k0 / 64 + 2 * lane, g, &xbar[warp][lane]);
-        }
-    } else {
-        const long long gk = (long long)prm.G * prm.K;
-        for (int c = xj * 32 + lane; c < nsteps * 128; c += xn * 32) {
-            const int t = c >> 7, row = (c >> 4) & 7, unit = c & 15;
-            const int col = k0 + t * kKS + unit * 8;  // first of the copy's 8 columns
-            const bool in = task_ok && row < prm.M && (long long)g * prm.K + col < gk;
-            const uint16_t *src = prm.x + (in ? (size_t)row * prm.ldx + (size_t)g * prm.K + col : 0);
-            cp_async_16_zfill(xregion + t * kSlotBytes + (unit >> 3) * 1024 + row * 128 +
-                                  (((unit & 7) ^ row) << 4),
-                              src, in ? 16u : 0u);
-        }
-        cp_async_wait_all();
-        __syncthreads();
+    // ---- x: token r's pieces of every step of the task, straight into registers (rows >= M
+    //      and blocks past the task as zeros)
+    uint4 xa[kPre][4];
+    {
+        const bool row_ok = r < prm.M && k1 > k0;
+        const uint16_t *xrow = prm.x + (size_t)r * prm.ldx + (size_t)g * prm.K + 8 * q;
+#pragma unroll
+        for (int t = 0; t < kPre; ++t)
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const int col = k0 + t * kKS + 32 * v;  // the piece's block
+                xa[t][v] = row_ok && t < boxed_steps && col < k1 ? ld_cg_v4(xrow + col) : make_uint4(0, 0, 0, 0);
+            }
     }
 
-    // ---- MMAs, in half steps (4 MMAs, 16 fragment registers each).  Step t's fragments are
-    //      in cur; the next half's arrive from tensor memory into nh while the current
-    //      half's MMAs run, and are moved into cur once those MMAs have been issued (the
-    //      asynchronous load never writes a register an MMA in flight may still read).
-    float acc[4][4];
+    // ---- MMAs: step 0's fragments in cur, the others back from tensor memory a step at a time
+    float acc[2][4];
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int a = 0; a < 2; ++a)
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[a][c] = 0.0f;
 #pragma unroll
     for (int t = 0; t < kPre; ++t) {
         if (t < nsteps) {
-            const bool more = t + 1 < nsteps;
-            if (prm.xtma && task_ok) {
-                const bool ok = err || mbar_wait_bounded(&xbar[xl][t], 0u, prm.timeout_ns);
-                if (__any_sync(0xFFFFFFFFu, !ok)) {
-                    if (lane == 0) report_timeout(prm.status);
-                    err = 1;
-                    *(volatile int *)&s_err = 1;
-                }
-            }
-            const int col = k0 + t * kKS;
-            const bool mine = t < boxed_steps && col + q * 32 < k1;
-            const bool run = !err && t < boxed_steps;
-            uint4 xv[2];
-            load_xhalf<0>(xregion + t * kSlotBytes, r, q, mine, xv);
-            uint32_t nh[16];
-            if (more) tmem_ld16(tbase + 32u * (t + 1), nh);       // next step, first half
-            if (run) mma_half<0>(cur, xv, acc);
-            load_xhalf<1>(xregion + t * kSlotBytes, r, q, mine, xv);
-            if (more) {
+            if (t > 0) {
+                tmem_ld32(tbase + 32u * t, cur);
                 tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 16; ++i) cur[i] = nh[i];
-                tmem_ld16(tbase + 32u * (t + 1) + 16u, nh);        // next step, second half
             }
-            if (run) mma_half<4>(cur, xv, acc);
-            if (more) {
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 16; ++i) cur[16 + i] = nh[i];
-            }
+            if (!err && t < boxed_steps) mma_step(cur, xa[t], acc);
         }
     }
 
@@ -704,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
         float v[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            v[c] = (acc[0][c] + acc[1][c]) + (acc[2][c] + acc[3][c]);
+            v[c] = acc[0][c] + acc[1][c];
             if ((c < 2 && fa) || (c >= 2 && fb)) v[c] = qnan;
         }
         if (prm.mode == kStreamPartials) {
@@ -785,12 +683,8 @@ __global__ void __launch_bounds__(kThreads, 2) lowm_kernel(const __grid_constant
         }
     }
 
-    // After an error, let the copies this warp issued land before the block exits.
-    if (err) {
-        if (lane == 0 && nbox > 0 && !prm.skip_loads) (void)mbar_wait_bounded(&wbar[warp], 0u, prm.timeout_ns);
-        if (prm.xtma && xj == 0 && task_ok && lane < nsteps)
-            (void)mbar_wait_bounded(&xbar[warp][lane], 0u, prm.timeout_ns);
-    }
+    // After an error, let the weight boxes this warp issued land before the block exits.
+    if (err && lane == 0 && nbox > 0 && !prm.skip_loads) (void)mbar_wait_bounded(&wbar[warp], 0u, prm.timeout_ns);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -854,45 +748,6 @@ cudaError_t weight_map(const uint8_t *w8, long long rows, int K, CUtensorMap *ou
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (res != CUDA_SUCCESS) return cudaErrorInvalidValue;
     keys[next] = MapKey{w8, rows, K};
-    maps[next] = m;
-    next = (next + 1) % 64;
-    if (used < 64) ++used;
-    *out = m;
-    return cudaSuccess;
-}
-
-// Tensor maps of recently used activations: x[M][ldx] bf16 as {64 columns, M rows, K/64
-// chunks, G groups}, box {64, 8, 2, 1}, 128-byte swizzle (the 8 x 128 tile of one step).
-// Needs K % 64 == 0.  Returns cudaErrorNotSupported where the driver declines the map.
-struct XKey {
-    const void *ptr;
-    long long ldx;
-    int M, K, G;
-};
-
-cudaError_t x_map(const void *x, int M, int K, int G, long long ldx, CUtensorMap *out) {
-    static std::mutex mu;
-    static XKey keys[64];
-    static CUtensorMap maps[64];
-    static int used = 0, next = 0;
-    std::lock_guard<std::mutex> lock(mu);
-    for (int i = 0; i < used; ++i)
-        if (keys[i].ptr == x && keys[i].ldx == ldx && keys[i].M == M && keys[i].K == K && keys[i].G == G) {
-            *out = maps[i];
-            return cudaSuccess;
-        }
-    EncodeTiledFn fn = encode_tiled_fn();
-    if (!fn) return cudaErrorNotSupported;
-    CUtensorMap m;
-    const cuuint64_t dims[4] = {64u, (cuuint64_t)M, (cuuint64_t)(K / 64), (cuuint64_t)G};
-    const cuuint64_t strides[3] = {(cuuint64_t)ldx * 2u, 128u, (cuuint64_t)K * 2u};
-    const cuuint32_t box[4] = {64u, 8u, (cuuint32_t)(kKS / 64), 1u};
-    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-    const CUresult res = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(x), dims, strides,
-                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (res != CUDA_SUCCESS) return cudaErrorNotSupported;
-    keys[next] = XKey{x, ldx, M, K, G};
     maps[next] = m;
     next = (next + 1) % 64;
     if (used < 64) ++used;
@@ -981,15 +836,6 @@ cudaError_t launch_lowm(const StreamPlan &pl, const void *x, long long ldx, cons
     LowParams prm;
     cudaError_t e = weight_map(w8, (long long)G * N, K, &prm.wmap);
     if (e != cudaSuccess) return e;
-    // x by one TMA box a task where every task starts on a 64-column chunk of its group
-    prm.xtma = 0;
-    if (K % 64 == 0 && pl.chunk_cols % 64 == 0 && pl.kt % 64 == 0) {
-        e = x_map(x, M, K, G, ldx, &prm.xmap);
-        if (e == cudaSuccess)
-            prm.xtma = 1;
-        else if (e != cudaErrorNotSupported)
-            return e;
-    }
     prm.x = static_cast<const uint16_t *>(x);
     prm.ldx = ldx;
     prm.ex = ex;
