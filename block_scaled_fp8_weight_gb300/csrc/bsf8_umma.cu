@@ -11,17 +11,21 @@
 // tile of up to 192 token rows (calls with more rows run one tile a grid z-index, each
 // rebuilding the weights it streams: past a few hundred rows the product is bound by the
 // tensor cores, not by the weight stream).
-// Per 64-column step:
-//   * the copy warp loads the step's codes (128 rows x 64 bytes, one TMA box; lane 0, up to
-//     10 steps ahead, before the dependency wait too) and the step's x tile (lane 1: the M
-//     token rows, zero-filled to a multiple of 16, x 64 columns, one box with the 128-byte
-//     swizzle);
-//   * eight rebuild warps (warp d rebuilds rows 16 d .. 16 d + 15) turn the codes into exact
-//     bf16 weights -- the rebuild of bsf8_device.cuh -- and store them as the MMA's A
-//     operand: K-major, 128-byte swizzle, 8-row atoms 1 KB apart;
-//   * one thread of the MMA warp issues four tcgen05.mma (M = 128, N = tokens, K = 16) into
-//     an fp32 accumulator in tensor memory and commits them to the barriers that free the
-//     step's A and x slots.
+// Per 128-column step:
+//   * one copy warp loads the step's codes (128 rows x 128 bytes, one TMA box, up to 8 steps
+//     ahead, before the dependency wait too), another the step's x tile (the token rows,
+//     zero-filled to a multiple of 16, x 128 columns, two boxes of 64 with the 128-byte
+//     swizzle), each wait loop on a warp of its own;
+//   * eight rebuild warps turn the codes into exact bf16 weights -- the rebuild of
+//     bsf8_device.cuh -- and store them straight into tensor memory as the MMA's A operand
+//     (thread = weight row = TMEM lane, two bf16 a column; the two warps of a TMEM lane
+//     quarter take 64 columns each);
+//   * one thread of the MMA warp issues eight tcgen05.mma (M = 128, N = tokens, K = 16; A in
+//     tensor memory, x from shared memory) into an fp32 accumulator in tensor memory and
+//     commits them to the barriers that free the step's A and x slots.
+// A in tensor memory rather than shared memory: at 192 tokens a step moved ~190 KB through
+// shared memory (the copies, the codes read, A written and read, x read), which bound the
+// step at ~1500 cycles against 768 of tensor-core work; A in tensor memory takes 64 KB off.
 // At the end the rebuild warps read the accumulators back (tcgen05.ld, thread = weight row;
 // two warps a TMEM lane quarter split the token columns) and store y (one split) or the
 // split's fp32 partials (the fixed-order reduce follows).
@@ -45,16 +49,18 @@ namespace {
 constexpr int kRows = 128;           // weight rows a block (the MMA's M)
 constexpr int kKB = 128;             // columns a step: 128-byte rows of codes
 constexpr int kHalf = 64;            // columns of one 128-byte swizzle atom of bf16
-constexpr int kCodesBytes = kRows * kKB;        // 16 KB of codes a step
-constexpr int kAHalfBytes = kRows * kHalf * 2;  // 16 KB: A tile of one atom column
-constexpr int kABytes = 2 * kAHalfBytes;        // 32 KB of bf16 a step
-constexpr int kDaMax = 3, kDcMax = 8, kDxMax = 12;  // ring depths, set per call
-// Dynamic shared memory a block: the A, x and codes rings, sized per call (x tiles grow
-// with the tokens): x 2 .. 12 tiles within 48 KB unless two need more, A 2 steps of
-// 32 KB, the codes ring the rest, 2 .. 8 steps.
+constexpr int kCodesBytes = kRows * kKB;  // 16 KB of codes a step
+constexpr int kACols = kKB / 2;      // TMEM columns of a step's A (two bf16 a 32-bit column)
+constexpr int kDsMax = 4, kDcMax = 8;  // ring depths, set per call
+// Dynamic shared memory a block: the x tiles of the stage ring (a stage = one step's A slot
+// in tensor memory and its x tile) and the codes ring, sized per call (x tiles grow with the
+// tokens): 2 .. 4 stages, as many as tensor memory holds A slots for and 64 KB of x tiles
+// unless two need more; the codes ring the rest, 2 .. 8 steps.
 constexpr int kSmemU = 208 * 1024;
-constexpr int kRebuildWarps = 8;                // 16 weight rows each
-constexpr int kThreadsU = (2 + kRebuildWarps) * 32;  // warp 0 copies, warp 1 MMA, 2.. rebuild
+constexpr int kRebuildWarps = 8;     // two a TMEM lane quarter, 64 columns of a step each
+// warp 0 copies codes, warp 1 issues MMAs, warps 2 .. 9 rebuild, warp 10 copies x
+constexpr int kXWarp = 2 + kRebuildWarps;
+constexpr int kThreadsU = (3 + kRebuildWarps) * 32;
 constexpr int kMaxTok = 192;  // tokens a block (a token tile; more rows take more tiles)
 constexpr int kMaxRowsU = 16384;  // token rows a call (BSF8_MAX_M)
 constexpr int kMaxSplitBlocks = 1024;  // 32-column exponent blocks of a split kept in smem
@@ -74,7 +80,8 @@ struct UmmaParams {
     float *partials;
     int M, N, K, G, S, chunk_cols, ntok;
     int to_partials;  // 1: store fp32 partials P[s] (even with one split), 0: store y
-    int dx, dc, da;   // x, codes and A ring depths
+    int ds, dc;       // stage (A slot + x tile) and codes ring depths
+    int tcols;        // tensor memory columns a block allocates (A slots, then accumulators)
     unsigned long long timeout_ns;
     int skip_loads;
     int *status;
@@ -122,12 +129,14 @@ __device__ __forceinline__ uint32_t mma_idesc(int n) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
 }
 
-__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
+// D (+)= A * B with A in tensor memory (lane = row of A, 8 columns = K 16 of bf16) and B in
+// shared memory (descriptor).
+__device__ __forceinline__ void umma_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -165,6 +174,20 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// 32 registers of this thread -> columns [taddr, taddr + 32) of its TMEM lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t max_xorsign_abs_u(uint32_t a, uint32_t b) {
     uint32_t d;
     asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -173,6 +196,34 @@ __device__ __forceinline__ uint32_t max_xorsign_abs_u(uint32_t a, uint32_t b) {
 
 __device__ __forceinline__ bool nan_code_seen_u(uint32_t mx) {
     return (mx & 0x7FFFu) >= 0x07F0u || ((mx >> 16) & 0x7FFFu) >= 0x07F0u;
+}
+
+// Rebuilds one 32-column block of this thread's row (c0: columns 0..15, c1: 16..31) to bf16,
+// a[i] = bf16x2(column 2i, column 2i + 1).  TWO: the scale 2^(e-127) in two multiplies (the
+// first by 2^120, so that no intermediate leaves bf16's range), exact for every exponent
+// byte; otherwise e <= 134 and one multiply by 2^(e-7).  mx keeps the largest magnitude
+// pattern before scaling (an e4m3 NaN code spreads to 0x07F0, above every finite code's
+// 0x07E0).  A template, so that the warp-uniform choice costs one branch a block.
+template <bool TWO>
+__device__ __forceinline__ void rebuild_block_u(const uint4 &c0, const uint4 &c1, uint32_t s1, uint32_t s2,
+                                                uint32_t (&a)[16], uint32_t &mx) {
+    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t t0, t1;
+        asm("prmt.b32 %0, %1, 0, 0x9180;" : "=r"(t0) : "r"(w[i]));
+        asm("prmt.b32 %0, %1, 0, 0xB3A2;" : "=r"(t1) : "r"(w[i]));
+        t0 = (t0 << 4) & 0x87F087F0u;
+        t1 = (t1 << 4) & 0x87F087F0u;
+        mx = max_xorsign_abs_u(mx, max_xorsign_abs_u(t0, t1));
+        uint32_t lo = bf16x2_mul(t0, s1), hi = bf16x2_mul(t1, s1);
+        if (TWO) {
+            lo = bf16x2_mul(lo, s2);
+            hi = bf16x2_mul(hi, s2);
+        }
+        a[2 * i] = lo;
+        a[2 * i + 1] = hi;
+    }
 }
 
 // Barrier of the rebuild warps only (named barrier 1).
@@ -191,11 +242,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64
 __global__ void __launch_bounds__(kThreadsU, 2) umma_kernel(const __grid_constant__ UmmaParams p) {
     extern __shared__ uint8_t dyn_smem[];
     uint8_t *const base = dyn_smem + ((1024u - (smem_u32(dyn_smem) & 1023u)) & 1023u);
-    uint8_t *const sA = base;                                   // da x 32 KB, 128B swizzle
-    uint8_t *const sX = sA + p.da * kABytes;                    // dx x ntok x 256 B
-    uint8_t *const sC = sX + p.dx * p.ntok * 256;                 // dc x 16 KB
-    __shared__ __align__(8) uint64_t full_c[kDcMax], empty_c[kDcMax], full_a[kDaMax], empty_a[kDaMax];
-    __shared__ __align__(8) uint64_t full_x[kDxMax], empty_x[kDxMax], d_full;
+    uint8_t *const sX = base;                                   // ds x ntok x 256 B
+    uint8_t *const sC = sX + p.ds * p.ntok * 256;               // dc x 16 KB
+    // full_c: a step's codes landed (TMA); empty_c: its rebuild read them (8 warps);
+    // full_x: a step's x tile landed (TMA); full_s: the stage is ready for the MMAs (8 rebuild
+    // warps, each after its part of A is in tensor memory; warp 2 after it also saw the x
+    // tile land, and all of them on a ragged last step, after they zeroed the x tail);
+    // empty_s: the stage's MMAs finished (commit); d_full: every MMA finished (commit).
+    __shared__ __align__(8) uint64_t full_c[kDcMax], empty_c[kDcMax];
+    __shared__ __align__(8) uint64_t full_x[kDsMax], full_s[kDsMax], empty_s[kDsMax], d_full;
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
     __shared__ uint32_t s_nan[4];  // per TMEM lane quarter: rows with an e4m3 NaN code
@@ -209,23 +264,19 @@ __global__ void __launch_bounds__(kThreadsU, 2) umma_kernel(const __grid_constan
     const int k0 = min(p.K, split * p.chunk_cols), k1 = min(p.K, k0 + p.chunk_cols);
     const int nkb = (k1 - k0 + kKB - 1) / kKB;
     const int nrun = (nkb + kChunkSteps - 1) / kChunkSteps;  // accumulators (runs of steps)
-    uint32_t tcols = 32;
-    while ((int)tcols < max(1, nrun) * p.ntok) tcols *= 2;   // the plan keeps this <= 512
     const int xbytes = p.ntok * 256;  // a step's x tile: two 64-column atoms
-    const int kDx = p.dx, kDc = p.dc, kDa = p.da;  // ring depths of this call
+    const int kDs = p.ds, kDc = p.dc;  // ring depths of this call
+    const uint32_t dbase = (uint32_t)(kDs * kACols);  // first accumulator column (A slots first)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kDcMax; ++i) {
             mbar_init(&full_c[i], 1);
             mbar_init(&empty_c[i], kRebuildWarps);
         }
-        for (int i = 0; i < kDaMax; ++i) {
-            mbar_init(&full_a[i], kRebuildWarps);
-            mbar_init(&empty_a[i], 1);
-        }
-        for (int i = 0; i < kDxMax; ++i) {
+        for (int i = 0; i < kDsMax; ++i) {
             mbar_init(&full_x[i], 1);
-            mbar_init(&empty_x[i], 1);
+            mbar_init(&full_s[i], kRebuildWarps);
+            mbar_init(&empty_s[i], 1);
         }
         mbar_init(&d_full, 1);
         s_err = 0;
@@ -234,7 +285,7 @@ __global__ void __launch_bounds__(kThreadsU, 2) umma_kernel(const __grid_constan
         prefetch_tmap(&p.cmap);
         prefetch_tmap(&p.xmap);
     }
-    if (warp == 1) tmem_alloc_u(&s_tmem, tcols);
+    if (warp == 1) tmem_alloc_u(&s_tmem, (uint32_t)p.tcols);
     tc_before();
     __syncthreads();
     tc_after();
@@ -242,14 +293,17 @@ __global__ void __launch_bounds__(kThreadsU, 2) umma_kernel(const __grid_constan
     const uint32_t tmem = s_tmem;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ copies
-        if (lane == 0) {  // codes: static, streamed ahead from the start
+        // ------------------------------------------------------------ codes
+        if (lane == 0) {  // static, streamed ahead from the start
             const uint64_t pol = evict_first_policy_u();
             int n = 0;
             bool bad = false;
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int cs = kb % kDc;
-                if (kb >= kDc && !mbar_wait_bounded(&empty_c[cs], (uint32_t)(((kb / kDc) - 1) & 1), p.timeout_ns)) {
+            // ring slot and its use's parity by counters (a division by the run-time depth costs
+            // a reciprocal sequence a step)
+            int cs = 0;
+            uint32_t ph = 0;
+            for (int kb = 0; kb < nkb; ++kb, cs = cs + 1 == kDc ? 0 : cs + 1, ph ^= cs == 0 ? 1u : 0u) {
+                if (kb >= kDc && !mbar_wait_bounded(&empty_c[cs], ph ^ 1u, p.timeout_ns)) {
                     bad = true;
                     break;
                 }
@@ -265,20 +319,25 @@ __global__ void __launch_bounds__(kThreadsU, 2) umma_kernel(const __grid_constan
             if (*(volatile int *)&s_err && !p.skip_loads)  // let issued copies land (bounded)
                 for (int i = max(0, n - kDc); i < n; ++i)
                     (void)mbar_wait_bounded(&full_c[i % kDc], (uint32_t)((i / kDc) & 1), p.timeout_ns);
-        } else if (lane == 1) {  // x: after the dependency wait
+        }
+        __syncwarp();
+    } else if (warp == kXWarp) {
+        // ------------------------------------------------------------ x, after the dependency wait
+        if (lane == 0) {
             pdl_wait();
             int n = 0;
             bool bad = false;
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int xs = kb % kDx;
-                if (kb >= kDx && !mbar_wait_bounded(&empty_x[xs], (uint32_t)(((kb / kDx) - 1) & 1), p.timeout_ns)) {
+            int ss = 0;
+            uint32_t ph = 0;
+            for (int kb = 0; kb < nkb; ++kb, ss = ss + 1 == kDs ? 0 : ss + 1, ph ^= ss == 0 ? 1u : 0u) {
+                if (kb >= kDs && !mbar_wait_bounded(&empty_s[ss], ph ^ 1u, p.timeout_ns)) {
                     bad = true;
                     break;
                 }
-                mbar_arrive_expect_tx(&full_x[xs], (uint32_t)xbytes);
+                mbar_arrive_expect_tx(&full_x[ss], (uint32_t)xbytes);
                 if (!p.skip_loads) {
-                    tma_3d_u(sX + xs * xbytes, &p.xmap, k0 + kb * kKB, g, tok0, &full_x[xs]);
-                    tma_3d_u(sX + xs * xbytes + xbytes / 2, &p.xmap, k0 + kb * kKB + kHalf, g, tok0, &full_x[xs]);
+                    tma_3d_u(sX + ss * xbytes, &p.xmap, k0 + kb * kKB, g, tok0, &full_x[ss]);
+                    tma_3d_u(sX + ss * xbytes + xbytes / 2, &p.xmap, k0 + kb * kKB + kHalf, g, tok0, &full_x[ss]);
                 }
                 ++n;
             }
@@ -287,62 +346,52 @@ __global__ void __launch_bounds__(kThreadsU, 2) umma_kernel(const __grid_constan
                 report_timeout(p.status);
             }
             if (*(volatile int *)&s_err && !p.skip_loads)
-                for (int i = max(0, n - kDx); i < n; ++i)
-                    (void)mbar_wait_bounded(&full_x[i % kDx], (uint32_t)((i / kDx) & 1), p.timeout_ns);
+                for (int i = max(0, n - kDs); i < n; ++i)
+                    (void)mbar_wait_bounded(&full_x[i % kDs], (uint32_t)((i / kDs) & 1), p.timeout_ns);
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issue
-        const uint32_t idesc = mma_idesc(p.ntok);
-        bool bad = false;
-        const int tail = (k1 - k0) % kKB;  // columns of the last step inside the split (0: all)
-        for (int kb = 0; kb < nkb; ++kb) {
-            const int as = kb % kDa, xs = kb % kDx;
-            if (!warp_wait(&full_a[as], (uint32_t)((kb / kDa) & 1), p.timeout_ns) ||
-                !warp_wait(&full_x[xs], (uint32_t)((kb / kDx) & 1), p.timeout_ns)) {
-                bad = true;
-                break;
-            }
-            uint8_t *xt = sX + xs * xbytes;
-            if (kb == nkb - 1 && tail != 0) {
-                // x columns past the split's end belong to the next split: zero them (the
-                // weights there are zero, and 0 * inf would be NaN); 16 units of 8 columns
-                const int fu = tail / 8, units = 16 - fu;
-                for (int i = lane; i < p.ntok * units; i += 32) {
-                    const int r = i / units, u = fu + i % units;
-                    *reinterpret_cast<uint4 *>(xt + (u >> 3) * (xbytes / 2) + (r >> 3) * 1024 + (r & 7) * 128 +
-                                               (((u & 7) ^ (r & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+        // ------------------------------------------------------------ MMA issue: one thread
+        // One wait, eight MMAs and one commit a step, nothing else: every instruction of this
+        // chain queues behind the rebuild warps' shared- and tensor-memory traffic (~100
+        // cycles each when the loop also synchronised its warp).
+        if (lane == 0) {
+            const uint32_t idesc = mma_idesc(p.ntok);
+            bool bad = false;
+            int ss = 0;
+            uint32_t ph = 0;
+            for (int kb = 0; kb < nkb; ++kb, ss = ss + 1 == kDs ? 0 : ss + 1, ph ^= ss == 0 ? 1u : 0u) {
+                if (!mbar_wait_bounded(&full_s[ss], ph, p.timeout_ns)) {
+                    bad = true;
+                    break;
                 }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-            }
-            if (lane == 0) {
                 tc_after();
-                const uint32_t sa = smem_u32(sA + as * kABytes), sb = smem_u32(xt);
-                const uint32_t dcol = (uint32_t)((kb / kChunkSteps) * p.ntok);  // this run's accumulator
+                const uint32_t sb = smem_u32(sX + ss * xbytes);
+                const uint32_t ta = tmem + (uint32_t)(ss * kACols);
+                const uint32_t dcol = tmem + dbase + (uint32_t)((kb / kChunkSteps) * p.ntok);  // this run's accumulator
 #pragma unroll
-                for (int ks = 0; ks < kKB / 16; ++ks) {  // atom column ks / 4, +32 bytes a K slice
-                    const uint64_t ad = sw128_desc(sa + (ks >> 2) * kAHalfBytes) + 2 * (ks & 3);
+                for (int ks = 0; ks < kKB / 16; ++ks) {  // x: atom column ks / 4, +32 bytes a K slice
                     const uint64_t bd = sw128_desc(sb + (ks >> 2) * (xbytes / 2)) + 2 * (ks & 3);
-                    umma_f16(tmem + dcol, ad, bd, idesc, (kb % kChunkSteps > 0 || ks > 0) ? 1u : 0u);
+                    umma_ts(dcol, ta + 8u * (uint32_t)ks, bd, idesc, (kb % kChunkSteps > 0 || ks > 0) ? 1u : 0u);
                 }
-                umma_commit(&empty_a[as]);
-                umma_commit(&empty_x[xs]);
+                umma_commit(&empty_s[ss]);
             }
-            __syncwarp();
+            if (bad) {
+                *(volatile int *)&s_err = 1;
+                report_timeout(p.status);
+            }
+            umma_commit(&d_full);  // completes once every MMA above has finished
         }
-        if (bad && lane == 0) {
-            s_err = 1;
-            report_timeout(p.status);
-        }
-        if (lane == 0) umma_commit(&d_full);  // completes once every MMA above has finished
         __syncwarp();
     } else {
         // ------------------------------------------------------------ rebuild + epilogue
-        const int d = warp - 2;                // rows 16 d .. 16 d + 15 of the block
-        const int rsub = lane >> 3, unit = lane & 7;  // rows 16 d + rsub + 4 i, 16 codes each
-        const int n32 = row0 + 32 * (d >> 1);  // first row of the warp's exponent row block
-        const bool rows_ok = n32 < p.N;
+        const int qd = warp & 3;               // TMEM lane quarter this warp may access
+        const int part = (warp - 2) >> 2;      // 0, 1: the step's columns 64 part .. (rebuild),
+                                               //       the token chunks 16 part + 32 i (epilogue)
+        const int row = 32 * qd + lane;        // this thread's weight row in the block = TMEM lane
+        const int n = row0 + row;
+        const bool rows_ok = row0 + 32 * qd < p.N;  // warp-uniform (N is a multiple of 32)
+        const int tail = (k1 - k0) % kKB;      // columns of the last step inside the split (0: all)
         {   // the split's exponent bytes of the block's four 32-row blocks (static: before the wait)
             const int kb0 = k0 / 32, nb = (k1 - k0) / 32;
             for (int i = threadIdx.x - 64; i < 4 * nb; i += kRebuildWarps * 32) {
@@ -353,109 +402,133 @@ __global__ void __launch_bounds__(kThreadsU, 2) umma_kernel(const __grid_constan
             }
             named_sync_rebuild();
         }
-        const uint8_t *erow = s_exp[d >> 1];
-        uint32_t mx[4] = {0, 0, 0, 0};
+        const uint8_t *erow = s_exp[qd];
+        const uint32_t tlane = tmem + ((uint32_t)(32 * qd) << 16);
+        uint32_t mx = 0;
         bool bad = false;
-        for (int kb = 0; kb < nkb; ++kb) {
-            const int cs = kb % kDc, as = kb % kDa;
-            if (!warp_wait(&full_c[cs], (uint32_t)((kb / kDc) & 1), p.timeout_ns) ||
-                (kb >= kDa && !warp_wait(&empty_a[as], (uint32_t)(((kb / kDa) - 1) & 1), p.timeout_ns))) {
+        int cs = 0, ss = 0;          // ring slots, and the parities of their current uses
+        uint32_t cph = 0, sph = 0;
+        for (int kb = 0; kb < nkb; ++kb, cs = cs + 1 == kDc ? 0 : cs + 1, cph ^= cs == 0 ? 1u : 0u,
+                 ss = ss + 1 == kDs ? 0 : ss + 1, sph ^= ss == 0 ? 1u : 0u) {
+            if (!warp_wait(&full_c[cs], cph, p.timeout_ns) ||
+                (kb >= kDs && !warp_wait(&empty_s[ss], sph ^ 1u, p.timeout_ns))) {
                 bad = true;
                 break;
             }
-            const int kcol = k0 + kb * kKB + unit * 16;  // the lane's 16 columns
-            const bool cols_ok = rows_ok && kcol < k1;
-            const uint32_t e = cols_ok ? (uint32_t)erow[(kcol - k0) / 32] : 127u;
-            const bool two = __any_sync(0xFFFFFFFFu, e > 134u);
-            uint32_t s1, s2 = 0;
-            if (two) {
-                s1 = 0x7B807B80u;
-                const uint32_t bb = e == 0 ? 0x0040u : (e << 7);
-                s2 = bb | (bb << 16);
-            } else {
-                const uint32_t b = (e + 120u) << 7;
-                s1 = b | (b << 16);
-            }
-            const uint8_t *cst = sC + cs * kCodesBytes;
-            uint8_t *ast = sA + as * kABytes;
+            tc_after();  // the MMAs that read this A slot have finished
+            const uint8_t *crow = sC + cs * kCodesBytes + row * 128;
+            uint32_t a[32];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int row = 16 * d + rsub + 4 * i;  // row inside the block
-                // codes: 128-byte rows with the 128-byte swizzle (unit u of row r at u ^ r % 8)
-                const uint4 c = cols_ok ? *reinterpret_cast<const uint4 *>(cst + row * 128 + ((unit ^ (row & 7)) << 4))
-                                        : make_uint4(0, 0, 0, 0);
-                uint32_t o[8];
-                const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint32_t t0, t1;
-                    asm("prmt.b32 %0, %1, 0, 0x9180;" : "=r"(t0) : "r"(w[j]));
-                    asm("prmt.b32 %0, %1, 0, 0xB3A2;" : "=r"(t1) : "r"(w[j]));
-                    t0 = (t0 << 4) & 0x87F087F0u;
-                    t1 = (t1 << 4) & 0x87F087F0u;
-                    mx[i] = max_xorsign_abs_u(mx[i], max_xorsign_abs_u(t0, t1));
-                    uint32_t lo = bf16x2_mul(t0, s1), hi = bf16x2_mul(t1, s1);
-                    if (two) {
-                        lo = bf16x2_mul(lo, s2);
-                        hi = bf16x2_mul(hi, s2);
+            for (int b = 0; b < 2; ++b) {  // the warp's two 32-column blocks of the step
+                const int cb = 2 * part + b;   // block inside the step
+                const int kcol = k0 + kb * kKB + 32 * cb;
+                uint32_t ab[16];
+                if (rows_ok && kcol < k1) {    // warp-uniform
+                    // codes: 128-byte rows with the 128-byte swizzle (unit u of row r at u ^ r % 8)
+                    const uint4 c0 = *reinterpret_cast<const uint4 *>(crow + (((2 * cb) ^ (row & 7)) << 4));
+                    const uint4 c1 = *reinterpret_cast<const uint4 *>(crow + (((2 * cb + 1) ^ (row & 7)) << 4));
+                    const uint32_t e = erow[(kcol - k0) / 32];  // one exponent a warp
+                    if (e > 134u) {
+                        const uint32_t bb = e << 7;  // 2^(e-127)
+                        rebuild_block_u<true>(c0, c1, 0x7B807B80u, bb | (bb << 16), ab, mx);
+                    } else {
+                        const uint32_t bb = (e + 120u) << 7;  // 2^(e-7)
+                        rebuild_block_u<false>(c0, c1, bb | (bb << 16), 0u, ab, mx);
                     }
-                    o[2 * j] = lo;
-                    o[2 * j + 1] = hi;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) ab[i] = 0u;
                 }
-                // A: the lane's 16 columns are units 2 (unit % 4) and +1 of atom column unit / 4
-                uint8_t *arow = ast + (unit >> 2) * kAHalfBytes + (row >> 3) * 1024 + (row & 7) * 128;
-                const int u0 = 2 * (unit & 3);
-                *reinterpret_cast<uint4 *>(arow + ((u0 ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-                *reinterpret_cast<uint4 *>(arow + (((u0 + 1) ^ (row & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) a[16 * b + i] = ab[i];
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // A is read by the tensor core
+            tmem_st32(tlane + (uint32_t)(ss * kACols + 32 * part), a);
+            tmem_wait_st();
+            tc_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&empty_c[cs]);
-                mbar_arrive(&full_a[as]);
+            if (lane == 0) mbar_arrive(&empty_c[cs]);
+            // The step's x tile must have landed before the MMAs read it: one warp sees to
+            // that (each wait costs its warp a few hundred cycles under the step's traffic),
+            // all of them on a ragged last step, whose tail they zero.
+            const bool tail_step = kb == nkb - 1 && tail != 0;
+            if ((warp == 2 || tail_step) && !warp_wait(&full_x[ss], sph, p.timeout_ns)) {
+                bad = true;
+                break;
             }
+            if (tail_step) {
+                // x columns past the split's end belong to the next split: zero them (the
+                // weights there are zero, and 0 * inf would be NaN); 16 units of 8 columns
+                uint8_t *xt = sX + ss * xbytes;
+                const int fu = tail / 8, units = 16 - fu;
+                for (int i = threadIdx.x - 64; i < p.ntok * units; i += kRebuildWarps * 32) {
+                    const int r = i / units, u = fu + i % units;
+                    *reinterpret_cast<uint4 *>(xt + (u >> 3) * (xbytes / 2) + (r >> 3) * 1024 + (r & 7) * 128 +
+                                               (((u & 7) ^ (r & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+            }
+            if (lane == 0) mbar_arrive(&full_s[ss]);
         }
         if (bad) {
             *(volatile int *)&s_err = 1;
             if (lane == 0) report_timeout(p.status);
         }
         // rows with an e4m3 NaN code, as bits of their TMEM lane quarter's mask
-        uint32_t nmask = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            if (nan_code_seen_u(mx[i])) nmask |= 1u << ((16 * d + rsub + 4 * i) & 31);
-        nmask = __reduce_or_sync(0xFFFFFFFFu, nmask);
-        if (lane == 0 && nmask) atomicOr(&s_nan[d >> 1], nmask);
+        const uint32_t nmask = __ballot_sync(0xFFFFFFFFu, nan_code_seen_u(mx));
+        if (lane == 0 && nmask) atomicOr(&s_nan[qd], nmask);
 
         pdl_wait();  // y may still be read by the kernels before this one
         const bool dok = warp_wait(&d_full, 0u, p.timeout_ns);
         named_sync_rebuild();  // every rebuild warp has posted its NaN rows
         tc_after();
-        const int qd = warp & 3;               // TMEM lane quarter this warp may read
-        const int half = (warp - 2) >> 2;      // warps of a quarter split the 16-column chunks
-        const int n = row0 + 32 * qd + lane;   // this thread's weight row = its TMEM lane
         const bool store = dok && !*(volatile int *)&s_err && n < p.N;
         const bool poison = (s_nan[qd] >> lane) & 1u;
-        for (int c0 = 16 * half; c0 < p.ntok; c0 += 32) {
+        // Uniform conditions are taken once a 16-token chunk, and the NaN rows by a select: a
+        // branch per element (each with its reconvergence) cost ~3x the loads and stores.
+        const int mrows = p.M - tok0;  // token rows of this tile that exist
+        const size_t mstride = (size_t)p.G * p.N;  // one token row further in y or P[s]
+        for (int c0 = 16 * part; store && c0 < p.ntok && c0 < mrows; c0 += 32) {
             float acc[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
-            for (int run = 0; run < nrun; ++run) {  // the runs' accumulators, in run order
+            if (nrun > 0) {
                 uint32_t r[16];
-                tmem_ld16(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(run * p.ntok + c0), r);
+                tmem_ld16(tlane + dbase + (uint32_t)c0, r);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) acc[j] = run == 0 ? __uint_as_float(r[j]) : acc[j] + __uint_as_float(r[j]);
+                for (int j = 0; j < 16; ++j) acc[j] = __uint_as_float(r[j]);
+            } else {  // a split past K's end (more splits than 32-column blocks fill): zeros
+#pragma unroll
+                for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
+            }
+            for (int run = 1; run < nrun; ++run) {  // the runs' accumulators, in run order
+                uint32_t r[16];
+                tmem_ld16(tlane + dbase + (uint32_t)(run * p.ntok + c0), r);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) acc[j] += __uint_as_float(r[j]);
             }
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int m = tok0 + c0 + j;
-                if (!store || m >= p.M) continue;
-                float v = acc[j];
-                if (poison) v = __uint_as_float(0x7FC00000u);
-                if (p.to_partials)
-                    p.partials[(((size_t)split * p.M + m) * p.G + g) * p.N + n] = v;
-                else
-                    p.y[((size_t)m * p.G + g) * p.N + n] = f32_to_bf16_rn(v);
+            for (int j = 0; j < 16; ++j) acc[j] = poison ? __uint_as_float(0x7FC00000u) : acc[j];
+            const size_t o0 = ((size_t)(tok0 + c0) * p.G + g) * p.N + n;
+            const int mj = min(16, mrows - c0);
+            if (p.to_partials) {
+                float *dst = p.partials + (size_t)split * p.M * mstride + o0;
+                if (mj == 16) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) dst[j * mstride] = acc[j];
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (j < mj) dst[j * mstride] = acc[j];
+                }
+            } else {
+                uint16_t *dst = p.y + o0;
+                if (mj == 16) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) dst[j * mstride] = f32_to_bf16_rn(acc[j]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (j < mj) dst[j * mstride] = f32_to_bf16_rn(acc[j]);
+                }
             }
         }
         if (!dok && lane == 0) report_timeout(p.status);
@@ -467,7 +540,7 @@ __global__ void __launch_bounds__(kThreadsU, 2) umma_kernel(const __grid_constan
         // every MMA must be finished before its accumulator columns are freed (bounded)
         (void)mbar_wait_bounded(&d_full, 0u, p.timeout_ns);
         tc_after();
-        tmem_dealloc_u(tmem, tcols);
+        tmem_dealloc_u(tmem, (uint32_t)p.tcols);
     }
 }
 
@@ -549,15 +622,26 @@ cudaError_t umma_map(const UKey &key, bool codes, CUtensorMap *out) {
 
 }  // namespace
 
+namespace {
+
+int umma_runs(const UmmaPlan &pl) {
+    return ((pl.chunk_cols + kKB - 1) / kKB + kChunkSteps - 1) / kChunkSteps;
+}
+
+// Tensor memory a block's A slots (kACols columns each) and its runs' accumulators (ntok
+// columns each) take.
+int umma_tmem_need(const UmmaPlan &pl, int da) { return da * kACols + umma_runs(pl) * pl.ntok; }
+
+}  // namespace
+
 UmmaPlan plan_umma(int M, int N, int K, int G, int S, bool partials) {
     UmmaPlan pl{};
     pl.S = S;
     pl.chunk_cols = ((K / 32 + S - 1) / S) * 32;
     pl.ntok = std::min(kMaxTok, (M + 15) / 16 * 16);  // tokens a tile
     pl.ttiles = (M + pl.ntok - 1) / std::max(1, pl.ntok);
-    // the split's runs of steps each need ntok accumulator columns of tensor memory
-    const int nrun = ((pl.chunk_cols + kKB - 1) / kKB + kChunkSteps - 1) / kChunkSteps;
-    pl.tmem_ok = (long long)nrun * pl.ntok <= kTmemMax;
+    // two A slots and the split's runs of steps (ntok accumulator columns each) in tensor memory
+    pl.tmem_ok = umma_tmem_need(pl, 2) <= kTmemMax;
     pl.row_blocks = (N + kRows - 1) / kRows;
     pl.grid_x = pl.row_blocks * S;
     pl.partials = partials || S > 1;
@@ -566,39 +650,50 @@ UmmaPlan plan_umma(int M, int N, int K, int G, int S, bool partials) {
     return pl;
 }
 
-// Splits for the tensor-core kernel: about one block an SM (the blocks stream, so more
-// blocks than SMs add a wave), then enough that the runs' accumulators fit tensor memory.
+// Up to 16 tokens two blocks share an SM (rings within ~106 KB, A slots and accumulators
+// within half of tensor memory): more blocks in flight to cover the per-step latency of one
+// block's pipeline, and no second wave on large N.
+bool umma_two_per_sm(const UmmaPlan &pl) { return pl.ntok <= 16 && umma_tmem_need(pl, 2) <= kTmemMax / 2; }
+
+// Splits for the tensor-core kernel: as many as keep every block in one wave (the blocks an
+// SM holds at once times the SMs; one block past that waits for a whole block's time -- 17
+// splits of the 1152-row weight made 153 blocks on 152 SMs), then enough that the A slots
+// and the runs' accumulators fit tensor memory.
 int umma_auto_split(int M, int N, int K, int G, int sms) {
     const long long ttiles = (M + kMaxTok - 1) / kMaxTok;
     const long long blocks = (long long)((N + kRows - 1) / kRows) * G * ttiles;
     const int smax = std::max(1, K / 32);
-    int S = (int)std::max(1LL, (sms + blocks / 2) / std::max(1LL, blocks));
+    const int per_sm = umma_two_per_sm(plan_umma(M, N, K, G, 1, false)) ? 2 : 1;
+    int S = (int)std::max(1LL, (long long)sms * per_sm / std::max(1LL, blocks));
     S = std::min(S, smax);
     while (S < smax && !plan_umma(M, N, K, G, S, false).ok) ++S;
     return S;
 }
 
-// Up to 16 tokens two blocks share an SM (rings within ~106 KB, accumulators within half of
-// tensor memory): more blocks in flight to cover the per-step latency of one block's
-// pipeline, and no second wave on large N.
-bool umma_two_per_sm(const UmmaPlan &pl) {
-    const int nrun = ((pl.chunk_cols + kKB - 1) / kKB + kChunkSteps - 1) / kChunkSteps;
-    return pl.ntok <= 16 && nrun * pl.ntok <= kTmemMax / 2;
-}
-
 int umma_smem_budget(const UmmaPlan &pl) { return umma_two_per_sm(pl) ? 106 * 1024 : kSmemU; }
 
-int umma_x_depth(const UmmaPlan &pl) {
-    const int bytes = umma_two_per_sm(pl) ? 8 * 1024 : 48 * 1024;
-    return std::max(2, std::min(kDxMax, bytes / (pl.ntok * 256)));
+// Stages (a step's A slot in tensor memory and its x tile): 2 .. 4, as many as tensor memory
+// leaves beside the accumulators and as 64 KB of x tiles hold (8 KB with two blocks an SM),
+// at least two.
+int umma_stage_depth(const UmmaPlan &pl) {
+    const bool two = umma_two_per_sm(pl);
+    const int cap = two ? kTmemMax / 2 : kTmemMax;
+    const int xcap = std::max(2, (two ? 8 * 1024 : 64 * 1024) / (pl.ntok * 256));
+    int ds = 2;
+    while (ds < kDsMax && ds < xcap && umma_tmem_need(pl, ds + 1) <= cap) ++ds;
+    return ds;
 }
 
-// A third A slot measured slower (the codes ring loses a step); two it is.
-int umma_a_depth(const UmmaPlan &) { return 2; }
-
 int umma_codes_depth(const UmmaPlan &pl) {
-    const int left = umma_smem_budget(pl) - 1024 - umma_a_depth(pl) * kABytes - umma_x_depth(pl) * pl.ntok * 256;
+    const int left = umma_smem_budget(pl) - 1024 - umma_stage_depth(pl) * pl.ntok * 256;
     return std::min(kDcMax, left / kCodesBytes);
+}
+
+// Tensor memory a block allocates: a power of two of at least 32 columns.
+int umma_tmem_cols(const UmmaPlan &pl) {
+    int c = 32;
+    while (c < umma_tmem_need(pl, umma_stage_depth(pl))) c *= 2;
+    return c;
 }
 
 cudaError_t launch_umma(const UmmaPlan &pl, const void *x, long long ldx, const uint8_t *w8,
@@ -624,10 +719,10 @@ cudaError_t launch_umma(const UmmaPlan &pl, const void *x, long long ldx, const 
     prm.chunk_cols = pl.chunk_cols;
     prm.ntok = pl.ntok;
     prm.to_partials = pl.partials ? 1 : 0;
-    prm.dx = umma_x_depth(pl);
+    prm.ds = umma_stage_depth(pl);
     prm.dc = umma_codes_depth(pl);
-    prm.da = umma_a_depth(pl);
-    if (prm.dc < 2) return cudaErrorInvalidValue;
+    prm.tcols = umma_tmem_cols(pl);
+    if (prm.dc < 2 || prm.tcols > (umma_two_per_sm(pl) ? kTmemMax / 2 : kTmemMax)) return cudaErrorInvalidValue;
     prm.timeout_ns = opt.timeout_ns;
     prm.skip_loads = opt.skip_loads;
     prm.status = status_word();

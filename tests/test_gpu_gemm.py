@@ -141,6 +141,7 @@ def test_head_sweep_sampled(bsf8_lib, M):
     (1, 64, 2560, 9, 80, 0),       # 80 tasks per slab: partials + reduce (workspace)
     (1, 96, 65536 // 8, 2, 1, 0),  # a long single split: 8 tasks of 1024 columns
     (1, 4096, 64, 192, 2, 0),      # the largest M
+    (1, 256, 544, 40, 8, 0),       # tensor-core tiles: 96-column splits, the last two empty
 ])
 def test_ragged_and_edge_shapes(bsf8_lib, G, N, K, M, S, pad):
     r = wl.rng(G * 1000 + N + K + M + S)
@@ -322,16 +323,18 @@ def test_default_kernel_fused_equals_partials_and_reduce(bsf8_lib, wk, M, S):
 def test_tensor_core_kernel_mid_rows(bsf8_lib, M, S):
     """The tensor-core kernel on the mid-row workload (G = 4 groups of W[1024, 4096]):
     sampled token rows within the oracle's tolerance, the fused call bitwise equal to its
-    two-pass form, and run-to-run bitwise reproducible.  Where a split's accumulators
-    (a run of 4 steps x the token tile) do not fit tensor memory -- one split of K = 4096
-    past 64 rows, two past 128 -- the forced kernel refuses the call (BSF8_ERR_VALUE)."""
+    two-pass form, and run-to-run bitwise reproducible.  Where two A slots (64 columns
+    each) and a split's accumulators (a run of 4 steps x the token tile, rows rounded up to
+    16) do not fit tensor memory's 512 columns -- one split of K = 4096 past 48 rows, two
+    past 96 -- the forced kernel refuses the call (BSF8_ERR_VALUE)."""
     wk = wl.MID
     w8, ex = wk.weights()
     x = wk.x(M=M)
     w8_d, ex_d, x_d = dev(w8, ex, x)
     bsf8.set_option(bsf8.OPT_GEMM_PATH, 5)
     try:
-        fits = (S == 1 and M <= 64) or (S == 2 and M <= 128) or S == 4
+        runs = (4096 // S // 128 + 3) // 4
+        fits = 2 * 64 + runs * ((M + 15) // 16 * 16) <= 512
         if not fits:
             with pytest.raises(bsf8.Bsf8Error) as e:
                 bsf8.gemm(x_d, w8_d, ex_d, split_k=S)
