@@ -127,6 +127,11 @@ inline bool ahead_one_split(int M, int N, int K, int G) {
 inline int call_auto_split(int M, int N, int K, int G) {
     if (M <= 8) return 1;
     if (ahead_one_split(M, N, K, G)) return 1;
+    // 9..24 rows elsewhere: the streaming kernel (or, on wide weights, the tensor-core kernel
+    // at one split); the streaming kernel cuts a split into tasks, and extra splits measured
+    // no faster (mid G = 4, 1024 x 4096, M = 16: 8.7 us at 1, 2, 4 and 8 splits, 19 us at
+    // the five a blocks-per-SM target gave)
+    if (M <= kUmmaMinRows) return 1;
     if (M > kUmmaMinRows && (long long)G * N < (1LL << 31)) {
         const int sms = sm_count();
         if (sms > 0) {

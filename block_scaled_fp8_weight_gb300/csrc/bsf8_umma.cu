@@ -67,9 +67,10 @@ constexpr int kMaxSplitBlocks = 1024;  // 32-column exponent blocks of a split k
 // The tensor core's fp32 accumulation into tensor memory loses accuracy with the number of
 // products accumulated in place (measured: the error grows linearly with the steps
 // accumulated, about eight times the fp32 index-order sum over 64 steps).  Each run of
-// kChunkSteps steps therefore goes to its own accumulator, and the runs are summed in
+// 2^run_shift steps therefore goes to its own accumulator, and the runs are summed in
 // fp32 on the CUDA cores in run order: the error is then that of an ordinary fp32 sum.
-constexpr int kChunkSteps = 4;  // 32 MMAs of K = 16 a run
+// Runs are 4 steps (32 MMAs of K = 16); 8 (64 MMAs, still within the error of an fp32 sum
+// by that measurement) where 4 would keep two blocks of up to 16 tokens from sharing an SM.
 constexpr int kTmemMax = 512;
 
 struct UmmaParams {
@@ -81,6 +82,7 @@ struct UmmaParams {
     int M, N, K, G, S, chunk_cols, ntok;
     int to_partials;  // 1: store fp32 partials P[s] (even with one split), 0: store y
     int ds, dc;       // stage (A slot + x tile) and codes ring depths
+    int run_shift;    // a run (one accumulator) is 2^run_shift steps
     int tcols;        // tensor memory columns a block allocates (A slots, then accumulators)
     unsigned long long timeout_ns;
     int skip_loads;
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(kThreadsU, 2) umma_kernel(const __grid_constan
     const int row0 = rb * kRows;  // first weight row of the block inside group g
     const int k0 = min(p.K, split * p.chunk_cols), k1 = min(p.K, k0 + p.chunk_cols);
     const int nkb = (k1 - k0 + kKB - 1) / kKB;
-    const int nrun = (nkb + kChunkSteps - 1) / kChunkSteps;  // accumulators (runs of steps)
+    const int nrun = (nkb + (1 << p.run_shift) - 1) >> p.run_shift;  // accumulators (runs of steps)
     const int xbytes = p.ntok * 256;  // a step's x tile: two 64-column atoms
     const int kDs = p.ds, kDc = p.dc;  // ring depths of this call
     const uint32_t dbase = (uint32_t)(kDs * kACols);  // first accumulator column (A slots first)
@@ -368,11 +370,12 @@ __global__ void __launch_bounds__(kThreadsU, 2) umma_kernel(const __grid_constan
                 tc_after();
                 const uint32_t sb = smem_u32(sX + ss * xbytes);
                 const uint32_t ta = tmem + (uint32_t)(ss * kACols);
-                const uint32_t dcol = tmem + dbase + (uint32_t)((kb / kChunkSteps) * p.ntok);  // this run's accumulator
+                const uint32_t dcol = tmem + dbase + (uint32_t)((kb >> p.run_shift) * p.ntok);  // this run's accumulator
+                const bool run_start = (kb & ((1 << p.run_shift) - 1)) == 0;
 #pragma unroll
                 for (int ks = 0; ks < kKB / 16; ++ks) {  // x: atom column ks / 4, +32 bytes a K slice
                     const uint64_t bd = sw128_desc(sb + (ks >> 2) * (xbytes / 2)) + 2 * (ks & 3);
-                    umma_ts(dcol, ta + 8u * (uint32_t)ks, bd, idesc, (kb % kChunkSteps > 0 || ks > 0) ? 1u : 0u);
+                    umma_ts(dcol, ta + 8u * (uint32_t)ks, bd, idesc, (!run_start || ks > 0) ? 1u : 0u);
                 }
                 umma_commit(&empty_s[ss]);
             }
@@ -625,7 +628,7 @@ cudaError_t umma_map(const UKey &key, bool codes, CUtensorMap *out) {
 namespace {
 
 int umma_runs(const UmmaPlan &pl) {
-    return ((pl.chunk_cols + kKB - 1) / kKB + kChunkSteps - 1) / kChunkSteps;
+    return ((pl.chunk_cols + kKB - 1) / kKB + (1 << pl.run_shift) - 1) >> pl.run_shift;
 }
 
 // Tensor memory a block's A slots (kACols columns each) and its runs' accumulators (ntok
@@ -640,7 +643,14 @@ UmmaPlan plan_umma(int M, int N, int K, int G, int S, bool partials) {
     pl.chunk_cols = ((K / 32 + S - 1) / S) * 32;
     pl.ntok = std::min(kMaxTok, (M + 15) / 16 * 16);  // tokens a tile
     pl.ttiles = (M + pl.ntok - 1) / std::max(1, pl.ntok);
-    // two A slots and the split's runs of steps (ntok accumulator columns each) in tensor memory
+    // two A slots and the split's runs of steps (ntok accumulator columns each) in tensor
+    // memory; up to 16 tokens, runs of 8 steps where 4 would not fit half of it
+    pl.run_shift = 2;
+    if (pl.ntok <= 16 && umma_tmem_need(pl, 2) > kTmemMax / 2) {
+        UmmaPlan p8 = pl;
+        p8.run_shift = 3;
+        if (umma_tmem_need(p8, 2) <= kTmemMax / 2) pl.run_shift = 3;
+    }
     pl.tmem_ok = umma_tmem_need(pl, 2) <= kTmemMax;
     pl.row_blocks = (N + kRows - 1) / kRows;
     pl.grid_x = pl.row_blocks * S;
@@ -720,6 +730,7 @@ cudaError_t launch_umma(const UmmaPlan &pl, const void *x, long long ldx, const 
     prm.ntok = pl.ntok;
     prm.to_partials = pl.partials ? 1 : 0;
     prm.ds = umma_stage_depth(pl);
+    prm.run_shift = pl.run_shift;
     prm.dc = umma_codes_depth(pl);
     prm.tcols = umma_tmem_cols(pl);
     if (prm.dc < 2 || prm.tcols > (umma_two_per_sm(pl) ? kTmemMax / 2 : kTmemMax)) return cudaErrorInvalidValue;
