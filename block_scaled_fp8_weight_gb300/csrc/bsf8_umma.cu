@@ -70,7 +70,8 @@ constexpr int kMaxSplitBlocks = 1024;  // 32-column exponent blocks of a split k
 // 2^run_shift steps therefore goes to its own accumulator, and the runs are summed in
 // fp32 on the CUDA cores in run order: the error is then that of an ordinary fp32 sum.
 // Runs are 4 steps (32 MMAs of K = 16); 8 (64 MMAs, still within the error of an fp32 sum
-// by that measurement) where 4 would keep two blocks of up to 16 tokens from sharing an SM.
+// by that measurement) where 4 would not fit tensor memory, or would keep two blocks of up
+// to 16 tokens from sharing an SM.
 constexpr int kTmemMax = 512;
 
 struct UmmaParams {
@@ -92,6 +93,12 @@ struct UmmaParams {
 __device__ __forceinline__ uint64_t evict_first_policy_u() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint64_t evict_normal_policy_u() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
     return pol;
 }
 
@@ -297,7 +304,9 @@ __global__ void __launch_bounds__(kThreadsU, 2) umma_kernel(const __grid_constan
     if (warp == 0) {
         // ------------------------------------------------------------ codes
         if (lane == 0) {  // static, streamed ahead from the start
-            const uint64_t pol = evict_first_policy_u();
+            // read once a call with one token tile (evict first); with more, every tile's blocks
+            // read the same codes, so they stay (M = 1024: 79 MB from DRAM for 50 MB of operands)
+            const uint64_t pol = gridDim.z > 1 ? evict_normal_policy_u() : evict_first_policy_u();
             int n = 0;
             bool bad = false;
             // ring slot and its use's parity by counters (a division by the run-time depth costs
@@ -644,12 +653,14 @@ UmmaPlan plan_umma(int M, int N, int K, int G, int S, bool partials) {
     pl.ntok = std::min(kMaxTok, (M + 15) / 16 * 16);  // tokens a tile
     pl.ttiles = (M + pl.ntok - 1) / std::max(1, pl.ntok);
     // two A slots and the split's runs of steps (ntok accumulator columns each) in tensor
-    // memory; up to 16 tokens, runs of 8 steps where 4 would not fit half of it
+    // memory (half of it up to 16 tokens, so that two blocks share an SM); runs of 8 steps
+    // where 4 would not fit (fewer splits: half the partials at 1024 rows)
     pl.run_shift = 2;
-    if (pl.ntok <= 16 && umma_tmem_need(pl, 2) > kTmemMax / 2) {
+    const int cap = pl.ntok <= 16 ? kTmemMax / 2 : kTmemMax;
+    if (umma_tmem_need(pl, 2) > cap) {
         UmmaPlan p8 = pl;
         p8.run_shift = 3;
-        if (umma_tmem_need(p8, 2) <= kTmemMax / 2) pl.run_shift = 3;
+        if (umma_tmem_need(p8, 2) <= cap || umma_tmem_need(pl, 2) > kTmemMax) pl.run_shift = 3;
     }
     pl.tmem_ok = umma_tmem_need(pl, 2) <= kTmemMax;
     pl.row_blocks = (N + kRows - 1) / kRows;

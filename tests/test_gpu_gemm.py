@@ -324,17 +324,17 @@ def test_tensor_core_kernel_mid_rows(bsf8_lib, M, S):
     """The tensor-core kernel on the mid-row workload (G = 4 groups of W[1024, 4096]):
     sampled token rows within the oracle's tolerance, the fused call bitwise equal to its
     two-pass form, and run-to-run bitwise reproducible.  Where two A slots (64 columns
-    each) and a split's accumulators (a run of 4 steps x the token tile, rows rounded up to
-    16) do not fit tensor memory's 512 columns -- one split of K = 4096 past 48 rows, two
-    past 96 -- the forced kernel refuses the call (BSF8_ERR_VALUE)."""
+    each) and a split's accumulators (one a run of 4 steps, or of 8 where 4 do not fit, x
+    the token tile, rows rounded up to 16) do not fit tensor memory's 512 columns -- one
+    split of K = 4096 past 96 rows -- the forced kernel refuses the call (BSF8_ERR_VALUE)."""
     wk = wl.MID
     w8, ex = wk.weights()
     x = wk.x(M=M)
     w8_d, ex_d, x_d = dev(w8, ex, x)
     bsf8.set_option(bsf8.OPT_GEMM_PATH, 5)
     try:
-        runs = (4096 // S // 128 + 3) // 4
-        fits = 2 * 64 + runs * ((M + 15) // 16 * 16) <= 512
+        steps, ntok = 4096 // S // 128, (M + 15) // 16 * 16
+        fits = any(2 * 64 + (steps + run - 1) // run * ntok <= 512 for run in (4, 8))
         if not fits:
             with pytest.raises(bsf8.Bsf8Error) as e:
                 bsf8.gemm(x_d, w8_d, ex_d, split_k=S)
