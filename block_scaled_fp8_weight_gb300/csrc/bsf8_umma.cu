@@ -54,7 +54,7 @@ constexpr int kACols = kKB / 2;      // TMEM columns of a step's A (two bf16 a 3
 constexpr int kDsMax = 4, kDcMax = 8;  // ring depths, set per call
 // Dynamic shared memory a block: the x tiles of the stage ring (a stage = one step's A slot
 // in tensor memory and its x tile) and the codes ring, sized per call (x tiles grow with the
-// tokens): 2 .. 4 stages, as many as tensor memory holds A slots for and 64 KB of x tiles
+// tokens): 2 .. 4 stages, as many as tensor memory holds A slots for and 144 KB of x tiles
 // unless two need more; the codes ring the rest, 2 .. 8 steps.
 constexpr int kSmemU = 208 * 1024;
 constexpr int kRebuildWarps = 8;     // two a TMEM lane quarter, 64 columns of a step each
@@ -69,9 +69,9 @@ constexpr int kMaxSplitBlocks = 1024;  // 32-column exponent blocks of a split k
 // accumulated, about eight times the fp32 index-order sum over 64 steps).  Each run of
 // 2^run_shift steps therefore goes to its own accumulator, and the runs are summed in
 // fp32 on the CUDA cores in run order: the error is then that of an ordinary fp32 sum.
-// Runs are 4 steps (32 MMAs of K = 16); 8 (64 MMAs, still within the error of an fp32 sum
-// by that measurement) where 4 would not fit tensor memory, or would keep two blocks of up
-// to 16 tokens from sharing an SM.
+// Runs are 8 steps (64 MMAs of K = 16, still within the error of an fp32 sum by that
+// measurement) past 16 tokens; up to 16 tokens 4 (32 MMAs), unless 4 would keep two blocks
+// from sharing an SM or not fit tensor memory at all.
 constexpr int kTmemMax = 512;
 
 struct UmmaParams {
@@ -653,9 +653,11 @@ UmmaPlan plan_umma(int M, int N, int K, int G, int S, bool partials) {
     pl.ntok = std::min(kMaxTok, (M + 15) / 16 * 16);  // tokens a tile
     pl.ttiles = (M + pl.ntok - 1) / std::max(1, pl.ntok);
     // two A slots and the split's runs of steps (ntok accumulator columns each) in tensor
-    // memory (half of it up to 16 tokens, so that two blocks share an SM); runs of 8 steps
-    // where 4 would not fit (fewer splits: half the partials at 1024 rows)
-    pl.run_shift = 2;
+    // memory (half of it up to 16 tokens, so that two blocks share an SM).  Past 16 tokens,
+    // runs of 8 steps: the room they leave takes more stages (mid rows at 128 / 192 tokens:
+    // 14.8 / 16.4 -> 14.0 / 15.7 us), and at large M fewer splits (half the partials at 1024
+    // rows); up to 16 tokens, runs of 8 only where 4 would not fit.
+    pl.run_shift = pl.ntok > 16 ? 3 : 2;
     const int cap = pl.ntok <= 16 ? kTmemMax / 2 : kTmemMax;
     if (umma_tmem_need(pl, 2) > cap) {
         UmmaPlan p8 = pl;
@@ -694,12 +696,12 @@ int umma_auto_split(int M, int N, int K, int G, int sms) {
 int umma_smem_budget(const UmmaPlan &pl) { return umma_two_per_sm(pl) ? 106 * 1024 : kSmemU; }
 
 // Stages (a step's A slot in tensor memory and its x tile): 2 .. 4, as many as tensor memory
-// leaves beside the accumulators and as 64 KB of x tiles hold (8 KB with two blocks an SM),
-// at least two.
+// leaves beside the accumulators and as 144 KB of x tiles hold (8 KB with two blocks an SM;
+// the codes ring keeps 3 .. 8 slots beside them), at least two.
 int umma_stage_depth(const UmmaPlan &pl) {
     const bool two = umma_two_per_sm(pl);
     const int cap = two ? kTmemMax / 2 : kTmemMax;
-    const int xcap = std::max(2, (two ? 8 * 1024 : 64 * 1024) / (pl.ntok * 256));
+    const int xcap = std::max(2, (two ? 8 * 1024 : 144 * 1024) / (pl.ntok * 256));
     int ds = 2;
     while (ds < kDsMax && ds < xcap && umma_tmem_need(pl, ds + 1) <= cap) ++ds;
     return ds;

@@ -324,9 +324,10 @@ def test_tensor_core_kernel_mid_rows(bsf8_lib, M, S):
     """The tensor-core kernel on the mid-row workload (G = 4 groups of W[1024, 4096]):
     sampled token rows within the oracle's tolerance, the fused call bitwise equal to its
     two-pass form, and run-to-run bitwise reproducible.  Where two A slots (64 columns
-    each) and a split's accumulators (one a run of 4 steps, or of 8 where 4 do not fit, x
-    the token tile, rows rounded up to 16) do not fit tensor memory's 512 columns -- one
-    split of K = 4096 past 96 rows -- the forced kernel refuses the call (BSF8_ERR_VALUE)."""
+    each) and a split's accumulators (one a run of 8 steps past 16 tokens, of 4 or 8 up to
+    16, x the token tile, rows rounded up to 16) do not fit tensor memory's 512 columns --
+    one split of K = 4096 past 96 rows -- the forced kernel refuses the call
+    (BSF8_ERR_VALUE)."""
     wk = wl.MID
     w8, ex = wk.weights()
     x = wk.x(M=M)
