@@ -73,6 +73,7 @@ constexpr int kMaxSplitBlocks = 1024;  // 32-column exponent blocks of a split k
 // measurement) past 16 tokens; up to 16 tokens 4 (32 MMAs), unless 4 would keep two blocks
 // from sharing an SM or not fit tensor memory at all.
 constexpr int kTmemMax = 512;
+constexpr int kMaxFold = 8;  // splits a cluster sums in shared memory (the portable cluster size)
 
 struct UmmaParams {
     CUtensorMap cmap;  // w8 as [G*N rows][K columns] bytes, box 128 x 128, 128-byte swizzle
@@ -84,6 +85,8 @@ struct UmmaParams {
     int to_partials;  // 1: store fp32 partials P[s] (even with one split), 0: store y
     int ds, dc;       // stage (A slot + x tile) and codes ring depths
     int run_shift;    // a run (one accumulator) is 2^run_shift steps
+    int cluster_fold; // 1: the S split blocks of a row block form a cluster and sum their
+                      // splits through distributed shared memory into y (no partials)
     int tcols;        // tensor memory columns a block allocates (A slots, then accumulators)
     unsigned long long timeout_ns;
     int skip_loads;
@@ -233,6 +236,27 @@ __device__ __forceinline__ void rebuild_block_u(const uint4 &c0, const uint4 &c1
         a[2 * i] = lo;
         a[2 * i + 1] = hi;
     }
+}
+
+// Shared-memory address `a` of this CTA mapped into cluster CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_u(uint32_t a, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ld_cluster_u32_u(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float4 ld_cluster_v4_u(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
 }
 
 // Barrier of the rebuild warps only (named barrier 1).
@@ -521,7 +545,11 @@ __global__ void __launch_bounds__(kThreadsU, 2) umma_kernel(const __grid_constan
             for (int j = 0; j < 16; ++j) acc[j] = poison ? __uint_as_float(0x7FC00000u) : acc[j];
             const size_t o0 = ((size_t)(tok0 + c0) * p.G + g) * p.N + n;
             const int mj = min(16, mrows - c0);
-            if (p.to_partials) {
+            if (p.cluster_fold) {  // the split's sums, token-major, in the freed stage memory
+                float *f = reinterpret_cast<float *>(base) + c0 * kRows + row;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) f[j * kRows] = acc[j];
+            } else if (p.to_partials) {
                 float *dst = p.partials + (size_t)split * p.M * mstride + o0;
                 if (mj == 16) {
 #pragma unroll
@@ -543,7 +571,10 @@ __global__ void __launch_bounds__(kThreadsU, 2) umma_kernel(const __grid_constan
                 }
             }
         }
-        if (!dok && lane == 0) report_timeout(p.status);
+        if (!dok && lane == 0) {
+            *(volatile int *)&s_err = 1;
+            report_timeout(p.status);
+        }
     }
 
     tc_before();
@@ -553,6 +584,57 @@ __global__ void __launch_bounds__(kThreadsU, 2) umma_kernel(const __grid_constan
         (void)mbar_wait_bounded(&d_full, 0u, p.timeout_ns);
         tc_after();
         tmem_dealloc_u(tmem, (uint32_t)p.tcols);
+    }
+    if (p.cluster_fold) {
+        // The cluster holds the S splits of this row block (rank = split).  Every block has
+        // put its split's sums in its shared memory; block `split` adds its slice of the
+        // tokens over the ranks in split order -- ((P0 + P1) + P2) + ..., fp32, as the reduce
+        // kernel does -- and stores y.  No block stores if any of them gave up a wait.
+        __shared__ int s_fold_ok;
+        cluster_sync();
+        if (threadIdx.x == 0) {
+            uint32_t bad = 0;
+            for (int r = 0; r < p.S; ++r) bad |= ld_cluster_u32_u(mapa_u(smem_u32(&s_err), (uint32_t)r));
+            s_fold_ok = bad == 0;
+        }
+        __syncthreads();
+        if (s_fold_ok) {
+            const int mrows = min(p.ntok, p.M - tok0);
+            const int ts = (mrows + p.S - 1) / p.S;
+            const int m_lo = min(mrows, split * ts), m_hi = min(mrows, m_lo + ts);
+            const int q4 = min(kRows, p.N - row0) / 4;  // 4-row groups that exist
+            const uint32_t fbase = smem_u32(base);
+            for (int i = threadIdx.x; i < (m_hi - m_lo) * q4; i += blockDim.x) {
+                const int ml = m_lo + i / q4, rr = 4 * (i % q4);
+                const uint32_t a = fbase + (uint32_t)((ml * kRows + rr) * 4);
+                float4 pv[kMaxFold];
+#pragma unroll
+                for (int r = 0; r < kMaxFold; ++r)
+                    if (r < p.S) pv[r] = ld_cluster_v4_u(mapa_u(a, (uint32_t)r));
+                float4 v = pv[0];
+#pragma unroll
+                for (int r = 1; r < kMaxFold; ++r)
+                    if (r < p.S) {
+                        v.x += pv[r].x;
+                        v.y += pv[r].y;
+                        v.z += pv[r].z;
+                        v.w += pv[r].w;
+                    }
+                uint16_t *dst = p.y + ((size_t)(tok0 + ml) * p.G + g) * p.N + row0 + rr;
+                const uint16_t b0 = f32_to_bf16_rn(v.x), b1 = f32_to_bf16_rn(v.y), b2 = f32_to_bf16_rn(v.z),
+                               b3 = f32_to_bf16_rn(v.w);
+                if ((reinterpret_cast<uintptr_t>(dst) & 7u) == 0) {  // N, row0, rr: multiples of 4
+                    *reinterpret_cast<uint2 *>(dst) =
+                        make_uint2((uint32_t)b0 | ((uint32_t)b1 << 16), (uint32_t)b2 | ((uint32_t)b3 << 16));
+                } else {
+                    dst[0] = b0;
+                    dst[1] = b1;
+                    dst[2] = b2;
+                    dst[3] = b3;
+                }
+            }
+        }
+        cluster_sync();  // no block leaves while another still reads its shared memory
     }
 }
 
@@ -644,6 +726,17 @@ int umma_runs(const UmmaPlan &pl) {
 // columns each) take.
 int umma_tmem_need(const UmmaPlan &pl, int da) { return da * kACols + umma_runs(pl) * pl.ntok; }
 
+// SMs of the current device (0 without one), looked up once per device.
+int sm_count_u() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int c = __atomic_load_n(&cached[dev], __ATOMIC_ACQUIRE);
+    if (c == 0 && cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && c > 0)
+        __atomic_store_n(&cached[dev], c, __ATOMIC_RELEASE);
+    return c > 0 ? c : 0;
+}
+
 }  // namespace
 
 UmmaPlan plan_umma(int M, int N, int K, int G, int S, bool partials) {
@@ -667,7 +760,15 @@ UmmaPlan plan_umma(int M, int N, int K, int G, int S, bool partials) {
     pl.tmem_ok = umma_tmem_need(pl, 2) <= kTmemMax;
     pl.row_blocks = (N + kRows - 1) / kRows;
     pl.grid_x = pl.row_blocks * S;
-    pl.partials = partials || S > 1;
+    // 2..8 splits of a call that wants y, all blocks in one wave: the split blocks of a row
+    // block form a cluster and sum in shared memory (mid rows, G = 4, 1024 x 4096, S = 4:
+    // 12.6 MB of partials and the reduce pass saved at 192 tokens, 15.5 -> 14.6 us).  Grids of
+    // several waves keep the partials (each wave's blocks would wait for their cluster's
+    // fold: head-like weight at 128 tokens 85.7 -> 89.0 us); not with two blocks an SM.
+    const long long blocks = (long long)pl.row_blocks * S * G * pl.ttiles;
+    pl.fold = !partials && S >= 2 && S <= kMaxFold && blocks <= sm_count_u() &&
+              !(pl.ntok <= 16 && umma_tmem_need(pl, 2) <= kTmemMax / 2);
+    pl.partials = partials || (S > 1 && !pl.fold);
     pl.ok = M >= 1 && M <= kMaxRowsU && (long long)G * N < (1LL << 31) && K < (1 << 30) && pl.tmem_ok &&
             pl.chunk_cols / 32 <= kMaxSplitBlocks;
     return pl;
@@ -742,6 +843,7 @@ cudaError_t launch_umma(const UmmaPlan &pl, const void *x, long long ldx, const 
     prm.chunk_cols = pl.chunk_cols;
     prm.ntok = pl.ntok;
     prm.to_partials = pl.partials ? 1 : 0;
+    prm.cluster_fold = pl.fold ? 1 : 0;
     prm.ds = umma_stage_depth(pl);
     prm.run_shift = pl.run_shift;
     prm.dc = umma_codes_depth(pl);
@@ -770,11 +872,18 @@ cudaError_t launch_umma(const UmmaPlan &pl, const void *x, long long ldx, const 
     cfg.blockDim = dim3(kThreadsU, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attrs[1];
+    cudaLaunchAttribute attrs[2];
     int na = 0;
     if (opt.pdl) {
         attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attrs[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    if (pl.fold) {  // grid x = row block * S + split: a cluster is one row block's splits
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = (unsigned)pl.S;
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = 1;
         ++na;
     }
     cfg.attrs = attrs;
