@@ -4,12 +4,13 @@
 // Some callers cannot hand the library a workspace: a serving engine that reserves all of
 // the GPU's memory up front for its own arena (weights, KV cache) has no allocation left to
 // give, and a plugin or callback running inside such an engine may not call the allocator
-// at all.  This entry point needs nothing from them but the inputs and the output: it runs
-// the two passes of the split-K GEMM -- bsf8_gemm_partials, then bsf8_splitk_reduce -- with
-// the partials in a buffer compiled into the library, a file-scope device array that every
-// GPU which loads the library holds until the process exits.  Those two passes run the
-// kernel bsf8_gemm runs for the same sizes and split count and sum the splits in the same
-// fixed order, so the result is bsf8_gemm's, bit for bit.
+// at all.  This entry point needs nothing from them but the inputs and the output.  Where
+// bsf8_gemm needs no workspace for the call (its kernels sum the splits on chip) it is
+// bsf8_gemm.  Otherwise it runs the two passes of the split-K GEMM -- bsf8_gemm_partials,
+// then bsf8_splitk_reduce -- with the partials in a buffer compiled into the library, a
+// file-scope device array that every GPU which loads the library holds until the process
+// exits.  Those two passes run the kernel bsf8_gemm runs for the same sizes and split count
+// and sum the splits in the same fixed order, so the result is bsf8_gemm's, bit for bit.
 #include "bsf8.h"
 
 #include <cuda_runtime.h>
@@ -67,6 +68,9 @@ extern "C" int bsf8_gemm_static_scratch(const void *x, const uint8_t *w8, const 
     // the split count bsf8_gemm uses
     const int S = split_k == 0 ? bsf8_gemm_auto_split(M, N, K, G) : split_k;
     if (S < 1) return -S;
+    // no workspace needed: bsf8_gemm itself
+    if (bsf8_gemm_workspace_bytes(M, N, K, G, S) == 0)
+        return bsf8_gemm(x, w8, exp, y, M, N, K, G, S, ldx, nullptr, 0, stream);
     // The partials P[S][M][G][N] must fit the compiled-in buffer.
     if ((size_t)S * M * G * N > kScratchFloats) return BSF8_ERR_WORKSPACE;
 

@@ -231,13 +231,16 @@ int bsf8_gemm_rows(const void *x, const uint8_t *w8, const uint8_t *exp, void *y
  * The pages have no counterpart for this entry point; it serves callers that cannot
  * allocate device memory for a workspace -- e.g. a serving engine that has reserved all of
  * the GPU's memory for its own arena, or a plugin running inside one that may not call
- * the allocator.  It runs bsf8_gemm_partials and then bsf8_splitk_reduce with the split
- * count bsf8_gemm uses (split_k 0: bsf8_gemm_auto_split), so its result equals bsf8_gemm's
- * bit for bit, with the partials held in a buffer compiled into the library:
+ * the allocator.  With the split count bsf8_gemm uses (split_k 0: bsf8_gemm_auto_split):
+ * where bsf8_gemm needs no workspace for the call (bsf8_gemm_workspace_bytes = 0: most
+ * shapes, whose kernels sum their splits on chip) it is bsf8_gemm; otherwise it runs
+ * bsf8_gemm_partials and then bsf8_splitk_reduce -- the same kernel and the same fixed-order
+ * sum -- so its result equals bsf8_gemm's bit for bit, with the partials held in a buffer
+ * compiled into the library:
  *   - the buffer is BSF8_STATIC_SCRATCH_BYTES (8 MiB) of device memory that every GPU
  *     which loads the library holds until the process exits;
- *   - a call whose partials S*M*G*N*4 bytes (S = the split count used) exceed it returns
- *     BSF8_ERR_WORKSPACE without launching anything;
+ *   - a call that needs partials whose S*M*G*N*4 bytes (S = the split count used) exceed
+ *     it returns BSF8_ERR_WORKSPACE without launching anything;
  *   - nothing is allocated and nothing needs clearing: every split writes all of its
  *     partials before the reduce reads them;
  *   - every call on a device shares that one buffer, so calls that can overlap on the GPU
