@@ -118,8 +118,17 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     return v;
 }
 
-__device__ __forceinline__ void sts64(uint32_t addr, uint32_t a, uint32_t b) {
-    asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// 1-D bulk copy of `bytes` (a multiple of 16) from global src to shared address dst (both
+// 16-byte aligned), completing that many bytes of transaction count on `bar`.
+__device__ __forceinline__ void bulk_g2s_addr(uint32_t dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
 }
 
 // Four 8 x 16-byte matrices of shared memory (row addresses from lanes 8i .. 8i + 7 for
@@ -135,12 +144,6 @@ __device__ __forceinline__ uint4 ldsm_x4(uint32_t addr) {
 __device__ __forceinline__ uint2 ldg64(const void *p) {
     uint2 v;
     asm volatile("ld.global.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-    return v;
-}
-
-__device__ __forceinline__ uint4 ldg128(const void *p) {
-    uint4 v;
-    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
     return v;
 }
 
@@ -227,33 +230,53 @@ __device__ __forceinline__ int row_scale(uint32_t mx, bool &ok) {
 // Converts the split's x (token rows 0 .. M-1, columns [k0, k0 + 32 cb) of group g) into
 // f16 x' at xh (rows pitch bytes apart; inside each 32-column block of 64 bytes, the 16
 // bytes at 16q hold columns 4q .. 4q + 3 and 16 + 4q .. 16 + 4q + 3, the MMA B operand of
-// lane quad q), sets s_sx[m] = s_m, and sets bit blk of s_bad for
-// every 32-column block whose x' is not exact for some row.  Run by all consumer threads
-// (tid 0 .. 255) between consumer barriers; the rows' loads are issued together.
-__device__ void convert_x(const WideParams &p, uint32_t xh, int g, int k0, int cb, int tid,
-                          uint32_t *s_max, uint32_t *s_bad, int *s_sx) {
+// lane quad q), sets s_sx[m] = s_m, and sets bit blk of s_bad for every 32-column block
+// whose x' is not exact for some row.  Run by all consumer threads (tid 0 .. 255) between
+// consumer barriers.  The rows first come into the same place as raw bf16 (one bulk copy
+// a row on `xbar`, phase xphase; a bf16 row takes the bytes its f16 row will), so both
+// passes read shared memory: loads from L2 in a loop took 2 to 5 us a conversion.  The
+// second pass converts each 64-byte block in place, one thread a block.  Returns false when
+// the copies did not land within the bound (nothing is converted then).
+__device__ bool convert_x(const WideParams &p, uint32_t xh, int g, int k0, int cb, int tid,
+                          uint32_t *s_max, uint32_t *s_bad, int *s_sx, uint64_t *xbar, uint32_t xphase,
+                          int *s_xfail) {
     const int nvec = 4 * cb;  // 16-byte vectors of a row
     const int lane = tid & 31;
     if (tid < kWWarps) s_max[tid] = 0;
     if (tid < kWBadWords) s_bad[tid] = 0;
+    if (tid == 0) *s_xfail = 0;
+    // the previous x' was read by the generic proxy; the copies write through the async one
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     consumers_sync();
-    // pass 1: each row's largest magnitude (bf16 magnitudes order as integers); the rows'
-    // loads are issued together
-    const uint16_t *src0 = p.x + (size_t)g * p.K + k0;
+    if (tid == 0) {
+        mbar_arrive_expect_tx(xbar, (uint32_t)(p.M * 64 * cb));
+        const uint16_t *src0 = p.x + (size_t)g * p.K + k0;
+        for (int m = 0; m < p.M; ++m)
+            bulk_g2s_addr(xh + (uint32_t)(m * p.pitch), src0 + (size_t)m * p.ldx, (uint32_t)(64 * cb), xbar);
+    }
+    // every consumer thread sees the copies complete (or the bound run out), and the block
+    // agrees on the outcome
+    if (!mbar_wait_bounded(xbar, xphase, p.timeout_ns)) atomicOr(s_xfail, 1);
+    consumers_sync();
+    const bool landed = *(volatile int *)s_xfail == 0;
+    if (!landed) {  // the copies must land before this memory is used again or freed (bounded)
+        (void)mbar_wait_bounded(xbar, xphase, p.timeout_ns);
+        consumers_sync();
+        return false;
+    }
+    // pass 1: each row's largest magnitude (bf16 magnitudes order as integers)
     uint32_t mx[kWWarps];
 #pragma unroll
     for (int m = 0; m < kWWarps; ++m) mx[m] = 0;
     for (int v = tid; v < nvec; v += kWWarps * 32) {
-        uint4 u[kWWarps];
 #pragma unroll
-        for (int m = 0; m < kWWarps; ++m)
-            if (m < p.M) u[m] = ldg128(src0 + (size_t)m * p.ldx + 8 * v);
-#pragma unroll
-        for (int m = 0; m < kWWarps; ++m)
-            if (m < p.M)
-                mx[m] = max_u16x2(mx[m], max_u16x2(max_u16x2(u[m].x & 0x7FFF7FFFu, u[m].y & 0x7FFF7FFFu),
-                                                   max_u16x2(u[m].z & 0x7FFF7FFFu, u[m].w & 0x7FFF7FFFu)));
-    }
+            for (int m = 0; m < kWWarps; ++m)
+                if (m < p.M) {
+                    const uint4 u = lds128(xh + (uint32_t)(m * p.pitch + 16 * v));
+                    mx[m] = max_u16x2(mx[m], max_u16x2(max_u16x2(u.x & 0x7FFF7FFFu, u.y & 0x7FFF7FFFu),
+                                                       max_u16x2(u.z & 0x7FFF7FFFu, u.w & 0x7FFF7FFFu)));
+                }
+        }
 #pragma unroll
     for (int m = 0; m < kWWarps; ++m) {
         if (m >= p.M) break;
@@ -263,51 +286,44 @@ __device__ void convert_x(const WideParams &p, uint32_t xh, int g, int k0, int c
         if (lane == 0 && v) atomicMax(&s_max[m], v);
     }
     consumers_sync();
-    // pass 2: convert; a vector is exact when each non-zero magnitude is >= thr
-    float sc[kWWarps];
-    uint32_t thr1[kWWarps];
-    bool rok[kWWarps];
-#pragma unroll
-    for (int m = 0; m < kWWarps; ++m) {
-        const int s = m < p.M ? row_scale(s_max[m], rok[m]) : 0;
-        if (m >= p.M) rok[m] = true;
-        sc[m] = exp2_int(-s);
-        thr1[m] = ((uint32_t)(s + 110) << 7) - 1u;  // |x| >= 2^(s-17); s >= -100
-        if (tid == m) s_sx[m] = s;
+    // pass 2: convert each row's 64-byte blocks in place, one thread a (row, block); a block
+    // is exact when each non-zero magnitude of every row is >= 2^(s_m - 17)
+    if (tid < p.M) {  // a row whose s_m is out of range gets 0 here and every block marked below
+        bool ok;
+        s_sx[tid] = row_scale(s_max[tid], ok);
     }
-    for (int v = tid; v < nvec; v += kWWarps * 32) {
-        uint4 u[kWWarps];
+    for (int u = tid; u < p.M * cb; u += kWWarps * 32) {
+        const int m = u / cb, blk = u - m * cb;
+        bool rok;
+        const int sm = row_scale(s_max[m], rok);
+        const float sc = exp2_int(-sm);
+        const uint32_t thr1 = ((uint32_t)(sm + 110) << 7) - 1u;  // |x| >= 2^(s-17); s >= -100
+        const uint32_t base = xh + (uint32_t)(m * p.pitch + 64 * blk);
+        uint32_t w[16];  // bf16 pairs: columns (2i, 2i + 1) of the block
 #pragma unroll
-        for (int m = 0; m < kWWarps; ++m)
-            if (m < p.M) u[m] = ldg128(src0 + (size_t)m * p.ldx + 8 * v);
-        bool bad = false;
-#pragma unroll
-        for (int m = 0; m < kWWarps; ++m) {
-            if (m >= p.M) break;
-            const uint32_t wv[4] = {u[m].x, u[m].y, u[m].z, u[m].w};
-            uint32_t o[4];
-            uint32_t mn = 0xFFFFFFFFu;  // per half: smallest magnitude minus one (zero -> 0xFFFF)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint32_t w = wv[k];
-                mn = min_u16x2(mn, ((w | 0x80008000u) - 0x00010001u) ^ 0x80008000u);
-                o[k] = pack_f16x2(__uint_as_float(w << 16) * sc[m], __uint_as_float(w & 0xFFFF0000u) * sc[m]);
-            }
-            // operand order inside a 32-column block: thread q's columns 4q .. 4q + 3 of
-            // its first and of its second 16 columns side by side (16 bytes)
-            const uint32_t base = xh + (uint32_t)(m * p.pitch + 64 * (v >> 2));
-            const int j = (v >> 1) & 1, q0 = 2 * (v & 1);
-            sts64(base + (uint32_t)(16 * q0 + 8 * j), o[0], o[1]);
-            sts64(base + (uint32_t)(16 * (q0 + 1) + 8 * j), o[2], o[3]);
-            bad = bad || !rok[m] || min(mn & 0xFFFFu, mn >> 16) < thr1[m];
+        for (int j = 0; j < 4; ++j) {
+            const uint4 v = lds128(base + 16 * j);
+            w[4 * j] = v.x;
+            w[4 * j + 1] = v.y;
+            w[4 * j + 2] = v.z;
+            w[4 * j + 3] = v.w;
         }
-        if (bad) {
-            const int blk = v >> 2;
-            atomicOr(&s_bad[blk >> 5], 1u << (blk & 31));
+        uint32_t o[16];
+        uint32_t mn = 0xFFFFFFFFu;  // per half: smallest magnitude minus one (zero -> 0xFFFF)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            mn = min_u16x2(mn, ((w[i] | 0x80008000u) - 0x00010001u) ^ 0x80008000u);
+            o[i] = pack_f16x2(__uint_as_float(w[i] << 16) * sc, __uint_as_float(w[i] & 0xFFFF0000u) * sc);
         }
+        // the 16 bytes at 16q: columns 4q .. 4q + 3 (pairs 2q, 2q + 1) and 16 + 4q ..
+        // 16 + 4q + 3 (pairs 8 + 2q, 9 + 2q)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) sts128(base + 16 * q, o[2 * q], o[2 * q + 1], o[8 + 2 * q], o[9 + 2 * q]);
+        if (!rok || min(mn & 0xFFFFu, mn >> 16) < thr1) atomicOr(&s_bad[blk >> 5], 1u << (blk & 31));
     }
     if (tid >= p.M && tid < kWWarps) s_sx[tid] = 0;
     consumers_sync();
+    return true;
 }
 
 // Step word of the warp's blocks blk0, blk0 + 1 (blk0 even): bit b = block blk0 + b lies
@@ -368,7 +384,8 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
     uint8_t *const ring = dyn_smem + ((1024u - (smem_u32(dyn_smem) & 1023u)) & 1023u);
     const int D = p.depth;
     uint8_t *const xh = ring + D * kWBox;  // f16 x of token rows 0 .. M-1
-    __shared__ __align__(8) uint64_t full[kWDepthMax], empty[kWDepthMax];
+    __shared__ __align__(8) uint64_t full[kWDepthMax], empty[kWDepthMax], xbar;
+    __shared__ int s_xfail;
     __shared__ uint32_t s_bad[kWBadWords];  // blocks of the split with an inexact x'
     __shared__ uint32_t s_max[kWWarps];     // per token row: largest magnitude bits
     __shared__ int s_sx[kWWarps];           // per token row: s_m
@@ -388,6 +405,7 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kWWarps);
         }
+        mbar_init(&xbar, 1);
         s_err = 0;
         for (int i = 0; i < kWRedSlots; ++i) red_cnt[i] = red_done[i] = 0;
         fence_mbar_init();
@@ -471,7 +489,7 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
     pdl_wait();
 
     int cur_gs = -1, slot = 0;
-    uint32_t phase = 0;
+    uint32_t phase = 0, xphase = 0;  // ring and x-copy barrier phases
     bool bad = false;
     const bool xr = r < p.M;  // this thread's B-operand token row is held
 
@@ -485,7 +503,11 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
         const int gs = s * p.G + g;
         if (gs != cur_gs) {
             consumers_sync();  // every consumer warp is done with the previous x'
-            convert_x(p, xh_s, g, k0, cb, tid, s_max, s_bad, s_sx);
+            if (!convert_x(p, xh_s, g, k0, cb, tid, s_max, s_bad, s_sx, &xbar, xphase, &s_xfail)) {
+                bad = true;
+                if (lane == 0) *(volatile int *)&s_err = 1;
+            }
+            xphase ^= 1u;
             cur_gs = gs;
         }
         const uint32_t C0 = step_code(E0, 16 * lane + 2 * w, cb, s_bad);
