@@ -318,6 +318,46 @@ def test_default_kernel_fused_equals_partials_and_reduce(bsf8_lib, wk, M, S):
     assert bsf8.gemm_kernel(M, wk.N, wk.K, wk.G, S) == bsf8.gemm_kernel(M, wk.N, wk.K, wk.G, S_used)
 
 
+@pytest.mark.parametrize("G,N,K,M,S", [
+    (2, 160, 544, 40, 4),     # a 32-row last row block, a 32-column tail step, 8 padded tokens
+    (1, 8192, 1024, 200, 2),  # two token tiles (192 + 8), 256 blocks: more than one wave, partials
+    (3, 256, 2048, 192, 8),   # eight splits summed in one cluster
+])
+def test_tensor_core_split_fold_edges(bsf8_lib, G, N, K, M, S):
+    """The tensor-core kernel's in-cluster split sum (one-wave calls of 2..8 splits) on
+    ragged shapes, and the partials it leaves to the reduce pass otherwise: within the
+    oracle's tolerance and bitwise equal to bsf8_gemm_partials + bsf8_splitk_reduce."""
+    r = wl.rng(G * 7919 + N + K + M + S)
+    w8 = wl.codes(r, (G, N, K))
+    ex = wl.exponents(r, (G, N // 32, K // 32), 115, 127)
+    x = wl.activations(r, M, G * K)
+    w8_d, ex_d, x_d = dev(w8, ex, x)
+    assert bsf8.gemm_kernel(M, N, K, G, S) == 5
+    y = run(x_d, w8_d, ex_d, S)
+    two = bf16_bits(bsf8.splitk_reduce(bsf8.gemm_partials(x_d, w8_d, ex_d, S)))
+    assert bsf8.device_status() == 0
+    assert np.array_equal(y, two)
+    rows = sorted({0, M // 2, M - 1})
+    assert_gemm_close(y[rows], oracle.gemm(x[rows], w8, ex), f"G={G} N={N} K={K} M={M} S={S}")
+
+
+def test_tensor_core_fold_output_alignment(bsf8_lib):
+    """y 2 bytes past an 8-byte boundary: the fold's stores take their scalar form and the
+    bits are those of an aligned y."""
+    wk, M, S = wl.MID, 64, 4
+    w8, ex = wk.weights()
+    x = wk.x(M=M)
+    w8_d, ex_d, x_d = dev(w8, ex, x)
+    n = M * wk.G * wk.N
+    buf = torch.empty(n + 4, dtype=torch.bfloat16, device="cuda")
+    y_odd = buf[1:n + 1].view(M, wk.G, wk.N)
+    assert y_odd.data_ptr() % 8 == 2
+    bsf8.gemm(x_d, w8_d, ex_d, split_k=S, out=y_odd)
+    ref = run(x_d, w8_d, ex_d, S)
+    assert bsf8.device_status() == 0
+    assert np.array_equal(bf16_bits(y_odd), ref)
+
+
 @pytest.mark.parametrize("M", [9, 16, 32, 64, 96, 128, 192])
 @pytest.mark.parametrize("S", [1, 2, 4])
 def test_tensor_core_kernel_mid_rows(bsf8_lib, M, S):
