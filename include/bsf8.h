@@ -118,11 +118,11 @@ int bsf8_dequant(const uint8_t *w8, const uint8_t *exp, void *out, int G, int N,
  *   workspace device scratch of at least bsf8_gemm_workspace_bytes(...) bytes, or
  *             NULL when that is 0: fp32 partials between the two passes, which the call
  *             runs when its kernel writes partials (the tensor-core kernel, M > 24, with
- *             more than one split -- past 192 rows at least ceil(K/1024) splits, as a
- *             token tile's accumulators must fit tensor memory; the other kernels when a
- *             slab of 16 rows needs more
- *             than 64 column tasks, e.g. split_k > 64).  No zeroing is needed; it must not
- *             be shared by calls that can overlap.
+ *             more than 8 splits, or 2..8 splits whose blocks take more than one wave of
+ *             the device's SMs -- past 192 rows at least ceil(K/2048) splits, as a token
+ *             tile's accumulators must fit tensor memory; the other kernels when a slab of
+ *             16 rows needs more than 64 column tasks, e.g. split_k > 64).  No zeroing is
+ *             needed; it must not be shared by calls that can overlap.
  * The splits are summed inside one thread block, across a cluster of up to 8 blocks (16
  * for the decode-ahead tensor-core kernel, where the device schedules such clusters)
  * through distributed shared memory, or by the fixed-order reduce of a second pass, always
