@@ -92,11 +92,13 @@ enum MainKernel {
     kKernelNone = -1, kKernelStream = 2, kKernelLowM = 4, kKernelUmma = 5, kKernelWide = 6, kKernelAhead = 7
 };
 
-// Above this many token rows the tensor-core kernel (tcgen05) runs: its MMAs are cheap
-// there, while the mma.sync kernels become bound by their MMA issue.  Measured on a GB300:
-// mid-row wo_a (G = 4, 1024 x 4096) at M = 64 takes 14 us against 35 us, at M = 192
-// 23 us against 92 us; at M = 16 the streaming kernel is ahead (9 us against 14 us).
-constexpr int kUmmaMinRows = 24;
+// Above this many token rows the tensor-core kernel (tcgen05) runs where the decode-ahead
+// tensor-core kernel does not: its MMAs are cheap there, while the mma.sync kernels become
+// bound by their MMA issue.  Measured on a GB300, mid rows (G = 4, 1024 x 4096): M = 20 / 24
+// 10.7 us against 15.6 streaming, M = 64 12 against 35, M = 192 14.5 against 91; at M = 9 /
+// 16 the streaming kernel is ahead (8.3 / 8.6 us against 11.7 / 10.6); the head-like weight
+// (32768 x 5120) at M = 20 / 24: 64 against 120 us.
+constexpr int kUmmaMinRows = 16;
 
 // Token rows the decode-ahead tensor-core kernel (bsf8_ahead.cu) serves by default from 9 up.
 constexpr int kAheadMaxRows = 32;
@@ -127,7 +129,7 @@ inline bool ahead_one_split(int M, int N, int K, int G) {
 inline int call_auto_split(int M, int N, int K, int G) {
     if (M <= 8) return 1;
     if (ahead_one_split(M, N, K, G)) return 1;
-    // 9..24 rows elsewhere: the streaming kernel (or, on wide weights, the tensor-core kernel
+    // 9..16 rows elsewhere: the streaming kernel (or, on wide weights, the tensor-core kernel
     // at one split); the streaming kernel cuts a split into tasks, and extra splits measured
     // no faster (mid G = 4, 1024 x 4096, M = 16: 8.7 us at 1, 2, 4 and 8 splits, 19 us at
     // the five a blocks-per-SM target gave)

@@ -117,7 +117,7 @@ int bsf8_dequant(const uint8_t *w8, const uint8_t *exp, void *out, int G, int N,
  *   split_k   0 = the library chooses (bsf8_gemm_auto_split), else 1 .. K/32
  *   workspace device scratch of at least bsf8_gemm_workspace_bytes(...) bytes, or
  *             NULL when that is 0: fp32 partials between the two passes, which the call
- *             runs when its kernel writes partials (the tensor-core kernel, M > 24, with
+ *             runs when its kernel writes partials (the tensor-core kernel, M > 16, with
  *             more than 8 splits, or 2..8 splits whose blocks take more than one wave of
  *             the device's SMs -- past 192 rows at least ceil(K/2048) splits, as a token
  *             tile's accumulators must fit tensor memory; the other kernels when a slab of
@@ -147,9 +147,10 @@ size_t bsf8_gemm_workspace_bytes(int M, int N, int K, int G, int split_k);
 /* The split count bsf8_gemm uses for split_k = 0.  Returns a value in 1 .. K/32, or a
  * negative status for invalid sizes.  1 up to 8 rows, and for 9..32 rows where the
  * decode-ahead tensor-core kernel takes the call in one split (its one-split grid fits the
- * device's SMs); otherwise for M <= 24 it depends on the sizes only (at most 8), for M > 24
- * (the tensor-core kernel) on the current device's SM count too.  With no device the
- * size-only rule applies. */
+ * device's SMs); otherwise 1 up to 16 rows, and past 16 (the tensor-core kernel) as many
+ * splits as keep its blocks in one wave of the current device's SMs, then enough that a
+ * split's accumulators fit tensor memory.  With no device, past 16 rows a size-only rule
+ * (at most 8) applies. */
 int bsf8_gemm_auto_split(int M, int N, int K, int G);
 
 /* Kernels of bsf8_gemm, as bsf8_gemm_kernel reports them and BSF8_OPT_GEMM_PATH forces them. */
@@ -324,9 +325,8 @@ enum {
                                    /*    fits one block an SM;                         */
                                    /*  - else 9..16 rows: the tensor-core kernel at    */
                                    /*    split_k 1 over at least one 128-row block per */
-                                   /*    SM, the streaming kernel otherwise (up to 24  */
-                                   /*    rows);                                        */
-                                   /*  - beyond 24 rows: the tensor-core kernel.       */
+                                   /*    SM, the streaming kernel otherwise;           */
+                                   /*  - beyond 16 rows: the tensor-core kernel.       */
                                    /* Else a BSF8_KERNEL_* value forces that kernel:   */
                                    /* 2 streaming (any call); 4 decode-ahead (M <= 8); */
                                    /* 5 tensor-core; 6 wide-weight (M <= 8; K and the  */

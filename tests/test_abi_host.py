@@ -133,11 +133,11 @@ def test_workspace_and_auto_split(lib):
     # wo_a one split sums its 8 tasks in the same left-to-right order as the page's 8 splits)
     assert lib.bsf8_gemm_auto_split(6, 1024, 4096, 2) == 1
     assert lib.bsf8_gemm_auto_split(6, 32768, 5120, 1) == 1
-    # 9..24 rows: one split too (the streaming and decode-ahead tensor-core kernels cut it
+    # 9..16 rows: one split too (the streaming and decode-ahead tensor-core kernels cut it
     # into column tasks; extra splits measured no faster on the streaming kernel)
     assert lib.bsf8_gemm_auto_split(12, 1024, 4096, 2) == 1
-    assert lib.bsf8_gemm_auto_split(24, 1024, 4096, 4) == 1
-    # past 24 rows, never more splits than 32-column blocks
+    assert lib.bsf8_gemm_auto_split(16, 1024, 4096, 4) == 1
+    # past 16 rows, never more splits than 32-column blocks
     assert lib.bsf8_gemm_auto_split(64, 32, 64, 1) == 2
     assert lib.bsf8_gemm_auto_split(0, 1024, 4096, 2) == -SHAPE
     for M in (1, 2, 8, 9, 64, 192):
