@@ -67,6 +67,7 @@ struct UmmaPlan {
     int S, chunk_cols, ntok, row_blocks, grid_x, ttiles;  // ttiles: token tiles of ntok rows
     int run_shift;  // log2 of the steps a tensor-memory accumulator takes (2, or 3: see bsf8_umma.cu)
     bool fold;      // 2..8 splits summed inside a cluster of the split blocks (no partials)
+    int sps;        // 128-column steps a ring stage holds (1 or 2)
     bool partials, tmem_ok, ok;  // ok: the kernel can run this call (else another kernel)
 };
 UmmaPlan plan_umma(int M, int N, int K, int G, int S, bool partials);

@@ -83,7 +83,8 @@ struct UmmaParams {
     float *partials;
     int M, N, K, G, S, chunk_cols, ntok;
     int to_partials;  // 1: store fp32 partials P[s] (even with one split), 0: store y
-    int ds, dc;       // stage (A slot + x tile) and codes ring depths
+    int ds, dc;       // stage (A slots + x tiles) and codes ring depths
+    int sps;          // 128-column steps a stage (and a codes slot) holds: 1 or 2
     int run_shift;    // a run (one accumulator) is 2^run_shift steps
     int cluster_fold; // 1: the S split blocks of a row block form a cluster and sum their
                       // splits through distributed shared memory into y (no partials)
@@ -272,11 +273,12 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64
 
 }  // namespace
 
+template <int SPS>  // 128-column steps a ring stage holds (1 or 2)
 __global__ void __launch_bounds__(kThreadsU, 2) umma_kernel(const __grid_constant__ UmmaParams p) {
     extern __shared__ uint8_t dyn_smem[];
     uint8_t *const base = dyn_smem + ((1024u - (smem_u32(dyn_smem) & 1023u)) & 1023u);
     uint8_t *const sX = base;                                   // ds x ntok x 256 B
-    uint8_t *const sC = sX + p.ds * p.ntok * 256;               // dc x 16 KB
+    uint8_t *const sC = sX + p.ds * p.sps * p.ntok * 256;       // dc x sps x 16 KB
     // full_c: a step's codes landed (TMA); empty_c: its rebuild read them (8 warps);
     // full_x: a step's x tile landed (TMA); full_s: the stage is ready for the MMAs (8 rebuild
     // warps, each after its part of A is in tensor memory; warp 2 after it also saw the x
@@ -299,7 +301,11 @@ __global__ void __launch_bounds__(kThreadsU, 2) umma_kernel(const __grid_constan
     const int nrun = (nkb + (1 << p.run_shift) - 1) >> p.run_shift;  // accumulators (runs of steps)
     const int xbytes = p.ntok * 256;  // a step's x tile: two 64-column atoms
     const int kDs = p.ds, kDc = p.dc;  // ring depths of this call
-    const uint32_t dbase = (uint32_t)(kDs * kACols);  // first accumulator column (A slots first)
+    constexpr int sps = SPS;           // steps a stage
+    const int nstg = (nkb + sps - 1) / sps;  // stages of the split
+    const int cslot = sps * kCodesBytes, xslot = sps * xbytes;  // bytes of a codes slot, an x stage
+    const uint32_t acols = (uint32_t)(sps * kACols);            // TMEM columns of a stage's A
+    const uint32_t dbase = (uint32_t)kDs * acols;  // first accumulator column (A slots first)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kDcMax; ++i) {
@@ -337,14 +343,19 @@ __global__ void __launch_bounds__(kThreadsU, 2) umma_kernel(const __grid_constan
             // a reciprocal sequence a step)
             int cs = 0;
             uint32_t ph = 0;
-            for (int kb = 0; kb < nkb; ++kb, cs = cs + 1 == kDc ? 0 : cs + 1, ph ^= cs == 0 ? 1u : 0u) {
-                if (kb >= kDc && !mbar_wait_bounded(&empty_c[cs], ph ^ 1u, p.timeout_ns)) {
+            for (int st = 0; st < nstg; ++st, cs = cs + 1 == kDc ? 0 : cs + 1, ph ^= cs == 0 ? 1u : 0u) {
+                if (st >= kDc && !mbar_wait_bounded(&empty_c[cs], ph ^ 1u, p.timeout_ns)) {
                     bad = true;
                     break;
                 }
-                mbar_arrive_expect_tx(&full_c[cs], (uint32_t)kCodesBytes);
+                const int ns = min(sps, nkb - st * sps);  // steps of this stage
+                mbar_arrive_expect_tx(&full_c[cs], (uint32_t)(ns * kCodesBytes));
                 if (!p.skip_loads)
-                    tma_2d_hint_u(sC + cs * kCodesBytes, &p.cmap, k0 + kb * kKB, g * p.N + row0, &full_c[cs], pol);
+#pragma unroll
+                    for (int j = 0; j < sps; ++j)
+                        if (j < ns)
+                            tma_2d_hint_u(sC + cs * cslot + j * kCodesBytes, &p.cmap, k0 + (st * sps + j) * kKB,
+                                          g * p.N + row0, &full_c[cs], pol);
                 ++n;
             }
             if (bad) {
@@ -364,16 +375,22 @@ __global__ void __launch_bounds__(kThreadsU, 2) umma_kernel(const __grid_constan
             bool bad = false;
             int ss = 0;
             uint32_t ph = 0;
-            for (int kb = 0; kb < nkb; ++kb, ss = ss + 1 == kDs ? 0 : ss + 1, ph ^= ss == 0 ? 1u : 0u) {
-                if (kb >= kDs && !mbar_wait_bounded(&empty_s[ss], ph ^ 1u, p.timeout_ns)) {
+            for (int st = 0; st < nstg; ++st, ss = ss + 1 == kDs ? 0 : ss + 1, ph ^= ss == 0 ? 1u : 0u) {
+                if (st >= kDs && !mbar_wait_bounded(&empty_s[ss], ph ^ 1u, p.timeout_ns)) {
                     bad = true;
                     break;
                 }
-                mbar_arrive_expect_tx(&full_x[ss], (uint32_t)xbytes);
-                if (!p.skip_loads) {
-                    tma_3d_u(sX + ss * xbytes, &p.xmap, k0 + kb * kKB, g, tok0, &full_x[ss]);
-                    tma_3d_u(sX + ss * xbytes + xbytes / 2, &p.xmap, k0 + kb * kKB + kHalf, g, tok0, &full_x[ss]);
-                }
+                const int ns = min(sps, nkb - st * sps);
+                mbar_arrive_expect_tx(&full_x[ss], (uint32_t)(ns * xbytes));
+                if (!p.skip_loads)
+#pragma unroll
+                    for (int j = 0; j < sps; ++j) {
+                        if (j >= ns) break;
+                        uint8_t *xt = sX + ss * xslot + j * xbytes;
+                        const int kc = k0 + (st * sps + j) * kKB;
+                        tma_3d_u(xt, &p.xmap, kc, g, tok0, &full_x[ss]);
+                        tma_3d_u(xt + xbytes / 2, &p.xmap, kc + kHalf, g, tok0, &full_x[ss]);
+                    }
                 ++n;
             }
             if (bad) {
@@ -395,20 +412,26 @@ __global__ void __launch_bounds__(kThreadsU, 2) umma_kernel(const __grid_constan
             bool bad = false;
             int ss = 0;
             uint32_t ph = 0;
-            for (int kb = 0; kb < nkb; ++kb, ss = ss + 1 == kDs ? 0 : ss + 1, ph ^= ss == 0 ? 1u : 0u) {
+            for (int st = 0; st < nstg; ++st, ss = ss + 1 == kDs ? 0 : ss + 1, ph ^= ss == 0 ? 1u : 0u) {
                 if (!mbar_wait_bounded(&full_s[ss], ph, p.timeout_ns)) {
                     bad = true;
                     break;
                 }
                 tc_after();
-                const uint32_t sb = smem_u32(sX + ss * xbytes);
-                const uint32_t ta = tmem + (uint32_t)(ss * kACols);
-                const uint32_t dcol = tmem + dbase + (uint32_t)((kb >> p.run_shift) * p.ntok);  // this run's accumulator
-                const bool run_start = (kb & ((1 << p.run_shift) - 1)) == 0;
+                const int ns = min(sps, nkb - st * sps);
 #pragma unroll
-                for (int ks = 0; ks < kKB / 16; ++ks) {  // x: atom column ks / 4, +32 bytes a K slice
-                    const uint64_t bd = sw128_desc(sb + (ks >> 2) * (xbytes / 2)) + 2 * (ks & 3);
-                    umma_ts(dcol, ta + 8u * (uint32_t)ks, bd, idesc, (!run_start || ks > 0) ? 1u : 0u);
+                for (int j = 0; j < sps; ++j) {
+                    if (j >= ns) break;
+                    const int kb = st * sps + j;
+                    const uint32_t sb = smem_u32(sX + ss * xslot + j * xbytes);
+                    const uint32_t ta = tmem + (uint32_t)ss * acols + (uint32_t)(j * kACols);
+                    const uint32_t dcol = tmem + dbase + (uint32_t)((kb >> p.run_shift) * p.ntok);  // this run's accumulator
+                    const bool run_start = (kb & ((1 << p.run_shift) - 1)) == 0;
+#pragma unroll
+                    for (int ks = 0; ks < kKB / 16; ++ks) {  // x: atom column ks / 4, +32 bytes a K slice
+                        const uint64_t bd = sw128_desc(sb + (ks >> 2) * (xbytes / 2)) + 2 * (ks & 3);
+                        umma_ts(dcol, ta + 8u * (uint32_t)ks, bd, idesc, (!run_start || ks > 0) ? 1u : 0u);
+                    }
                 }
                 umma_commit(&empty_s[ss]);
             }
@@ -444,57 +467,63 @@ __global__ void __launch_bounds__(kThreadsU, 2) umma_kernel(const __grid_constan
         bool bad = false;
         int cs = 0, ss = 0;          // ring slots, and the parities of their current uses
         uint32_t cph = 0, sph = 0;
-        for (int kb = 0; kb < nkb; ++kb, cs = cs + 1 == kDc ? 0 : cs + 1, cph ^= cs == 0 ? 1u : 0u,
+        for (int st = 0; st < nstg; ++st, cs = cs + 1 == kDc ? 0 : cs + 1, cph ^= cs == 0 ? 1u : 0u,
                  ss = ss + 1 == kDs ? 0 : ss + 1, sph ^= ss == 0 ? 1u : 0u) {
             if (!warp_wait(&full_c[cs], cph, p.timeout_ns) ||
-                (kb >= kDs && !warp_wait(&empty_s[ss], sph ^ 1u, p.timeout_ns))) {
+                (st >= kDs && !warp_wait(&empty_s[ss], sph ^ 1u, p.timeout_ns))) {
                 bad = true;
                 break;
             }
             tc_after();  // the MMAs that read this A slot have finished
-            const uint8_t *crow = sC + cs * kCodesBytes + row * 128;
-            uint32_t a[32];
+            const int ns = min(sps, nkb - st * sps);
 #pragma unroll
-            for (int b = 0; b < 2; ++b) {  // the warp's two 32-column blocks of the step
-                const int cb = 2 * part + b;   // block inside the step
-                const int kcol = k0 + kb * kKB + 32 * cb;
-                uint32_t ab[16];
-                if (rows_ok && kcol < k1) {    // warp-uniform
-                    // codes: 128-byte rows with the 128-byte swizzle (unit u of row r at u ^ r % 8)
-                    const uint4 c0 = *reinterpret_cast<const uint4 *>(crow + (((2 * cb) ^ (row & 7)) << 4));
-                    const uint4 c1 = *reinterpret_cast<const uint4 *>(crow + (((2 * cb + 1) ^ (row & 7)) << 4));
-                    const uint32_t e = erow[(kcol - k0) / 32];  // one exponent a warp
-                    if (e > 134u) {
-                        const uint32_t bb = e << 7;  // 2^(e-127)
-                        rebuild_block_u<true>(c0, c1, 0x7B807B80u, bb | (bb << 16), ab, mx);
+            for (int j = 0; j < sps; ++j) {
+                if (j >= ns) break;
+                const int kb = st * sps + j;
+                const uint8_t *crow = sC + cs * cslot + j * kCodesBytes + row * 128;
+                uint32_t a[32];
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {  // the warp's two 32-column blocks of the step
+                    const int cb = 2 * part + b;   // block inside the step
+                    const int kcol = k0 + kb * kKB + 32 * cb;
+                    uint32_t ab[16];
+                    if (rows_ok && kcol < k1) {    // warp-uniform
+                        // codes: 128-byte rows with the 128-byte swizzle (unit u of row r at u ^ r % 8)
+                        const uint4 c0 = *reinterpret_cast<const uint4 *>(crow + (((2 * cb) ^ (row & 7)) << 4));
+                        const uint4 c1 = *reinterpret_cast<const uint4 *>(crow + (((2 * cb + 1) ^ (row & 7)) << 4));
+                        const uint32_t e = erow[(kcol - k0) / 32];  // one exponent a warp
+                        if (e > 134u) {
+                            const uint32_t bb = e << 7;  // 2^(e-127)
+                            rebuild_block_u<true>(c0, c1, 0x7B807B80u, bb | (bb << 16), ab, mx);
+                        } else {
+                            const uint32_t bb = (e + 120u) << 7;  // 2^(e-7)
+                            rebuild_block_u<false>(c0, c1, bb | (bb << 16), 0u, ab, mx);
+                        }
                     } else {
-                        const uint32_t bb = (e + 120u) << 7;  // 2^(e-7)
-                        rebuild_block_u<false>(c0, c1, bb | (bb << 16), 0u, ab, mx);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) ab[i] = 0u;
                     }
-                } else {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) ab[i] = 0u;
+                    for (int i = 0; i < 16; ++i) a[16 * b + i] = ab[i];
                 }
-#pragma unroll
-                for (int i = 0; i < 16; ++i) a[16 * b + i] = ab[i];
+                tmem_st32(tlane + (uint32_t)ss * acols + (uint32_t)(j * kACols + 32 * part), a);
             }
-            tmem_st32(tlane + (uint32_t)(ss * kACols + 32 * part), a);
             tmem_wait_st();
             tc_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_c[cs]);
-            // The step's x tile must have landed before the MMAs read it: one warp sees to
+            // The stage's x tiles must have landed before the MMAs read them: one warp sees to
             // that (each wait costs its warp a few hundred cycles under the step's traffic),
-            // all of them on a ragged last step, whose tail they zero.
-            const bool tail_step = kb == nkb - 1 && tail != 0;
-            if ((warp == 2 || tail_step) && !warp_wait(&full_x[ss], sph, p.timeout_ns)) {
+            // all of them in the stage of a ragged last step, whose tail they zero.
+            const bool tail_stage = st == nstg - 1 && tail != 0;
+            if ((warp == 2 || tail_stage) && !warp_wait(&full_x[ss], sph, p.timeout_ns)) {
                 bad = true;
                 break;
             }
-            if (tail_step) {
+            if (tail_stage) {
                 // x columns past the split's end belong to the next split: zero them (the
                 // weights there are zero, and 0 * inf would be NaN); 16 units of 8 columns
-                uint8_t *xt = sX + ss * xbytes;
+                uint8_t *xt = sX + ss * xslot + (ns - 1) * xbytes;
                 const int fu = tail / 8, units = 16 - fu;
                 for (int i = threadIdx.x - 64; i < p.ntok * units; i += kRebuildWarps * 32) {
                     const int r = i / units, u = fu + i % units;
@@ -724,7 +753,7 @@ int umma_runs(const UmmaPlan &pl) {
 
 // Tensor memory a block's A slots (kACols columns each) and its runs' accumulators (ntok
 // columns each) take.
-int umma_tmem_need(const UmmaPlan &pl, int da) { return da * kACols + umma_runs(pl) * pl.ntok; }
+int umma_tmem_need(const UmmaPlan &pl, int da) { return da * std::max(1, pl.sps) * kACols + umma_runs(pl) * pl.ntok; }
 
 // SMs of the current device (0 without one), looked up once per device.
 int sm_count_u() {
@@ -742,6 +771,7 @@ int sm_count_u() {
 UmmaPlan plan_umma(int M, int N, int K, int G, int S, bool partials) {
     UmmaPlan pl{};
     pl.S = S;
+    pl.sps = 1;
     pl.chunk_cols = ((K / 32 + S - 1) / S) * 32;
     pl.ntok = std::min(kMaxTok, (M + 15) / 16 * 16);  // tokens a tile
     pl.ttiles = (M + pl.ntok - 1) / std::max(1, pl.ntok);
@@ -768,6 +798,15 @@ UmmaPlan plan_umma(int M, int N, int K, int G, int S, bool partials) {
     const long long blocks = (long long)pl.row_blocks * S * G * pl.ttiles;
     pl.fold = !partials && S >= 2 && S <= kMaxFold && blocks <= sm_count_u() &&
               !(pl.ntok <= 16 && umma_tmem_need(pl, 2) <= kTmemMax / 2);
+    // Two 128-column steps a stage for 17..128 tokens where two stages and two code slots of
+    // that size fit: every barrier handoff of the step chain (~300-400 cycles each, traced)
+    // then serves twice the work.
+    if (pl.tmem_ok && pl.ntok > 16 && pl.ntok <= 128 && (pl.chunk_cols + kKB - 1) / kKB >= 2) {
+        UmmaPlan p2 = pl;
+        p2.sps = 2;
+        if (umma_tmem_need(p2, 2) <= kTmemMax && 1024 + 2 * 2 * pl.ntok * 256 + 2 * 2 * kCodesBytes <= kSmemU)
+            pl.sps = 2;
+    }
     pl.partials = partials || (S > 1 && !pl.fold);
     pl.ok = M >= 1 && M <= kMaxRowsU && (long long)G * N < (1LL << 31) && K < (1 << 30) && pl.tmem_ok &&
             pl.chunk_cols / 32 <= kMaxSplitBlocks;
@@ -802,15 +841,18 @@ int umma_smem_budget(const UmmaPlan &pl) { return umma_two_per_sm(pl) ? 106 * 10
 int umma_stage_depth(const UmmaPlan &pl) {
     const bool two = umma_two_per_sm(pl);
     const int cap = two ? kTmemMax / 2 : kTmemMax;
-    const int xcap = std::max(2, (two ? 8 * 1024 : 144 * 1024) / (pl.ntok * 256));
+    const int xcap = std::max(2, (two ? 8 * 1024 : 144 * 1024) / (pl.sps * pl.ntok * 256));
+    const int left2 = umma_smem_budget(pl) - 1024 - 2 * pl.sps * kCodesBytes;  // two code slots kept
     int ds = 2;
-    while (ds < kDsMax && ds < xcap && umma_tmem_need(pl, ds + 1) <= cap) ++ds;
+    while (ds < kDsMax && ds < xcap && umma_tmem_need(pl, ds + 1) <= cap &&
+           (ds + 1) * pl.sps * pl.ntok * 256 <= left2)
+        ++ds;
     return ds;
 }
 
 int umma_codes_depth(const UmmaPlan &pl) {
-    const int left = umma_smem_budget(pl) - 1024 - umma_stage_depth(pl) * pl.ntok * 256;
-    return std::min(kDcMax, left / kCodesBytes);
+    const int left = umma_smem_budget(pl) - 1024 - umma_stage_depth(pl) * pl.sps * pl.ntok * 256;
+    return std::min(kDcMax, left / (pl.sps * kCodesBytes));
 }
 
 // Tensor memory a block allocates: a power of two of at least 32 columns.
@@ -845,6 +887,7 @@ cudaError_t launch_umma(const UmmaPlan &pl, const void *x, long long ldx, const 
     prm.to_partials = pl.partials ? 1 : 0;
     prm.cluster_fold = pl.fold ? 1 : 0;
     prm.ds = umma_stage_depth(pl);
+    prm.sps = pl.sps;
     prm.run_shift = pl.run_shift;
     prm.dc = umma_codes_depth(pl);
     prm.tcols = umma_tmem_cols(pl);
@@ -860,11 +903,13 @@ cudaError_t launch_umma(const UmmaPlan &pl, const void *x, long long ldx, const 
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!__atomic_load_n(&configured[dev], __ATOMIC_ACQUIRE)) {
-        e = cudaFuncSetAttribute(umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemU);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(umma_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 (int)cudaSharedmemCarveoutMaxShared);
-        if (e != cudaSuccess) return e;
+        for (const void *fn : {(const void *)umma_kernel<1>, (const void *)umma_kernel<2>}) {
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemU);
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     (int)cudaSharedmemCarveoutMaxShared);
+            if (e != cudaSuccess) return e;
+        }
         __atomic_store_n(&configured[dev], 1, __ATOMIC_RELEASE);
     }
     cudaLaunchConfig_t cfg = {};
@@ -888,7 +933,7 @@ cudaError_t launch_umma(const UmmaPlan &pl, const void *x, long long ldx, const 
     }
     cfg.attrs = attrs;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, umma_kernel, prm);
+    return pl.sps == 2 ? cudaLaunchKernelEx(&cfg, umma_kernel<2>, prm) : cudaLaunchKernelEx(&cfg, umma_kernel<1>, prm);
 }
 
 }  // namespace bsf8
