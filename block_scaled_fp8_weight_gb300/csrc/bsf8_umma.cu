@@ -1,5 +1,5 @@
 // bsf8_umma.cu -- the tensor-core (tcgen05) GEMM: weight rows stream in, are rebuilt to
-// bf16 in shared memory and multiplied by the fifth-generation tensor cores.
+// bf16 straight into tensor memory and multiplied by the fifth-generation tensor cores.
 //
 //   y[m][g][n] = bf16( sum_{s=0..S-1} P[s][m][g][n] ),  summed s = 0, 1, ... in fp32,
 //   W[g][n][k] = bf16( e4m3(w8[g][n][k]) * 2^(exp[g][n/32][k/32] - 127) ).
@@ -10,30 +10,32 @@
 // A block owns 128 weight rows (a row block of one group), the columns of one split and a
 // tile of up to 192 token rows (calls with more rows run one tile a grid z-index, each
 // rebuilding the weights it streams: past a few hundred rows the product is bound by the
-// tensor cores, not by the weight stream).
-// Per 128-column step:
-//   * one copy warp loads the step's codes (128 rows x 128 bytes, one TMA box, up to 8 steps
-//     ahead, before the dependency wait too), another the step's x tile (the token rows,
-//     zero-filled to a multiple of 16, x 128 columns, two boxes of 64 with the 128-byte
-//     swizzle), each wait loop on a warp of its own;
+// tensor cores, not by the weight stream).  The work moves in ring stages of one or two
+// 128-column steps (two for 17..128 tokens where they fit: each barrier handoff then serves
+// twice the work).  Per stage:
+//   * one copy warp loads the stage's codes (per step 128 rows x 128 bytes, one TMA box; up
+//     to 8 stages ahead, before the dependency wait too), another its x tiles (per step the
+//     token rows, zero-filled to a multiple of 16, x 128 columns, two boxes of 64 with the
+//     128-byte swizzle), each wait loop on a warp of its own;
 //   * eight rebuild warps turn the codes into exact bf16 weights -- the rebuild of
 //     bsf8_device.cuh -- and store them straight into tensor memory as the MMA's A operand
 //     (thread = weight row = TMEM lane, two bf16 a column; the two warps of a TMEM lane
-//     quarter take 64 columns each);
-//   * one thread of the MMA warp issues eight tcgen05.mma (M = 128, N = tokens, K = 16; A in
-//     tensor memory, x from shared memory) into an fp32 accumulator in tensor memory and
-//     commits them to the barriers that free the step's A and x slots.
+//     quarter take 64 columns of each step);
+//   * one thread of the MMA warp issues eight tcgen05.mma a step (M = 128, N = tokens,
+//     K = 16; A in tensor memory, x from shared memory) into an fp32 accumulator in tensor
+//     memory and commits them to the barrier that frees the stage.
 // A in tensor memory rather than shared memory: at 192 tokens a step moved ~190 KB through
 // shared memory (the copies, the codes read, A written and read, x read), which bound the
 // step at ~1500 cycles against 768 of tensor-core work; A in tensor memory takes 64 KB off.
 // At the end the rebuild warps read the accumulators back (tcgen05.ld, thread = weight row;
-// two warps a TMEM lane quarter split the token columns) and store y (one split) or the
-// split's fp32 partials (the fixed-order reduce follows).
-// Codes, A and x slots are rings with full/empty mbarriers; every wait is bounded, and on
+// two warps a TMEM lane quarter split the token columns) and store y (one split), the
+// split's sums into shared memory for the cluster of split blocks to fold (2..8 splits in
+// one wave), or the split's fp32 partials (the fixed-order reduce follows).
+// Codes and stages are rings with full/empty mbarriers; every wait is bounded, and on
 // timeout the block records BSF8_ERR_TIMEOUT, stores nothing and returns.
 //
-// The weights are static, so their copies and the rebuild of the first steps run before the
-// programmatic-dependent-launch wait; x is read and y written after it.
+// The weights are static, so their copies and the rebuild of the first stages run before
+// the programmatic-dependent-launch wait; x is read and y written after it.
 #include "bsf8_device.cuh"
 #include "bsf8_internal.h"
 
