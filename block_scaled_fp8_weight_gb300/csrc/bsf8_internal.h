@@ -61,8 +61,9 @@ cudaError_t launch_stream(const StreamPlan &plan, const void *x, long long ldx, 
                           cudaStream_t stream, bool rows_exp = false);
 
 // Tensor-core kernel (bsf8_umma.cu): 128-row blocks, one split and one token tile (up to 192
-// rows) a block.  With more than one split it writes fp32 partials (the fixed-order reduce
-// follows).
+// rows) a block.  With more than one split the split blocks of a row block sum in a cluster
+// (2..8 splits whose blocks fit one wave), else it writes fp32 partials (the fixed-order
+// reduce follows).
 struct UmmaPlan {
     int S, chunk_cols, ntok, row_blocks, grid_x, ttiles;  // ttiles: token tiles of ntok rows
     int run_shift;  // log2 of the steps a tensor-memory accumulator takes (2, or 3: see bsf8_umma.cu)
