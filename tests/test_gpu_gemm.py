@@ -76,7 +76,7 @@ def test_integer_data_is_exact(bsf8_lib):
 
 # ------------------------------------------------------------ tolerance cases
 
-def check(wk, M, S, ldx_pad=0, rows=None, n_range=None, literal=False):
+def check(wk, M, S, ldx_pad=0, rows=None, n_range=None, n_blocks=None, literal=False):
     w8, ex = wk.weights()
     x = wk.x(M=M)
     if ldx_pad:
@@ -89,6 +89,11 @@ def check(wk, M, S, ldx_pad=0, rows=None, n_range=None, literal=False):
         n0, n1 = n_range
         y = y[:, :, n0:n1]
         w8, ex = w8[:, n0:n1], ex[:, n0 // 32:n1 // 32]
+    if n_blocks is not None:         # and/or whole 32-row blocks of weight rows
+        b = np.asarray(n_blocks)
+        n = (32 * b[:, None] + np.arange(32)[None, :]).reshape(-1)
+        y = y[:, :, n]
+        w8, ex = w8[:, n], ex[:, b]
     ref = oracle.gemm(x, w8, ex)
     return assert_gemm_close(y, ref, f"{wk.name} M={M} S={S}", literal=literal)
 
@@ -124,9 +129,13 @@ def test_gate_up_sweep(bsf8_lib, M):
     check(wl.GATE_UP, M, 0, rows=rows)
 
 
-@pytest.mark.parametrize("M", [1, 6, 12, 16, 128])
+@pytest.mark.parametrize("M", [1, 3, 6, 8, 12, 16, 128])
 def test_head_sweep_sampled(bsf8_lib, M):
-    rows = sorted({0, M - 1})
+    """The head-like weight across the kernels' row ranges (wide-weight up to 8 rows):
+    three token rows against the oracle on 64 blocks of 32 weight rows spread evenly over
+    all 1024 (so that every SM's share of the rows is sampled) and on the last 2048 rows."""
+    rows = sorted({0, M // 2, M - 1})
+    check(wl.HEAD, M, 0, rows=rows, n_blocks=np.linspace(0, 1023, 64).round().astype(int))
     check(wl.HEAD, M, 0, rows=rows, n_range=(32768 - 2048, 32768))
 
 
