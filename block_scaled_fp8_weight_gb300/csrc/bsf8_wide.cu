@@ -76,6 +76,8 @@ constexpr int kWBadWords = kWMaxBlocks / 32;
 constexpr int kWFastLo = 16, kWFastHi = 200;  // exponent bytes of the f16 path
 constexpr int kWSmin = -100, kWSmax = 100;    // token scales of the f16 path
 static_assert(kWMaxChunk / kWStepK <= 32, "one step word a lane");
+// up to 8 token rows: one consumer warp a row in the x scan, tokens rotated mod 8 at a task's end
+static_assert(kWWarps == 8, "eight consumer warps, eight token rows");
 // dynamic shared memory at most (18 KB of the 227 KB are left to the static arrays):
 // alignment slack, the ring and the f16 x of the token rows
 constexpr size_t kWSmemMax = 227 * 1024 - 18 * 1024;
@@ -232,6 +234,42 @@ __device__ __forceinline__ int row_scale(uint32_t mx, bool &ok) {
     return ok ? s : 0;
 }
 
+// The 64-byte block at shared address base as 16 bf16 pairs: w[i] = columns (2i, 2i + 1).
+__device__ __forceinline__ void load_block64(uint32_t base, uint32_t (&w)[16]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint4 v = lds128(base + 16 * j);
+        w[4 * j] = v.x;
+        w[4 * j + 1] = v.y;
+        w[4 * j + 2] = v.z;
+        w[4 * j + 3] = v.w;
+    }
+}
+
+// Writes block blk of a token row (its bf16 pairs w, read from base) back to base as f16
+// x' = x * 2^-s_m in the MMA B layout, s_m from the row's largest magnitude bits smax, and
+// sets bit blk of bad when some non-zero |x| of the block is below 2^(s_m - 17) (x' not
+// exact) or s_m is out of the f16 path's range.
+__device__ __forceinline__ void convert_block64(const uint32_t (&w)[16], uint32_t base, uint32_t smax, int blk,
+                                                uint32_t *bad) {
+    bool rok;
+    const int sm = row_scale(smax, rok);
+    const float sc = exp2_int(-sm);
+    const uint32_t thr1 = ((uint32_t)(sm + 110) << 7) - 1u;  // |x| >= 2^(s-17); s >= -100
+    uint32_t o[16];
+    uint32_t mn = 0xFFFFFFFFu;  // per half: smallest magnitude minus one (zero -> 0xFFFF)
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        mn = min_u16x2(mn, ((w[i] | 0x80008000u) - 0x00010001u) ^ 0x80008000u);
+        o[i] = pack_f16x2(__uint_as_float(w[i] << 16) * sc, __uint_as_float(w[i] & 0xFFFF0000u) * sc);
+    }
+    // the 16 bytes at 16q: columns 4q .. 4q + 3 (pairs 2q, 2q + 1) and 16 + 4q ..
+    // 16 + 4q + 3 (pairs 8 + 2q, 9 + 2q)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) sts128(base + 16 * q, o[2 * q], o[2 * q + 1], o[8 + 2 * q], o[9 + 2 * q]);
+    if (!rok || min(mn & 0xFFFFu, mn >> 16) < thr1) atomicOr(&bad[blk >> 5], 1u << (blk & 31));
+}
+
 // Converts the split's x (token rows 0 .. M-1, columns [k0, k0 + 32 cb) of group g) into
 // f16 x' at xh (rows pitch bytes apart; inside each 32-column block of 64 bytes, the 16
 // bytes at 16q hold columns 4q .. 4q + 3 and 16 + 4q .. 16 + 4q + 3, the MMA B operand of
@@ -269,26 +307,21 @@ __device__ bool convert_x(const WideParams &p, uint32_t xh, int g, int k0, int c
         consumers_sync();
         return false;
     }
-    // pass 1: each row's largest magnitude (bf16 magnitudes order as integers)
-    uint32_t mx[kWWarps];
-#pragma unroll
-    for (int m = 0; m < kWWarps; ++m) mx[m] = 0;
-    for (int v = tid; v < nvec; v += kWWarps * 32) {
-#pragma unroll
-            for (int m = 0; m < kWWarps; ++m)
-                if (m < p.M) {
-                    const uint4 u = lds128(xh + (uint32_t)(m * p.pitch + 16 * v));
-                    mx[m] = max_u16x2(mx[m], max_u16x2(max_u16x2(u.x & 0x7FFF7FFFu, u.y & 0x7FFF7FFFu),
-                                                       max_u16x2(u.z & 0x7FFF7FFFu, u.w & 0x7FFF7FFFu)));
-                }
+    // pass 1: each row's largest magnitude (bf16 magnitudes order as integers), one warp a
+    // row, so that the rows' loads and shuffle chains run side by side
+    if ((tid >> 5) < p.M) {
+        const uint32_t row = xh + (uint32_t)((tid >> 5) * p.pitch);
+        uint32_t mx = 0;
+#pragma unroll 4
+        for (int v = lane; v < nvec; v += 32) {
+            const uint4 u = lds128(row + 16u * (uint32_t)v);
+            mx = max_u16x2(mx, max_u16x2(max_u16x2(u.x & 0x7FFF7FFFu, u.y & 0x7FFF7FFFu),
+                                         max_u16x2(u.z & 0x7FFF7FFFu, u.w & 0x7FFF7FFFu)));
         }
-#pragma unroll
-    for (int m = 0; m < kWWarps; ++m) {
-        if (m >= p.M) break;
-        uint32_t v = max(mx[m] & 0xFFFFu, mx[m] >> 16);
+        uint32_t v = max(mx & 0xFFFFu, mx >> 16);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-        if (lane == 0 && v) atomicMax(&s_max[m], v);
+        if (lane == 0) s_max[tid >> 5] = v;
     }
     consumers_sync();
     // pass 2: convert each row's 64-byte blocks in place, one thread a (row, block); a block
@@ -297,34 +330,24 @@ __device__ bool convert_x(const WideParams &p, uint32_t xh, int g, int k0, int c
         bool ok;
         s_sx[tid] = row_scale(s_max[tid], ok);
     }
-    for (int u = tid; u < p.M * cb; u += kWWarps * 32) {
-        const int m = u / cb, blk = u - m * cb;
-        bool rok;
-        const int sm = row_scale(s_max[m], rok);
-        const float sc = exp2_int(-sm);
-        const uint32_t thr1 = ((uint32_t)(sm + 110) << 7) - 1u;  // |x| >= 2^(s-17); s >= -100
-        const uint32_t base = xh + (uint32_t)(m * p.pitch + 64 * blk);
-        uint32_t w[16];  // bf16 pairs: columns (2i, 2i + 1) of the block
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint4 v = lds128(base + 16 * j);
-            w[4 * j] = v.x;
-            w[4 * j + 1] = v.y;
-            w[4 * j + 2] = v.z;
-            w[4 * j + 3] = v.w;
+    // Units u = tid + 256 j in pairs (j even, j + 1), both blocks' loads ahead of either's
+    // arithmetic.
+    const int nu = p.M * cb, ustride = kWWarps * 32;
+    for (int u0 = tid; u0 < nu; u0 += 2 * ustride) {
+        const int u1 = u0 + ustride;
+        const int m0 = u0 / cb, b0 = u0 - m0 * cb;
+        const uint32_t base0 = xh + (uint32_t)(m0 * p.pitch + 64 * b0);
+        uint32_t w0[16], w1[16];
+        load_block64(base0, w0);
+        if (u1 < nu) {
+            const int m1 = u1 / cb, b1 = u1 - m1 * cb;
+            const uint32_t base1 = xh + (uint32_t)(m1 * p.pitch + 64 * b1);
+            load_block64(base1, w1);
+            convert_block64(w0, base0, s_max[m0], b0, s_bad);
+            convert_block64(w1, base1, s_max[m1], b1, s_bad);
+        } else {
+            convert_block64(w0, base0, s_max[m0], b0, s_bad);
         }
-        uint32_t o[16];
-        uint32_t mn = 0xFFFFFFFFu;  // per half: smallest magnitude minus one (zero -> 0xFFFF)
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            mn = min_u16x2(mn, ((w[i] | 0x80008000u) - 0x00010001u) ^ 0x80008000u);
-            o[i] = pack_f16x2(__uint_as_float(w[i] << 16) * sc, __uint_as_float(w[i] & 0xFFFF0000u) * sc);
-        }
-        // the 16 bytes at 16q: columns 4q .. 4q + 3 (pairs 2q, 2q + 1) and 16 + 4q ..
-        // 16 + 4q + 3 (pairs 8 + 2q, 9 + 2q)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) sts128(base + 16 * q, o[2 * q], o[2 * q + 1], o[8 + 2 * q], o[9 + 2 * q]);
-        if (!rok || min(mn & 0xFFFFu, mn >> 16) < thr1) atomicOr(&s_bad[blk >> 5], 1u << (blk & 31));
     }
     if (tid >= p.M && tid < kWWarps) s_sx[tid] = 0;
     consumers_sync();
@@ -636,7 +659,7 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
             __threadfence_block();
             if (!*(volatile int *)&s_err) {
                 const int n = rb * kWRows + lane;  // lane = row of the task
-                for (int m = 0; m < p.M; ++m) {
+                auto sum_store = [&](int m) {
                     float v = red[rs][0][lane][m];
 #pragma unroll
                     for (int ww = 1; ww < kWWarps; ++ww) v += red[rs][ww][lane][m];
@@ -644,6 +667,18 @@ __global__ void __launch_bounds__(kWThreads, 1) wide_kernel(const __grid_constan
                         p.partials[(((size_t)s * p.M + m) * p.G + g) * p.N + n] = v;
                     else
                         p.y[((size_t)m * p.G + g) * p.N + n] = f32_to_bf16_rn(v);
+                };
+                if (p.M >= 4) {
+                    // tokens in a lane-rotated order: in iteration j lane quad k takes token
+                    // (j + k) mod 8, so an iteration's loads hit 32 distinct banks (token by
+                    // token they hit four, eight ways each); the sum order is the same
+#pragma unroll 1
+                    for (int j = 0; j < kWWarps; ++j) {
+                        const int m = (j + (lane >> 2)) & (kWWarps - 1);
+                        if (m < p.M) sum_store(m);
+                    }
+                } else {
+                    for (int m = 0; m < p.M; ++m) sum_store(m);
                 }
             }
             __syncwarp();
